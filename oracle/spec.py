@@ -1,0 +1,157 @@
+"""Layer-skip self-drafting, chain / tree verification and the round loop (oracle).
+
+Test infrastructure only.
+
+A round at committed length s with last emitted token t0 (not yet in the
+cache), following the self-speculative decoding page (m.lqnn.cn/news/278124,
+§2.1, §3.3, §4.2, §4.3):
+
+1. draft: k passes of layers [0, L) with one row each, t0 at position s
+   then d_1 .. d_{k-1} at s+1 .., each through the final norm and the shared
+   LM head; d_{j+1} = argmax (greedy) or a draw from q_j = softmax(logits/T).
+   Each pass writes layers [0, L) of the cache at its slot.
+2. one more first-L pass on d_k at position s+k, without the LM head.  The
+   page sends k+1 rows through the upper layers but drafts only k tokens;
+   this pass is the plainest way to give the verifier the layer-L hidden
+   state of every row while the first-L KV of all k+1 rows comes from the
+   draft (KV reuse, §2.1).
+3. verify: layers [L, N) on the k+1 hidden rows at positions s .. s+k, each
+   row seeing the committed context plus the rows before it (causal), then
+   final norm and LM head: k+1 target rows.
+4. accept (accept.py), 5. commit: length s + a + 1.
+
+Tree verification (FlashSpec page, lnrk.cn/news/47842, §2.2, §3.2, §4.1,
+§5.2): the nodes go in level order, node i at position s + depth(i) in slot
+s + i, each seeing the committed context, its ancestors and itself (padding
+and siblings masked).  The page's "parent offset + 1" rule is the depth; its
+remark that depth ids broke its outputs concerns a target trained with
+injected position ids, which a plain target does not have.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .accept import (accept_greedy_chain, accept_greedy_tree, argmax_lowest,
+                     commit_chain, commit_tree_moves, apply_moves, int_weights,
+                     sample_index, tree_depths)
+from .decoder import softmax
+
+
+def draft(dec, cache, s, t0, k, temp=0.0, u_draft=None):
+    """Layer-skip draft at committed length ``s`` from token ``t0``.
+
+    Returns ``(draft_tokens[k], h_L[k+1, d], draft_logits[k, V], q[k, V] or None)``.
+    ``q`` (float32 softmax at ``temp``) is returned in sampling mode only,
+    where ``u_draft[j]`` drives the draw of d_{j+1}.
+    """
+    L = dec.shape.exit_layer
+    toks, hs, lgs, qs = [], [], [], []
+    cur = int(t0)
+    for j in range(k + 1):
+        h = dec.embed([cur])
+        vis = [np.arange(0, s + j + 1)]
+        h = dec.run_layers(h, 0, L, [s + j], [s + j], vis, cache)
+        hs.append(h[0])
+        if j == k:
+            break
+        lg = dec.logits(h)[0]
+        lgs.append(lg)
+        if temp == 0.0:
+            cur = argmax_lowest(lg)
+        else:
+            q = softmax(lg / temp).astype(np.float32)
+            qs.append(q)
+            cur = sample_index(int_weights(q), u_draft[j])
+        toks.append(cur)
+    lgs = np.stack(lgs) if lgs else np.zeros((0, dec.shape.vocab))
+    return toks, np.stack(hs), lgs, (np.stack(qs) if qs else None)
+
+
+def chain_visibility(s, T):
+    return [np.arange(0, s + t + 1) for t in range(T)]
+
+
+def tree_visibility(s, parents):
+    vis = []
+    for i in range(len(parents)):
+        anc = [i]
+        while parents[anc[-1]] >= 0:
+            anc.append(int(parents[anc[-1]]))
+        vis.append(np.concatenate([np.arange(0, s), s + np.array(sorted(anc))]))
+    return vis
+
+
+def verify(dec, cache, s, h_in, lo, parents=None):
+    """Layers ``[lo, N)`` over rows ``h_in [T, d]`` in slots ``s .. s+T-1``.
+
+    Chain when ``parents`` is None (positions s+t, causal), else a
+    level-order tree (positions s + depth, ancestor-only visibility).
+    Returns the target logits ``[T, V]``.
+    """
+    T = h_in.shape[0]
+    slots = s + np.arange(T)
+    if parents is None:
+        pos, vis = slots, chain_visibility(s, T)
+    else:
+        pos, vis = s + tree_depths(parents), tree_visibility(s, parents)
+    h = dec.run_layers(np.asarray(h_in, dtype=np.float64), lo, dec.n_layers, pos, slots, vis, cache)
+    return dec.logits(h)
+
+
+def decode_step(dec, cache, token):
+    """One plain autoregressive step: all layers on ``token`` at the committed end."""
+    s = cache.length
+    h = dec.run_layers(dec.embed([token]), 0, dec.n_layers, [s], [s], [np.arange(0, s + 1)], cache)
+    cache.length = s + 1
+    return dec.logits(h)[0]
+
+
+def generate_greedy_ar(dec, prompt, n_new, max_ctx=None):
+    """Plain greedy decoding: the first ``n_new`` tokens after ``prompt``."""
+    cache = dec.new_cache(max_ctx or (len(prompt) + n_new + 1))
+    out = [argmax_lowest(dec.prefill(cache, prompt))]
+    while len(out) < n_new:
+        out.append(argmax_lowest(decode_step(dec, cache, out[-1])))
+    return out
+
+
+def spec_round_greedy(dec, cache, t0, k):
+    """One greedy chain round; returns ``(emitted, a, next, target_logits)``."""
+    s = cache.length
+    L = dec.shape.exit_layer
+    d, hL, _, _ = draft(dec, cache, s, t0, k)
+    logits = verify(dec, cache, s, hL, L)
+    a, nxt = accept_greedy_chain(d, logits)
+    cache.length = commit_chain(s, a)
+    return list(d[:a]) + [nxt], a, nxt, logits
+
+
+def generate_greedy_spec(dec, prompt, n_new, k, max_ctx=None, log=None):
+    """Greedy self-speculative decoding; equals :func:`generate_greedy_ar`.
+
+    ``log`` (a list) receives ``(s, a)`` per round.
+    """
+    cache = dec.new_cache(max_ctx or (len(prompt) + n_new + k + 2))
+    t0 = argmax_lowest(dec.prefill(cache, prompt))
+    out = [t0]
+    while len(out) < n_new:
+        s = cache.length
+        emitted, a, t0, _ = spec_round_greedy(dec, cache, t0, k)
+        out += emitted
+        if log is not None:
+            log.append((s, a))
+    return out[:n_new]
+
+
+def tree_round_greedy(dec, cache, tokens, parents):
+    """Greedy tree round over level-order ``tokens`` (all layers from the embedding).
+
+    Returns ``(depth, node, path, next, logits)`` and commits the path.
+    """
+    s = cache.length
+    logits = verify(dec, cache, s, dec.embed(tokens), 0, parents)
+    depth, node, path, nxt = accept_greedy_tree(tokens, parents, logits)
+    moves, new_len = commit_tree_moves(s, path)
+    apply_moves(cache, moves)
+    cache.length = new_len
+    return depth, node, path, nxt, logits

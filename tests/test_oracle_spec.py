@@ -1,0 +1,166 @@
+"""Pins of the oracle's draft / verify / round loop on the tiny fp32 model.
+
+* greedy self-speculative output equals plain greedy decoding token for token
+  (self-speculative decoding page, §5.2: the lossless check);
+* an all-accepted round emits k+1 tokens and a first-position rejection
+  emits exactly one (same page, §2.1);
+* the draft's first-L KV equals a full forward's first-L KV (KV reuse, §2.1);
+* the draft logits are the layer-L hidden state through the final norm and
+  LM head of a full forward;
+* after many rounds a fresh prefill of the committed tokens reproduces every
+  committed KV row and the write pointer equals the committed count (§3.3);
+* a tree with unit branching verifies exactly like a chain.
+"""
+import numpy as np
+import pytest
+
+from oracle import spec as S
+from oracle.accept import accept_greedy_chain, accept_greedy_tree, argmax_lowest
+from synthetic import SHAPES, ModelShape, make_tokens, make_weights, weights_to_numpy, tree_parents
+from oracle.decoder import Decoder
+
+
+PROMPT_LEN, N_NEW = 32, 64
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    shape = SHAPES["tiny"]
+    return Decoder(shape, weights_to_numpy(make_weights(shape, seed=1)))
+
+
+@pytest.fixture(scope="module")
+def prompt():
+    return make_tokens(PROMPT_LEN, SHAPES["tiny"].vocab, seed=1)
+
+
+@pytest.fixture(scope="module")
+def ar_tokens(tiny, prompt):
+    return S.generate_greedy_ar(tiny, prompt, N_NEW)
+
+
+@pytest.mark.parametrize("k", [1, 4, 7])
+def test_greedy_spec_equals_greedy_ar(tiny, prompt, ar_tokens, k):
+    log = []
+    out = S.generate_greedy_spec(tiny, prompt, N_NEW, k, log=log)
+    assert out == ar_tokens
+    assert all(0 <= a <= k for _, a in log)
+
+
+def test_greedy_spec_equals_ar_deeper_draft():
+    shape = ModelShape(4, 64, 4, 2, 16, 128, 96, 2, "f32", init_std=0.2)
+    dec = Decoder(shape, weights_to_numpy(make_weights(shape, seed=8)))
+    pr = make_tokens(10, shape.vocab, seed=8)
+    ar = S.generate_greedy_ar(dec, pr, 40)
+    log = []
+    assert S.generate_greedy_spec(dec, pr, 40, 3, log=log) == ar
+    assert any(a > 0 for _, a in log)        # the 2-of-4-layer draft is kept sometimes
+
+
+def _planted_round(dec, prompt, draft_tokens, k):
+    cache = dec.new_cache(PROMPT_LEN + k + 4)
+    t0 = argmax_lowest(dec.prefill(cache, prompt))
+    s = cache.length
+    L = dec.shape.exit_layer
+    hs = []
+    for j, tok in enumerate([t0] + list(draft_tokens)):
+        h = dec.run_layers(dec.embed([tok]), 0, L, [s + j], [s + j], [np.arange(s + j + 1)], cache)
+        hs.append(h[0])
+    logits = S.verify(dec, cache, s, np.stack(hs), L)
+    return accept_greedy_chain(draft_tokens, logits)
+
+
+def test_round_bounds(tiny, prompt, ar_tokens):
+    k = 4
+    a, nxt = _planted_round(tiny, prompt, ar_tokens[1:k + 1], k)
+    assert a == k and nxt == ar_tokens[k + 1]                # k + 1 tokens emitted
+    bad = list(ar_tokens[1:k + 1])
+    bad[0] = (bad[0] + 1) % tiny.shape.vocab
+    a, nxt = _planted_round(tiny, prompt, bad, k)
+    assert a == 0 and nxt == ar_tokens[1]                    # exactly one token emitted
+
+
+def test_draft_kv_and_logits_match_full_forward(tiny, prompt):
+    k = 3
+    cache = tiny.new_cache(PROMPT_LEN + k + 2)
+    t0 = argmax_lowest(tiny.prefill(cache, prompt))
+    s = cache.length
+    d, hL, dlog, _ = S.draft(tiny, cache, s, t0, k)
+    seq = np.concatenate([prompt, [t0], d])
+    ref = tiny.new_cache(len(seq))
+    L = tiny.shape.exit_layer
+    n = len(seq)
+    h = tiny.run_layers(tiny.embed(seq), 0, L, np.arange(n), np.arange(n),
+                        [np.arange(t + 1) for t in range(n)], ref)
+    for l in range(L):
+        np.testing.assert_allclose(cache.k[l][:n], ref.k[l][:n], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(cache.v[l][:n], ref.v[l][:n], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(hL, h[s:s + k + 1], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(dlog, tiny.logits(h[s:s + k]), rtol=1e-10, atol=1e-12)
+    assert d == [argmax_lowest(r) for r in tiny.logits(h[s:s + k])]
+
+
+def test_committed_kv_matches_fresh_prefill(tiny, prompt):
+    k = 4
+    cache = tiny.new_cache(PROMPT_LEN + N_NEW + k + 2)
+    t0 = argmax_lowest(tiny.prefill(cache, prompt))
+    committed = list(prompt)
+    for _ in range(10):
+        s = cache.length
+        emitted, a, nxt, _ = S.spec_round_greedy(tiny, cache, t0, k)
+        committed += [t0] + emitted[:-1]
+        assert cache.length == s + a + 1 == len(committed)   # write pointer == committed length
+        t0 = nxt
+    fresh = tiny.new_cache(len(committed))
+    tiny.prefill(fresh, np.array(committed))
+    n = len(committed)
+    for l in range(tiny.n_layers):
+        np.testing.assert_allclose(cache.k[l][:n], fresh.k[l][:n], rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(cache.v[l][:n], fresh.v[l][:n], rtol=1e-9, atol=1e-11)
+
+
+def test_unit_branching_tree_is_chain(tiny, prompt):
+    k = 4
+    toks = make_tokens(k + 1, tiny.shape.vocab, seed=3)
+    c1, c2 = tiny.new_cache(PROMPT_LEN + 8), tiny.new_cache(PROMPT_LEN + 8)
+    tiny.prefill(c1, prompt)
+    tiny.prefill(c2, prompt)
+    s = c1.length
+    chain = S.verify(tiny, c1, s, tiny.embed(toks), 0)
+    tree = S.verify(tiny, c2, s, tiny.embed(toks), 0, tree_parents([1] * k))
+    np.testing.assert_array_equal(chain, tree)
+
+
+def test_tree_rows_see_only_ancestors(tiny, prompt):
+    """Changing a node's token changes only the rows of its subtree."""
+    par = tree_parents([2, 2])
+    toks = make_tokens(7, tiny.shape.vocab, seed=4)
+    c1, c2 = tiny.new_cache(PROMPT_LEN + 8), tiny.new_cache(PROMPT_LEN + 8)
+    tiny.prefill(c1, prompt)
+    tiny.prefill(c2, prompt)
+    s = c1.length
+    a = S.verify(tiny, c1, s, tiny.embed(toks), 0, par)
+    t2 = toks.copy()
+    t2[1] = (t2[1] + 5) % tiny.shape.vocab          # node 1 has children 3, 4
+    b = S.verify(tiny, c2, s, tiny.embed(t2), 0, par)
+    changed = [i for i in range(7) if not np.array_equal(a[i], b[i])]
+    assert changed == [1, 3, 4]
+
+
+def test_tree_round_commit(tiny, prompt):
+    par = tree_parents([2, 2])
+    cache = tiny.new_cache(PROMPT_LEN + 10)
+    t0 = argmax_lowest(tiny.prefill(cache, prompt))
+    ar = S.generate_greedy_ar(tiny, prompt, 4)
+    toks = make_tokens(7, tiny.shape.vocab, seed=5)
+    toks[0] = t0
+    toks[2] = ar[1]        # plant: node 2 (depth 1) and its child 6 (depth 2) on the greedy path
+    toks[6] = ar[2]
+    s = cache.length
+    depth, node, path, nxt, logits = S.tree_round_greedy(tiny, cache, toks, par)
+    assert (depth, node, path, nxt) == (2, 6, [0, 2, 6], ar[3])
+    assert cache.length == s + 3
+    fresh = tiny.new_cache(s + 3)
+    tiny.prefill(fresh, np.concatenate([prompt, [t0, ar[1], ar[2]]]))
+    for l in range(tiny.n_layers):
+        np.testing.assert_allclose(cache.k[l][:s + 3], fresh.k[l][:s + 3], rtol=1e-9, atol=1e-11)
