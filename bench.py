@@ -1,0 +1,348 @@
+"""Benchmark: layer-skip self-speculative greedy rounds on the 7B-shaped model.
+
+Workload (one step = one whole round of the verification path):
+  7B-shaped Llama decoder (32 layers, d 4096, 32 heads x 128, FFN 11008,
+  vocab 32000), bf16 random-init N(0, 0.02) weights (13.5 GB), draft = first
+  12 layers + LM head, verify = layers 12..31 reusing the draft's KV, chain
+  k = 4, committed context 4096 per sequence (a seeded synthetic KV context,
+  standing in for a prefilled random prompt), greedy acceptance, batch 1 (or
+  --batch 8).  A round = spec_draft (k+1 first-12-layer passes, k LM heads) +
+  spec_verify (layers 12..31 over k+1 rows, LM head, fused greedy acceptance)
+  + kv_commit; the next round starts from the emitted token.
+
+Metric: verified candidate tokens/s (k+1 per sequence per round, over the
+whole round time) -- with accepted tokens/s, the verify-step-only rate and the
+HBM roofline fraction of the dominant kernel (the tcgen05 GEMM) alongside.
+Weights and KV (> L2) are re-streamed every round, so no L2 flush is needed.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified candidate tokens/s and accepted tokens/s @1 GB300; % HBM roofline"
+WORKLOAD = "llama7b-shape layer-skip self-spec (draft 12/32 layers), chain k=4, ctx 4096, greedy"
+K_DRAFT, CTX, SEED = 4, 4096, 4
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (sampled round, scaled)
+def oracle_round_sample(batch, budget_s=20.0):
+    """Time the float64 oracle on a bounded sample of one round and scale it.
+
+    Sample: one decoder layer of the 7B shape with 1 row (a draft pass) and
+    with k+1 rows (a verify pass) over a 4096-token context, and the LM head
+    with 1 and k+1 rows.  A round is 5 x 12 one-row layer passes + 4 one-row
+    heads + 20 (k+1)-row layer passes + one (k+1)-row head per sequence.
+    Returns (seconds per round for ``batch`` sequences, sample description,
+    threads).
+    """
+    import numpy as np
+    import dataclasses
+    import torch
+    from synthetic import SHAPES, make_weights, weights_to_numpy, make_kv_context
+    from oracle.decoder import Decoder
+    shape = dataclasses.replace(SHAPES["llama7b"], n_layers=1, exit_layer=0)
+    w = weights_to_numpy(make_weights(shape, SEED, device="cpu"))
+    dec = Decoder(shape, w)
+    k, v = make_kv_context(shape, 1, CTX, SEED, device="cpu")
+    cache = dec.new_cache(CTX + K_DRAFT + 2)
+    cache.load(k[:, 0].float().numpy(), v[:, 0].float().numpy())
+    rng = np.random.default_rng(0)
+
+    def layer(rows):
+        h = rng.standard_normal((rows, shape.d_model)) * 0.02
+        pos = CTX + np.arange(rows)
+        vis = [np.arange(CTX + r + 1) for r in range(rows)]
+        t = time.perf_counter()
+        dec.layer(0, h, pos, pos, vis, cache)
+        return time.perf_counter() - t
+
+    def head(rows):
+        h = rng.standard_normal((rows, shape.d_model))
+        t = time.perf_counter()
+        dec.logits(h)
+        return time.perf_counter() - t
+
+    t1, t5, h1, h5 = layer(1), layer(K_DRAFT + 1), head(1), head(K_DRAFT + 1)
+    per_seq = (K_DRAFT + 1) * 12 * t1 + K_DRAFT * h1 + 20 * t5 + h5
+    threads = torch.get_num_threads()
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        threads = max([i.get("num_threads", 1) for i in info] + [1])
+    except Exception:
+        pass
+    desc = (f"one 7B-shape layer at 1 and {K_DRAFT + 1} rows and the LM head at 1 and {K_DRAFT + 1} rows "
+            f"over a {CTX}-token context, scaled to a round (5x12 + 20 layer passes, 5 heads)")
+    return per_seq * batch, desc, threads
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cores = os.cpu_count()
+    times = []
+    desc, threads = "", cores
+    for i in range(args.warmup + args.steps):
+        t, desc, threads = oracle_round_sample(args.batch)
+        if i >= args.warmup:
+            times.append(t)
+    per_round = statistics.mean(times)
+    cand = args.batch * (K_DRAFT + 1)
+    val = cand / per_round
+    line = {
+        "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_round * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random weights and KV context)",
+        "config": {"workload": WORKLOAD, "batch": args.batch, "k": K_DRAFT, "ctx": CTX},
+        "impl": "reference",
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decoding_verify_04_gb300 import spec
+    from synthetic import SHAPES, make_weights, make_kv_context, make_tokens
+
+    shape = SHAPES["llama7b"]
+    B, k = args.batch, K_DRAFT
+    steps, warm = args.steps, args.warmup
+    grow = (steps + warm + 2) * (k + 1) + 8
+    w = make_weights(shape, SEED + rank, device="cuda")
+    model = spec.Model(shape, w, max_rows=max(64, B * (k + 1)), max_batch=B, max_position=CTX + grow + 64)
+    del w
+    torch.cuda.empty_cache()
+    kv = spec.KVCache(model, B, CTX + grow)
+    for b in range(B):
+        kc, vc = make_kv_context(shape, 1, CTX, SEED * 1000 + rank * 100 + b, device="cuda")
+        kv.import_rows(b, 0, kc[:, 0].contiguous(), vc[:, 0].contiguous())
+        del kc, vc
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    kv.set_lengths([CTX] * B)
+
+    t0 = torch.from_numpy(make_tokens(B, shape.vocab, SEED, "t0")).cuda()
+    cand = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
+    hL = torch.empty((B, k + 1, shape.d_model), dtype=torch.float32, device="cuda")
+    acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    ev_v0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev_v1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    acc_log = torch.zeros((steps, B), dtype=torch.int32, device="cuda")
+
+    def step(i=None):
+        spec.spec_draft(model, kv, t0, k, cand, hL)
+        if i is not None:
+            ev_v0[i].record(stream)
+        spec.spec_verify(model, kv, [k + 1] * B, cand, k + 1, h_in=hL, h_stride=k + 1, acc_len=acc, next_tok=nxt)
+        if i is not None:
+            ev_v1[i].record(stream)
+            acc_log[i].copy_(acc)
+        spec.kv_commit(kv, acc)
+        t0.copy_(nxt)
+
+    for _ in range(warm):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = Clocks(local)
+    clocks.start()
+    model.profile(True)
+    n_launch0 = model.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    model.profile(False)
+    launches = model.launch_count() - n_launch0
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    verify_ms = sum(ev_v0[i].elapsed_time(ev_v1[i]) for i in range(steps)) / steps
+    accepted = int(acc_log.sum().item())
+    g_ms, g_bytes, g_n = model.profile_read(0)
+    a_ms, _, a_n = model.profile_read(1)
+    err = model.device_error()
+    if err:
+        raise SystemExit(f"device error word {err} set during the bench")
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+
+    # e2e: the same rounds through the public API with the round's input (t0)
+    # copied in from pinned host memory and its result read back each step
+    t0_host = torch.empty(B, dtype=torch.int32).pin_memory()
+    res_host = torch.empty((B, k + 3), dtype=torch.int32).pin_memory()
+    t0_host.copy_(t0.cpu())
+    res_dev = torch.empty((B, k + 3), dtype=torch.int32, device="cuda")
+    e_steps = max(3, steps // 2)
+    torch.cuda.synchronize()
+    tw0 = time.perf_counter()
+    for _ in range(e_steps):
+        t0.copy_(t0_host, non_blocking=True)
+        spec.spec_draft(model, kv, t0, k, cand, hL)
+        spec.spec_verify(model, kv, [k + 1] * B, cand, k + 1, h_in=hL, h_stride=k + 1, acc_len=acc, next_tok=nxt)
+        spec.kv_commit(kv, acc)
+        res_dev[:, :k + 1].copy_(cand)
+        res_dev[:, k + 1].copy_(acc)
+        res_dev[:, k + 2].copy_(nxt)
+        res_host.copy_(res_dev, non_blocking=True)
+        torch.cuda.synchronize()
+        t0_host.copy_(res_host[:, k + 2])
+    e2e_s = (time.perf_counter() - tw0) / e_steps
+    e2e_val = world * B * (k + 1) / e2e_s
+
+    hbm, peak_kind = peaks()
+    cand_per_step = B * (k + 1)
+    value = world * cand_per_step * steps / (ms / 1e3)
+    g_avg_ms = g_ms / max(g_n, 1)
+    g_avg_bytes = g_bytes / max(g_n, 1)
+    achieved = g_avg_bytes / (g_avg_ms / 1e3) / 1e9 if g_n else None
+    # verify step algorithmic bytes: layers 12..31 + LM head weights + KV of layers 12..31 read once
+    d, F, V = shape.d_model, shape.d_ff, shape.vocab
+    layer_w = (3 * d * d + d * d + 2 * F * d + d * F) * 2
+    ctx_now = CTX + (warm + steps) * 1  # at least one token per round
+    kv_bytes = 20 * 2 * shape.n_kv_heads * shape.head_dim * 2 * (CTX + k + 1) * B
+    verify_bytes = 20 * layer_w + V * d * 2 + kv_bytes
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm,
+        "ms_per_step": ms / steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded random-init weights and KV context; no dataset)",
+        "config": {"workload": WORKLOAD, "batch": B, "k": k, "ctx": CTX, "exit_layer": 12, "n_layers": 32,
+                   "l2": "inputs larger than L2 (13.5 GB weights re-streamed each round)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "accepted_tokens_per_s": world * (accepted + B * steps) / (ms / 1e3),
+        "acceptance_rate": accepted / (B * steps * k),
+        "verify_ms": verify_ms,
+        "verify_candidate_tokens_per_s": world * cand_per_step / (verify_ms / 1e3),
+        "verify_hbm_gbs": verify_bytes / (verify_ms / 1e3) / 1e9,
+        "verify_hbm_frac": verify_bytes / (verify_ms / 1e3) / 1e9 / hbm,
+        "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel (tcgen05 skinny GEMM, all launches in the timed region)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": (achieved / hbm) if achieved else None, "traffic": None,
+                     "peak_source": peak_kind, "launches": g_n, "avg_launch_us": g_avg_ms * 1e3,
+                     "avg_launch_bytes": g_avg_bytes},
+        "attention": {"launches": a_n, "total_ms_per_step": a_ms / steps},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,
+                "d2h_bytes_per_step": 4 * B * (k + 3)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sec, desc, thr = oracle_round_sample(B)
+        line["cpu_baseline"] = {"value": cand_per_step / sec, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

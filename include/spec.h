@@ -1,0 +1,282 @@
+/*
+ * spec.h -- C ABI of libspec.so, the GB300 (sm_103a) verification path of
+ * speculative decoding with layer-skip self-drafting.
+ *
+ * What the calls compute (one round at committed length s, last emitted
+ * token t0 not yet in the cache):
+ *   spec_draft   k+1 passes of layers [0, L) (one row per sequence each):
+ *                t0, d_1, ..., d_k at positions s .. s+k; the first k passes
+ *                go through the final RMSNorm and the shared LM head and
+ *                pick d_{j+1} = argmax.  Writes layers [0, L) of the KV cache
+ *                and returns the layer-L hidden state of all k+1 rows
+ *                ("self-speculative decoding" page, m.lqnn.cn/news/278124,
+ *                section 2.1 layer skip and KV reuse, section 4.2 draft stage).
+ *   spec_verify  layers [L, N) over the candidate rows -- a chain (row j sees
+ *                the context and rows 0..j) or a level-order token tree (a
+ *                node sees the context, its ancestors and itself; position id
+ *                s + depth) -- then final norm and LM head; optionally fused
+ *                greedy acceptance (same page, sections 2.1, 4.3; FlashSpec
+ *                page, lnrk.cn/news/47842, sections 2.2, 3.2, 4.1, 5.2).
+ *   spec_accept  rejection sampling: keep x with probability min(1, p/q),
+ *                else draw from max(0, p - q) normalised (p when that is all
+ *                zero); all kept -> bonus draw from the last target row
+ *                (self-speculative decoding page, sections 2.4 and 4.3).
+ *   kv_commit    keep the accepted rows, drop the rest: length s + a + 1,
+ *                tree paths compacted into consecutive slots (same page,
+ *                sections 3.3 and 4.5; FlashSpec page, section 4.1).
+ *   spec_schedule_k  confidence-scheduled draft length (DSpark page,
+ *                0539edu.com/news/4524681, sections 2.2 and 2.3).
+ *
+ * Conventions
+ *   - Every pointer argument documented "device" is a CUDA device pointer
+ *     on the current device; "host" is ordinary host memory.  The caller owns
+ *     every buffer it passes; the library only borrows it for the call (or,
+ *     for asynchronous calls, until the work on `stream` completes).
+ *   - The library owns the packed weights (spec_model), the KV cache and
+ *     lengths (spec_kv) and its internal workspaces.  Calls on one model
+ *     must be ordered on one stream: the workspaces are shared.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls
+ *     marked "async" only enqueue work; calls marked "sync" return after the
+ *     stream has drained.
+ *   - Return value: SPEC_OK (0) or a negative SPEC_ERR_* code; the message
+ *     of the last error on the calling thread is spec_last_error().  No C++
+ *     exception crosses the ABI.  Errors found on the device (token id out of
+ *     range, KV capacity exceeded, a bounded wait that ran out) set the
+ *     model's device error word, read and cleared by spec_device_error().
+ *   - Layouts are row-major; "[a][b]" means b is contiguous.
+ */
+#ifndef SPEC_H
+#define SPEC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_OK               0
+#define SPEC_ERR_ARG         -1   /* bad argument (null, size, range)           */
+#define SPEC_ERR_CAPACITY    -2   /* rows, batch or context beyond the limits   */
+#define SPEC_ERR_CUDA        -3   /* a CUDA runtime call failed                 */
+#define SPEC_ERR_DEVICE      -4   /* device error word was set                  */
+#define SPEC_ERR_UNSUPPORTED -5   /* shape or mode this build does not handle   */
+
+#define SPEC_DTYPE_F32  0
+#define SPEC_DTYPE_BF16 1
+
+/* device error word bits (spec_device_error) */
+#define SPEC_DEVERR_TOKEN     1   /* a token id outside [0, vocab)              */
+#define SPEC_DEVERR_CAPACITY  2   /* a row slot at or beyond the KV capacity    */
+#define SPEC_DEVERR_TIMEOUT   4   /* a bounded pipeline wait ran out            */
+#define SPEC_DEVERR_POSITION  8   /* a position id beyond the rotary table      */
+
+typedef struct spec_model spec_model;
+typedef struct spec_kv spec_kv;
+
+/* Llama-style decoder: RMSNorm, rotate-half RoPE, GQA attention, SwiGLU FFN,
+ * untied LM head, no biases.  Limits of this build: head_dim in {64, 128};
+ * n_heads a multiple of n_kv_heads; d_model, n_heads*head_dim and d_ff
+ * multiples of 64; bf16 weights run on the tcgen05 tensor-core GEMM, f32
+ * weights on a CUDA-core GEMM. */
+typedef struct spec_model_config {
+    int32_t n_layers;      /* N                                                  */
+    int32_t d_model;       /* d                                                  */
+    int32_t n_heads;       /* H query heads                                      */
+    int32_t n_kv_heads;    /* Hkv                                                */
+    int32_t head_dim;      /* hd                                                 */
+    int32_t d_ff;          /* F                                                  */
+    int32_t vocab;         /* V                                                  */
+    int32_t exit_layer;    /* L: the draft runs layers [0, L), 0 <= L < N        */
+    int32_t dtype;         /* SPEC_DTYPE_F32 or SPEC_DTYPE_BF16 (all weights)    */
+    int32_t max_rows;      /* most candidate rows of all sequences in one call   */
+    int32_t max_batch;     /* most sequences in one call                         */
+    int32_t max_position;  /* every position id must be < max_position           */
+    float   rms_eps;       /* RMSNorm epsilon                                    */
+    float   rope_theta;    /* RoPE base                                          */
+} spec_model_config;
+
+/* Per-row summary of a target logits row. */
+typedef struct spec_row_stats {
+    float   top1;          /* largest logit                                      */
+    float   top2;          /* second largest logit (another index)               */
+    float   sum_exp;       /* sum over the vocabulary of exp(logit - top1)       */
+    int32_t argmax;        /* lowest index holding top1                          */
+} spec_row_stats;
+
+/* Order of the weight pointers given to spec_model_create. */
+#define SPEC_W_EMBED       0   /* [V][d]                                   */
+#define SPEC_W_LM_HEAD     1   /* [V][d]                                   */
+#define SPEC_W_FINAL_NORM  2   /* [d]                                      */
+#define SPEC_W_LAYER0      3   /* then 9 per layer l at 3 + 9*l + j:       */
+#define SPEC_WL_ATTN_NORM  0   /* [d]                                      */
+#define SPEC_WL_Q          1   /* [H*hd][d]                                */
+#define SPEC_WL_K          2   /* [Hkv*hd][d]                              */
+#define SPEC_WL_V          3   /* [Hkv*hd][d]                              */
+#define SPEC_WL_O          4   /* [d][H*hd]                                */
+#define SPEC_WL_FFN_NORM   5   /* [d]                                      */
+#define SPEC_WL_GATE       6   /* [F][d]                                   */
+#define SPEC_WL_UP         7   /* [F][d]                                   */
+#define SPEC_WL_DOWN       8   /* [d][F]                                   */
+#define SPEC_W_COUNT(n_layers) (3 + 9 * (n_layers))
+
+/* Bounds of the confidence-scheduled draft length (DSpark page, 2.2-2.3). */
+typedef struct spec_k_schedule {
+    int32_t min_k, max_k;  /* clamp range of k                                   */
+    double  low, high;     /* confidence thresholds mapped to min_k and max_k    */
+    double  decay;         /* EMA decay of the acceptance rate                   */
+} spec_k_schedule;
+
+/* Last error message of the calling thread ("" if none).  The string stays
+ * valid until the next failing call on the same thread. */
+const char* spec_last_error(void);
+
+/* Number of SMs and compute capability of the current device (sync). */
+int spec_device_info(int32_t* num_sms, int32_t* cc_major, int32_t* cc_minor);
+
+/* Create a model on the current device from weights in the order of
+ * SPEC_W_* (`weights`: host array of SPEC_W_COUNT(n_layers) device
+ * pointers, each tensor of cfg->dtype, row-major [out][in]).  The library
+ * packs them into its own memory (fused Q|K|V rows, gate/up rows
+ * interleaved in blocks of 64), builds the rotary tables and workspaces, and
+ * synchronises `stream` before returning: the caller may free its copies
+ * afterwards.  sync.  Errors: ARG (null / non-positive sizes), UNSUPPORTED
+ * (outside the limits above), CUDA (allocation or copy failed). */
+int spec_model_create(const spec_model_config* cfg, const void* const* weights,
+                      void* stream, spec_model** out);
+void spec_model_destroy(spec_model* m);
+
+/* Read and clear the model's device error word (SPEC_DEVERR_* bits). sync. */
+int spec_device_error(spec_model* m, int32_t* host_bits);
+
+/* KV cache for `batch` sequences of up to `max_ctx` slots each, every layer,
+ * K and V, in the model dtype: layout [layer][seq][kv_head][slot][hd]
+ * (one allocation, never grown).  Lengths start at 0.  sync. */
+int spec_kv_create(spec_model* m, int32_t batch, int32_t max_ctx, spec_kv** out);
+void spec_kv_destroy(spec_kv* kv);
+
+/* Committed lengths: set from / copy to host int32 [batch].  sync. */
+int spec_kv_set_lengths(spec_kv* kv, const int32_t* host_len, void* stream);
+int spec_kv_get_lengths(spec_kv* kv, int32_t* host_len, void* stream);
+
+/* Copy KV rows between the cache and a device buffer laid out
+ * [n_layers][n_slots][Hkv][hd] in the model dtype, for sequence `seq`,
+ * layers [layer0, layer0+n_layers), slots [slot0, slot0+n_slots).  Used to
+ * load a synthetic committed context and to inspect the cache.  Lengths
+ * are not changed.  async. */
+int spec_kv_import(spec_kv* kv, int32_t seq, int32_t layer0, int32_t n_layers,
+                   int32_t slot0, int32_t n_slots, const void* k, const void* v,
+                   void* stream);
+int spec_kv_export(spec_kv* kv, int32_t seq, int32_t layer0, int32_t n_layers,
+                   int32_t slot0, int32_t n_slots, void* k, void* v, void* stream);
+
+/* Causal pass of all layers over `n` prompt tokens (device int32 [n]) of
+ * sequence `seq`, appended at its committed length, which then grows by n.
+ * Optional outputs for the last row: `last_logits` (device f32 [V]) and
+ * `next_tok` (device int32 [1], its argmax).  async. */
+int spec_prefill(spec_model* m, spec_kv* kv, int32_t seq, const int32_t* tokens,
+                 int32_t n, float* last_logits, int32_t* next_tok, void* stream);
+
+/* Greedy layer-skip draft for sequences [0, batch) with draft length k.
+ *   t0       device int32 [batch]    last emitted token of each sequence
+ *   cand     device int32 [batch][k+1]  out: cand[b][0] = t0[b], cand[b][j] = d_j
+ *   h_L      device f32 [batch][k+1][d] out: layer-L residual state of each row
+ *   draft_logits device f32 [batch][k][V] out, nullable: the k draft rows
+ * Writes KV layers [0, L) at slots s_b .. s_b+k; lengths unchanged.  async.
+ * Requires exit_layer >= 1. */
+int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0, int32_t k,
+               int32_t* cand, float* h_L, float* draft_logits, void* stream);
+
+/* Verification forward of the candidate rows of sequences [0, batch).
+ *   n_rows   host int32 [batch]: rows of sequence b (chain: k_b+1; tree:
+ *            node count).  Sum <= max_rows, each <= 64.
+ *   h_in     device f32 [batch][h_stride][d]: layer-L state of each row (from
+ *            spec_draft); the forward runs layers [L, N).  NULL: rows are
+ *            embedded from `tokens` and the forward runs layers [0, N).
+ *   tokens   device int32 [batch][tok_stride]: row tokens (row 0 = t0, then
+ *            the draft tokens or tree nodes in level order).
+ *   tree_parent  host int32 [n_rows[0]] parent of each node (parent[0] = -1,
+ *            parent[i] < i), shared by all sequences; NULL = chain.
+ *   logits   device f32 [sum n_rows][V], nullable: target logits.
+ *   stats    device spec_row_stats [sum n_rows], nullable.
+ *   acc_len, next_tok  device int32 [batch], nullable (both or neither):
+ *            fused greedy acceptance -- chain: leading draft tokens equal to
+ *            the previous row's argmax; tree: deepest node whose whole path
+ *            matches (ties to the lowest node index); next_tok = argmax of
+ *            the last accepted row.
+ *   path     device int32 [batch][64]: accepted rows root first (tree mode
+ *            with fused acceptance; nullable in chain mode).
+ * Writes KV of the forward's layers at slots s_b .. s_b+n_rows[b]-1; lengths
+ * unchanged.  async. */
+int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows,
+                const float* h_in, int32_t h_stride, const int32_t* tokens,
+                int32_t tok_stride, const int32_t* tree_parent, float* logits,
+                spec_row_stats* stats, int32_t* acc_len, int32_t* next_tok,
+                int32_t* path, void* stream);
+
+/* Rejection-sampling acceptance of a chain (no model needed).
+ *   p      device f32 [batch][k+1][vocab]  target probabilities
+ *   q      device f32 [batch][k][vocab]    draft probabilities
+ *   draft  device int32 [batch][k]         draft tokens
+ *   u      device f32 [batch][k+1]         uniforms, each m * 2^-24, m in [0, 2^24)
+ *   acc_len, next_tok  device int32 [batch] out
+ * Ratio test u_j * q_j(x) < p_j(x) exactly (q_j(x) = 0 rejects); the draw
+ * (residual max(0, p - q) in f32, or p when that is all zero, or the bonus
+ * row p_k) is an integer inverse CDF over w = floor(r * 2^32) driven by
+ * u[k].  Bit-exact and deterministic.  async. */
+int spec_accept(const float* p, const float* q, const int32_t* draft, const float* u,
+                int32_t batch, int32_t k, int32_t vocab, int32_t* acc_len,
+                int32_t* next_tok, void* stream);
+
+/* Greedy acceptance from target logits (the unfused form of spec_verify's
+ * fused acceptance).  logits device f32 [batch][n_rows][vocab]; tokens device
+ * int32 [batch][n_rows]; tree_parent host int32 [n_rows] or NULL (chain);
+ * path device int32 [batch][64], nullable in chain mode.  async. */
+int spec_accept_greedy(const float* logits, const int32_t* tokens,
+                       const int32_t* tree_parent, int32_t batch, int32_t n_rows,
+                       int32_t vocab, int32_t* acc_len, int32_t* next_tok,
+                       int32_t* path, void* stream);
+
+/* Commit the accepted rows of sequences [0, batch): acc_len device int32
+ * [batch].  Chain (path NULL): length s_b + acc_len[b] + 1.  Tree: path
+ * device int32 [batch][path_stride] (root first) -- the rows of depth
+ * 1..acc_len[b] move from slot s_b + path[b][d] to slot s_b + d in every
+ * layer, then the length becomes s_b + acc_len[b] + 1.  async. */
+int kv_commit(spec_kv* kv, int32_t batch, const int32_t* acc_len, const int32_t* path,
+              int32_t path_stride, void* stream);
+
+/* Probabilities of the two largest logits of each row, from row summaries:
+ * out[2r] = 1 / sum_exp, out[2r+1] = exp(top2 - top1) / sum_exp (float64).
+ * stats device [rows]; out device f64 [rows][2].  async. */
+int spec_row_probs(const spec_row_stats* stats, int32_t rows, double* out, void* stream);
+
+/* Confidence-scheduled draft length, one round, sequences [0, batch):
+ *   top_probs device f64 [sum n_rows][2]: top-1 and top-2 target probabilities
+ *            of every verified row (spec_row_probs)
+ *   n_rows   host int32 [batch]: k_b + 1 rows of sequence b (k_b >= 1)
+ *   acc_len  device int32 [batch]; ema device f64 [batch] (updated in place)
+ *   k_next   device int32 [batch] out; conf device f64 [batch] out, nullable
+ * acceptance = a/k_b; ema = decay*ema + (1-decay)*acceptance;
+ * conf = 0.4*mean(top1) + 0.3*min(5*mean(top1 - top2), 1) + 0.3*ema;
+ * k_next = clamp(trunc(min_k + (max_k-min_k)*(conf-low)/(high-low)), min_k, max_k).
+ * Float64 with one rounding per written operation, left to right, no
+ * contraction; means are left-to-right sums divided by the count.  async. */
+int spec_schedule_k(const double* top_probs, const int32_t* n_rows, const int32_t* acc_len,
+                    double* ema, int32_t batch, const spec_k_schedule* sch, int32_t* k_next,
+                    double* conf, void* stream);
+
+/* Tracing.  spec_profile(m, 1) starts a fresh record: from then on every GEMM
+ * and attention launch of this model is bracketed by CUDA events on its
+ * stream, with the launch's algorithmic bytes (weights once, activation rows
+ * in and out).  spec_profile(m, 0) stops recording.  spec_profile_read sums
+ * the recorded launches of one kind (0 GEMM, 1 attention): total device
+ * milliseconds, bytes and launch count; sync.  spec_launch_count returns the
+ * number of kernels this model has launched since it was created. */
+int spec_profile(spec_model* m, int32_t enable);
+int spec_profile_read(spec_model* m, int32_t kind, double* total_ms, double* bytes, int32_t* launches);
+int spec_launch_count(spec_model* m, int64_t* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_H */

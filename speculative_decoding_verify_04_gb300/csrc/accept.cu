@@ -1,0 +1,333 @@
+// Acceptance, KV commit and draft-length scheduling kernels.
+//
+// Rejection sampling ("self-speculative decoding" page, m.lqnn.cn/news/278124,
+// section 2.4 and the acceptance routine of section 4.3): draft token x at
+// position j is kept with probability min(1, p_j(x)/q_j(x)) -- zero when
+// q_j(x) = 0 -- tested as u_j * q_j(x) < p_j(x), exact in float64 because the
+// product of two float32 values has at most 48 significant bits.  At the first
+// rejection the correction is drawn from max(0, p_j - q_j) (clipped, section
+// 5.2), or from p_j when that residual is all zero; when all k are kept a bonus
+// token is drawn from p_k.  "Draw" is an integer inverse CDF so the result is
+// bit-exact on any machine: w_x = floor(r_x * 2^32) (an exact power-of-two
+// scaling of a float32), S = sum w (exact in 64 bits), t = floor(m * S / 2^24)
+// for the uniform u = m * 2^-24, and the token is the smallest x whose inclusive
+// prefix sum of w exceeds t.
+#include <algorithm>
+
+#include "model.cuh"
+#include "stats.cuh"
+
+namespace spec {
+
+constexpr int kAcceptThreads = 256;
+constexpr int kAcceptWarps = kAcceptThreads / 32;
+constexpr int kStep = 128;                 // elements per warp step (32 lanes x 4)
+constexpr int kMaxSteps = 64;              // steps per warp segment (V <= 8*64*128 = 65536)
+
+SPEC_DEV unsigned long long weight_of(float r) {
+    return __float2ull_rz(r * 4294967296.0f);     // r in [0,1]: exact scaling, then floor
+}
+
+SPEC_DEV float row_value(const float* p, const float* q, int x, int mode) {
+    // mode 0: residual max(0, p - q); 1: p
+    if (mode == 0) return fmaxf(__fsub_rn(p[x], q[x]), 0.f);
+    return p[x];
+}
+
+__global__ void __launch_bounds__(kAcceptThreads)
+accept_sample_kernel(const float* __restrict__ p, const float* __restrict__ q, const int* __restrict__ draft,
+                     const float* __restrict__ u, int k, int V, int* acc_len, int* next_tok) {
+    __shared__ unsigned long long step_sum[kAcceptWarps][kMaxSteps];
+    __shared__ unsigned long long warp_tot[kAcceptWarps];
+    __shared__ int s_a, s_mode, s_tok;
+    const int b = blockIdx.x, t = threadIdx.x, w = t >> 5, lane = t & 31;
+
+    if (w == 0) {
+        bool rej = false;
+        if (lane < k) {
+            const int x = draft[(size_t)b * k + lane];
+            if (x < 0 || x >= V) {
+                rej = true;
+            } else {
+                const float qx = q[((size_t)b * k + lane) * V + x];
+                const float px = p[((size_t)b * (k + 1) + lane) * V + x];
+                const float uj = u[(size_t)b * (k + 1) + lane];
+                rej = !(qx > 0.f && (double)uj * (double)qx < (double)px);
+            }
+        }
+        const unsigned mask = __ballot_sync(0xffffffffu, rej);
+        if (lane == 0) {
+            s_a = mask ? (__ffs(mask) - 1) : k;
+            s_mode = (s_a < k) ? 0 : 1;
+        }
+    }
+    __syncthreads();
+    const int a = s_a;
+    const float* pr = p + ((size_t)b * (k + 1) + a) * V;
+    const float* qr = (a < k) ? q + ((size_t)b * k + a) * V : nullptr;
+    const int seg = (V + kAcceptWarps - 1) / kAcceptWarps;
+    const int s0 = w * seg, s1 = min(V, s0 + seg);
+
+    unsigned long long S = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int mode = s_mode;
+        unsigned long long tot = 0;
+        for (int st = 0, base = s0; base < s1; base += kStep, ++st) {
+            unsigned long long ws = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int x = base + i * 32 + lane;
+                if (x < s1) ws += weight_of(row_value(pr, qr, x, mode));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+            if (lane == 0) step_sum[w][st] = ws;
+            tot += ws;
+        }
+        if (lane == 0) warp_tot[w] = tot;
+        __syncthreads();
+        S = 0;
+        for (int i = 0; i < kAcceptWarps; ++i) S += warp_tot[i];
+        if (S != 0 || mode == 1) break;
+        __syncthreads();
+        if (t == 0) s_mode = 1;           // residual all zero: draw from p
+        __syncthreads();
+    }
+    const int mode = s_mode;
+    const unsigned long long m = (unsigned long long)(u[(size_t)b * (k + 1) + k] * 16777216.0f);
+    const unsigned long long thr = m * (S >> 24) + ((m * (S & 0xFFFFFFull)) >> 24);
+    // the warp whose segment holds the threshold
+    unsigned long long before = 0;
+    int ww = 0;
+    for (; ww < kAcceptWarps - 1; ++ww) {
+        if (before + warp_tot[ww] > thr) break;
+        before += warp_tot[ww];
+    }
+    if (w == ww) {
+        const int ws0 = ww * seg, ws1 = min(V, ws0 + seg);
+        int st = 0;
+        for (int base = ws0; base < ws1; base += kStep, ++st) {
+            if (before + step_sum[ww][st] > thr) break;
+            before += step_sum[ww][st];
+        }
+        const int base = ws0 + st * kStep;
+        int found = -1;
+        for (int i = 0; i < 4 && found < 0; ++i) {
+            const int x = base + i * 32 + lane;
+            unsigned long long wv = (x < ws1) ? weight_of(row_value(pr, qr, x, mode)) : 0ull;
+            unsigned long long inc = wv;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long nb = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += nb;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, before + inc > thr);
+            if (hit) found = base + i * 32 + (__ffs(hit) - 1);
+            before += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) s_tok = found;
+    }
+    __syncthreads();
+    if (t == 0) {
+        acc_len[b] = a;
+        next_tok[b] = s_tok;
+    }
+}
+
+// Unfused greedy acceptance: per sequence, row summaries from the logits then
+// the chain or tree rule.  The tree (parent and depth of each node) travels in
+// the kernel parameters.
+struct TreeArrays { int parent[kMaxSeqRows]; int depth[kMaxSeqRows]; };
+
+__global__ void __launch_bounds__(256)
+accept_greedy_kernel(const float* __restrict__ logits, const int* __restrict__ tokens, int n_rows, int V,
+                     int tree, TreeArrays ta, int* acc_len, int* next_tok, int* path) {
+    __shared__ spec_row_stats rs[kMaxSeqRows];
+    __shared__ int par[kMaxSeqRows], dep[kMaxSeqRows];
+    const int b = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x < kMaxSeqRows) { par[threadIdx.x] = ta.parent[threadIdx.x]; dep[threadIdx.x] = ta.depth[threadIdx.x]; }
+    for (int j = w; j < n_rows; j += 8) {
+        const float* row = logits + ((size_t)b * n_rows + j) * V;
+        spec_row_stats s = stat_empty();
+        for (int x = lane; x < V; x += 32) {
+            spec_row_stats one;
+            one.top1 = row[x]; one.top2 = -INFINITY; one.sum_exp = 1.f; one.argmax = x;
+            stat_merge(s, one);
+        }
+        s = stat_warp_merge(s);
+        if (lane == 0) rs[j] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int* tok = tokens + (size_t)b * n_rows;
+        int* pth = path ? path + (size_t)b * kMaxSeqRows : nullptr;
+        if (tree) accept_tree_one(rs, 0, n_rows, tok, par, dep, acc_len + b, next_tok + b, pth);
+        else accept_chain_one(rs, 0, n_rows, tok, acc_len + b, next_tok + b, pth);
+    }
+}
+
+// Tree commit: rows of depth 1..a move from slot s+path[d] to slot s+d, in
+// increasing depth (a move never overwrites a later move's source).  One CTA
+// per (layer, kv head, sequence); lengths are updated by a second launch.
+template <typename KT>
+__global__ void commit_tree_kernel(KT* kc, KT* vc, const int* len, const int* acc_len, const int* path,
+                                   int path_stride, int n_layers, int n_kv_heads, int kv_batch, int kv_ctx,
+                                   int hd, int* err) {
+    const int lh = blockIdx.x, b = blockIdx.y;
+    const int layer = lh / n_kv_heads, kvh = lh % n_kv_heads;
+    const int s = len[b], a = acc_len[b];
+    const size_t head = (((size_t)layer * kv_batch + b) * n_kv_heads + kvh) * kv_ctx;
+    for (int d = 1; d <= a; ++d) {
+        const int src = s + path[(size_t)b * path_stride + d], dst = s + d;
+        if (src >= kv_ctx || dst >= kv_ctx) { if (threadIdx.x == 0) dev_error(err, SPEC_DEVERR_CAPACITY); return; }
+        KT kv0 = KT(), vv0 = KT();
+        const int i = threadIdx.x;
+        if (i < hd) { kv0 = kc[(head + src) * hd + i]; vv0 = vc[(head + src) * hd + i]; }
+        __syncthreads();
+        if (i < hd) { kc[(head + dst) * hd + i] = kv0; vc[(head + dst) * hd + i] = vv0; }
+        __syncthreads();
+    }
+}
+
+__global__ void commit_len_kernel(int* len, const int* acc_len, int batch, int kv_ctx, int* err) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= batch) return;
+    const int n = len[b] + acc_len[b] + 1;
+    if (n > kv_ctx) dev_error(err, SPEC_DEVERR_CAPACITY);
+    len[b] = min(n, kv_ctx);
+}
+
+// Draft-length schedule: float64, explicit rounding (no contraction), in the
+// order written in the header.
+struct SchedParams {
+    int batch;
+    int row0[kMaxPlanBatch];
+    int n_rows[kMaxPlanBatch];
+    int min_k, max_k;
+    double low, high, decay;
+};
+
+__global__ void schedule_kernel(const double* __restrict__ probs, const int* __restrict__ acc_len, double* ema,
+                                SchedParams sp, int* k_next, double* conf_out) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= sp.batch) return;
+    const int n = sp.n_rows[b], k = n - 1, r0 = sp.row0[b];
+    const double acc = __ddiv_rn((double)acc_len[b], (double)k);
+    const double e = __dadd_rn(__dmul_rn(sp.decay, ema[b]), __dmul_rn(__dsub_rn(1.0, sp.decay), acc));
+    double s1 = 0.0, sg = 0.0;
+    for (int i = 0; i < n; ++i) {
+        const double p1 = probs[2 * (size_t)(r0 + i)], p2 = probs[2 * (size_t)(r0 + i) + 1];
+        s1 = __dadd_rn(s1, p1);
+        sg = __dadd_rn(sg, __dsub_rn(p1, p2));
+    }
+    const double avg1 = __ddiv_rn(s1, (double)n), avgg = __ddiv_rn(sg, (double)n);
+    const double gap = fmin(__dmul_rn(avgg, 5.0), 1.0);
+    const double c = __dadd_rn(__dadd_rn(__dmul_rn(0.4, avg1), __dmul_rn(0.3, gap)), __dmul_rn(0.3, e));
+    const double lin = __dadd_rn((double)sp.min_k,
+                                 __ddiv_rn(__dmul_rn((double)(sp.max_k - sp.min_k), __dsub_rn(c, sp.low)),
+                                           __dsub_rn(sp.high, sp.low)));
+    long long kk = (long long)lin;            // truncation toward zero
+    kk = kk < sp.min_k ? sp.min_k : (kk > sp.max_k ? sp.max_k : kk);
+    ema[b] = e;
+    k_next[b] = (int)kk;
+    if (conf_out) conf_out[b] = c;
+}
+
+__global__ void row_probs_kernel(const spec_row_stats* __restrict__ st, int rows, double* out) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows) return;
+    const spec_row_stats s = st[r];
+    const double S = (double)s.sum_exp;
+    out[2 * (size_t)r] = __ddiv_rn(1.0, S);
+    out[2 * (size_t)r + 1] = __ddiv_rn(exp((double)s.top2 - (double)s.top1), S);
+}
+
+}  // namespace spec
+
+using namespace spec;
+
+extern "C" int spec_accept(const float* p, const float* q, const int32_t* draft, const float* u, int32_t batch,
+                           int32_t k, int32_t vocab, int32_t* acc_len, int32_t* next_tok, void* stream) {
+    if (!p || !q || !draft || !u || !acc_len || !next_tok) return set_error(SPEC_ERR_ARG, "spec_accept: null pointer");
+    if (batch <= 0 || k < 1 || k > 32 || vocab <= 0) return set_error(SPEC_ERR_ARG, "spec_accept: bad sizes");
+    if (vocab > kAcceptWarps * kMaxSteps * kStep) return set_error(SPEC_ERR_UNSUPPORTED, "spec_accept: vocab too large");
+    accept_sample_kernel<<<batch, kAcceptThreads, 0, (cudaStream_t)stream>>>(p, q, draft, u, k, vocab, acc_len, next_tok);
+    return check_cuda(cudaGetLastError(), "spec_accept launch");
+}
+
+extern "C" int spec_accept_greedy(const float* logits, const int32_t* tokens, const int32_t* tree_parent,
+                                  int32_t batch, int32_t n_rows, int32_t vocab, int32_t* acc_len,
+                                  int32_t* next_tok, int32_t* path, void* stream) {
+    if (!logits || !tokens || !acc_len || !next_tok) return set_error(SPEC_ERR_ARG, "spec_accept_greedy: null pointer");
+    if (batch <= 0 || n_rows < 1 || n_rows > kMaxSeqRows || vocab <= 0)
+        return set_error(SPEC_ERR_ARG, "spec_accept_greedy: bad sizes");
+    if (tree_parent && !path) return set_error(SPEC_ERR_ARG, "spec_accept_greedy: tree mode needs path");
+    TreeArrays ta{};
+    if (tree_parent) {
+        if (tree_parent[0] != -1) return set_error(SPEC_ERR_ARG, "tree_parent[0] must be -1");
+        ta.parent[0] = -1;
+        for (int i = 1; i < n_rows; ++i) {
+            if (tree_parent[i] < 0 || tree_parent[i] >= i) return set_error(SPEC_ERR_ARG, "tree_parent[i] must be in [0, i)");
+            ta.parent[i] = tree_parent[i];
+            ta.depth[i] = ta.depth[tree_parent[i]] + 1;
+        }
+    }
+    accept_greedy_kernel<<<batch, 256, 0, (cudaStream_t)stream>>>(logits, tokens, n_rows, vocab, tree_parent ? 1 : 0,
+                                                                  ta, acc_len, next_tok, path);
+    return check_cuda(cudaGetLastError(), "spec_accept_greedy launch");
+}
+
+extern "C" int kv_commit(spec_kv* kv, int32_t batch, const int32_t* acc_len, const int32_t* path,
+                         int32_t path_stride, void* stream) {
+    if (!kv || !acc_len) return set_error(SPEC_ERR_ARG, "kv_commit: null pointer");
+    if (batch <= 0 || batch > kv->batch) return set_error(SPEC_ERR_ARG, "kv_commit: bad batch");
+    spec_model* m = kv->m;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (path) {
+        if (path_stride < 1) return set_error(SPEC_ERR_ARG, "kv_commit: bad path stride");
+        dim3 grid(m->cfg.n_layers * m->cfg.n_kv_heads, batch);
+        const int threads = m->cfg.head_dim;
+        if (m->bf16)
+            commit_tree_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
+                (__nv_bfloat16*)kv->k, (__nv_bfloat16*)kv->v, kv->len, acc_len, path, path_stride, m->cfg.n_layers,
+                m->cfg.n_kv_heads, kv->batch, kv->max_ctx, m->cfg.head_dim, m->err);
+        else
+            commit_tree_kernel<float><<<grid, threads, 0, st>>>((float*)kv->k, (float*)kv->v, kv->len, acc_len, path,
+                                                                path_stride, m->cfg.n_layers, m->cfg.n_kv_heads,
+                                                                kv->batch, kv->max_ctx, m->cfg.head_dim, m->err);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return check_cuda(e, "kv_commit tree launch");
+    }
+    commit_len_kernel<<<(batch + 127) / 128, 128, 0, st>>>(kv->len, acc_len, batch, kv->max_ctx, m->err);
+    m->launches += path ? 2 : 1;
+    return check_cuda(cudaGetLastError(), "kv_commit launch");
+}
+
+extern "C" int spec_row_probs(const spec_row_stats* stats, int32_t rows, double* out, void* stream) {
+    if (!stats || !out || rows <= 0) return set_error(SPEC_ERR_ARG, "spec_row_probs: bad arguments");
+    row_probs_kernel<<<(rows + 127) / 128, 128, 0, (cudaStream_t)stream>>>(stats, rows, out);
+    return check_cuda(cudaGetLastError(), "spec_row_probs launch");
+}
+
+extern "C" int spec_schedule_k(const double* top_probs, const int32_t* n_rows, const int32_t* acc_len, double* ema,
+                               int32_t batch, const spec_k_schedule* sch, int32_t* k_next, double* conf,
+                               void* stream) {
+    if (!top_probs || !n_rows || !acc_len || !ema || !sch || !k_next)
+        return set_error(SPEC_ERR_ARG, "spec_schedule_k: null pointer");
+    if (batch <= 0 || batch > kMaxPlanBatch) return set_error(SPEC_ERR_ARG, "spec_schedule_k: bad batch");
+    if (sch->min_k < 1 || sch->max_k < sch->min_k || !(sch->high > sch->low))
+        return set_error(SPEC_ERR_ARG, "spec_schedule_k: bad schedule");
+    SchedParams sp{};
+    sp.batch = batch;
+    int r = 0;
+    for (int b = 0; b < batch; ++b) {
+        if (n_rows[b] < 2) return set_error(SPEC_ERR_ARG, "spec_schedule_k: n_rows must be >= 2 (k >= 1)");
+        sp.row0[b] = r;
+        sp.n_rows[b] = n_rows[b];
+        r += n_rows[b];
+    }
+    sp.min_k = sch->min_k; sp.max_k = sch->max_k;
+    sp.low = sch->low; sp.high = sch->high; sp.decay = sch->decay;
+    schedule_kernel<<<(batch + 127) / 128, 128, 0, (cudaStream_t)stream>>>(top_probs, acc_len, ema, sp, k_next, conf);
+    return check_cuda(cudaGetLastError(), "spec_schedule_k launch");
+}

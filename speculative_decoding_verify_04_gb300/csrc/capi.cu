@@ -1,0 +1,845 @@
+// C ABI entry points: model and KV lifecycle, row plans, the forward passes
+// behind spec_prefill / spec_draft / spec_verify.
+//
+// Layer-skip self-drafting ("self-speculative decoding" page,
+// m.lqnn.cn/news/278124, sections 2.1, 3.3, 4.2, 4.3): one KV cache serves the
+// draft (layers [0, L)) and the verifier (layers [L, N)); the draft's pass over
+// a row writes that row's first-L KV and leaves its layer-L residual state,
+// which the verifier continues from.  Position ids are the committed length
+// plus the row's offset (chain) or depth (tree).
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "model.cuh"
+#include "stats.cuh"
+
+namespace spec {
+
+static thread_local std::string g_err;
+
+int set_error(int code, const std::string& msg) {
+    g_err = msg;
+    return code;
+}
+
+int check_cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return SPEC_OK;
+    g_err = std::string(what) + ": " + cudaGetErrorString(e);
+    return SPEC_ERR_CUDA;
+}
+
+int prof_start(spec_model* m, cudaStream_t st) {
+    if (!m->prof_on) return -1;
+    const size_t i = m->prof_n;
+    if (2 * i + 2 > m->prof_ev.size()) {
+        cudaEvent_t a, b;
+        if (cudaEventCreate(&a) != cudaSuccess) return -1;
+        if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return -1; }
+        m->prof_ev.push_back(a);
+        m->prof_ev.push_back(b);
+        m->prof_kind.push_back(0);
+        m->prof_bytes.push_back(0.0);
+    }
+    cudaEventRecord(m->prof_ev[2 * i], st);
+    m->prof_n = i + 1;
+    return (int)i;
+}
+
+void prof_stop(spec_model* m, int slot, cudaStream_t st, int kind, double bytes) {
+    if (slot < 0) return;
+    cudaEventRecord(m->prof_ev[2 * slot + 1], st);
+    m->prof_kind[slot] = kind;
+    m->prof_bytes[slot] = bytes;
+}
+
+#define SPEC_TRY(x)                          \
+    do {                                     \
+        int rc_ = (x);                       \
+        if (rc_ != SPEC_OK) return rc_;      \
+    } while (0)
+#define SPEC_CUDA(x, what) SPEC_TRY(check_cuda((x), what))
+
+// ---------------------------------------------------------------------------
+// small kernels
+template <typename T>
+__global__ void to_f32_kernel(const T* __restrict__ src, float* __restrict__ dst, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = to_f32<T>(src[i]);
+}
+
+// cos/sin of pos * theta^(-2i/hd), evaluated in float64 and rounded once
+__global__ void rope_table_kernel(float* cs, float* sn, int max_pos, int half, double theta) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)max_pos * half) return;
+    const int pos = (int)(idx / half), i = (int)(idx % half);
+    const double inv = pow(theta, -2.0 * (double)i / (double)(2 * half));
+    const double ang = (double)pos * inv;
+    cs[idx] = (float)cos(ang);
+    sn[idx] = (float)sin(ang);
+}
+
+struct PlanArgs {
+    PlanParams p;
+    int row0[kMaxPlanBatch];
+};
+
+// Row plan.  mode 0 chain: row j of sequence b at slot / position s_b + j.
+// mode 1 tree: slot s_b + j, position s_b + depth(j).  mode 2 draft pass j:
+// one row per sequence at slot / position s_b + j.
+__global__ void plan_kernel(PlanArgs a, RowPlan plan, const int* __restrict__ len, int T) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const PlanParams& p = a.p;
+    if (t < p.batch) {
+        plan.seq_row0[t] = (p.mode == 2) ? t : a.row0[t];
+        plan.seq_nrows[t] = (p.mode == 2) ? 1 : p.n_rows[t];
+        plan.seq_base[t] = len[t];
+    }
+    if (t < kMaxSeqRows) {
+        plan.tree_parent[t] = p.parent[t];
+        plan.tree_depth[t] = p.depth[t];
+    }
+    if (t >= T) return;
+    int b, j;
+    if (p.mode == 2) {
+        b = t;
+        j = p.pass;
+    } else {
+        int lo = 0, hi = p.batch - 1;      // last sequence with row0 <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.row0[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        j = t - a.row0[b];
+    }
+    const int s = len[b];
+    plan.row_seq[t] = b;
+    plan.row_local[t] = j;
+    plan.row_slot[t] = s + j;
+    plan.row_pos[t] = s + (p.mode == 1 ? p.depth[j] : j);
+}
+
+// First residual rows of a forward: from the layer-L state (h_in) or the token
+// embedding.  Writes h, the gained GEMM input and per-128-feature sums of h^2.
+template <typename WT>
+__global__ void __launch_bounds__(128)
+prologue_kernel(const float* __restrict__ h_in, int h_stride, const int* __restrict__ tok, int tok_stride,
+                int tok_col, const WT* __restrict__ embed, RowPlan plan, int d, int vocab,
+                const float* __restrict__ gain, float* h, WT* x, float* ss, int ss_stride, int* err) {
+    __shared__ float red[4];
+    const int r = blockIdx.x, t = threadIdx.x;
+    const int b = plan.row_seq[r], j = plan.row_local[r];
+    const float* src_h = nullptr;
+    const WT* src_e = nullptr;
+    if (h_in) {
+        src_h = h_in + ((size_t)b * h_stride + j) * d;
+    } else {
+        int token = tok[(size_t)b * tok_stride + tok_col + j];
+        if (token < 0 || token >= vocab) {
+            if (t == 0) dev_error(err, SPEC_DEVERR_TOKEN);
+            token = 0;
+        }
+        src_e = embed + (size_t)token * d;
+    }
+    const int n_tiles = (d + 127) / 128;
+    for (int tile = 0; tile < n_tiles; ++tile) {
+        const int n = tile * 128 + t;
+        float v = 0.f;
+        if (n < d) {
+            v = src_h ? src_h[n] : to_f32<WT>(src_e[n]);
+            h[(size_t)r * d + n] = v;
+            x[(size_t)r * d + n] = from_f32<WT>(v * gain[n]);
+        }
+        float s = warp_sum(v * v);
+        if ((t & 31) == 0) red[t >> 5] = s;
+        __syncthreads();
+        if (t == 0) ss[(size_t)tile * ss_stride + r] = (red[0] + red[1]) + (red[2] + red[3]);
+        __syncthreads();
+    }
+}
+
+__global__ void copy_rows_kernel(const float* __restrict__ h, float* __restrict__ dst, int rows, int d,
+                                 int dst_row_stride, int dst_col) {
+    const int r = blockIdx.x;
+    for (int n = threadIdx.x; n < d; n += blockDim.x)
+        dst[((size_t)r * dst_row_stride + dst_col) * d + n] = h[(size_t)r * d + n];
+}
+
+__global__ void set_col0_kernel(const int* __restrict__ t0, int* cand, int stride, int batch) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < batch) cand[(size_t)b * stride] = t0[b];
+}
+
+__global__ void add_len_kernel(int* len, int seq, int n, int cap, int* err) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        const int v = len[seq] + n;
+        if (v > cap) dev_error(err, SPEC_DEVERR_CAPACITY);
+        len[seq] = min(v, cap);
+    }
+}
+
+template <typename T>
+__global__ void kv_copy_kernel(T* cache, T* buf, int to_cache, int seq, int layer0, int n_layers, int slot0,
+                               int n_slots, int kv_batch, int Hkv, int ctx, int hd) {
+    const size_t total = (size_t)n_layers * n_slots * Hkv * hd;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int e = (int)(i % hd);
+        size_t rest = i / hd;
+        const int h = (int)(rest % Hkv); rest /= Hkv;
+        const int s = (int)(rest % n_slots);
+        const int l = (int)(rest / n_slots);
+        const size_t c = ((((size_t)(layer0 + l) * kv_batch + seq) * Hkv + h) * ctx + slot0 + s) * hd + e;
+        if (to_cache) cache[c] = buf[i]; else buf[i] = cache[c];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// forward orchestration
+struct HeadSpec {
+    int mode;                      // HeadMode
+    int T, r0;                     // rows of the head launch
+    float* logits; int logits_stride; int logits_row0;
+    spec_row_stats* user_stats;
+    int* cand; int cand_stride; int cand_col;
+    const int* tokens; int tok_stride;
+    int* acc_len; int* next_tok; int* path;
+    int batch;
+};
+
+static EpiParams base_epi(spec_model* m, spec_kv* kv, int T) {
+    const spec_model_config& c = m->cfg;
+    EpiParams e{};
+    e.T = T;
+    e.r0 = 0;
+    e.ss_in = m->ss_part;
+    e.ss_tiles = (c.d_model + kTileN - 1) / kTileN;
+    e.ss_stride = c.max_rows;
+    e.inv_d = 1.0f / (float)c.d_model;
+    e.eps = c.rms_eps;
+    e.plan = m->plan;
+    e.err = m->err;
+    e.q = m->q;
+    e.kc = kv->k;
+    e.vc = kv->v;
+    e.kv_batch = kv->batch;
+    e.kv_ctx = kv->max_ctx;
+    e.n_heads = c.n_heads;
+    e.n_kv_heads = c.n_kv_heads;
+    e.head_dim = c.head_dim;
+    e.rope_cos = m->rope_cos;
+    e.rope_sin = m->rope_sin;
+    e.max_position = c.max_position;
+    e.q_scale = 1.0f / sqrtf((float)c.head_dim);
+    e.h = m->h;
+    e.d_model = c.d_model;
+    e.ss_out = m->ss_part;
+    e.act = m->x_act;
+    e.d_ff = c.d_ff;
+    e.vocab = c.vocab;
+    e.stat_part = m->stat_part;
+    e.row_stats = m->row_stats;
+    e.done_counter = m->counters + m->n_counters - 1;
+    return e;
+}
+
+static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows_per_seq, int lo, int hi,
+                      int tree, bool head_follows, cudaStream_t st) {
+    const spec_model_config& c = m->cfg;
+    const int qdim = c.n_heads * c.head_dim;
+    for (int l = lo; l < hi; ++l) {
+        LayerWeights& L = m->layers[l];
+        EpiParams e = base_epi(m, kv, T);
+        e.layer = l;
+        {   // Q|K|V
+            EpiParams q = e;
+            q.kind = EPI_QKV;
+            q.N = m->qkv_n;
+            GemmLaunch g{&L.tm_qkv, nullptr, L.qkv, m->x_in, c.d_model, m->qkv_n, c.d_model};
+            SPEC_TRY(launch_gemm(m, g, q, 0, st));
+        }
+        {   // attention
+            AttnParams a{};
+            a.q = m->q;
+            a.kc = kv->k;
+            a.vc = kv->v;
+            a.out = m->x_attn;
+            a.plan = m->plan;
+            a.batch = batch;
+            a.kv_batch = kv->batch;
+            a.kv_ctx = kv->max_ctx;
+            a.layer = l;
+            a.n_heads = c.n_heads;
+            a.n_kv_heads = c.n_kv_heads;
+            a.head_dim = c.head_dim;
+            a.tree = tree;
+            a.err = m->err;
+            SPEC_TRY(launch_attention(m, a, max_rows_per_seq, st));
+        }
+        {   // O projection + residual
+            EpiParams o = e;
+            o.kind = EPI_RESID;
+            o.N = c.d_model;
+            o.gain_next = L.ffn_g;
+            o.x_next = m->x_in;
+            GemmLaunch g{&L.tm_o, nullptr, L.o, m->x_attn, qdim, c.d_model, qdim};
+            SPEC_TRY(launch_gemm(m, g, o, 1, st));
+        }
+        {   // gate | up -> SwiGLU
+            EpiParams s = e;
+            s.kind = EPI_SWIGLU;
+            s.N = m->gu_n;
+            GemmLaunch g{&L.tm_gu, nullptr, L.gu, m->x_in, c.d_model, m->gu_n, c.d_model};
+            SPEC_TRY(launch_gemm(m, g, s, 0, st));
+        }
+        {   // down projection + residual
+            EpiParams dn = e;
+            dn.kind = EPI_RESID;
+            dn.N = c.d_model;
+            dn.gain_next = (l + 1 < hi || !head_follows) ? (l + 1 < c.n_layers ? m->layers[l + 1].attn_g : m->final_g)
+                                                         : m->final_g;
+            dn.x_next = m->x_in;
+            GemmLaunch g{&L.tm_down, nullptr, L.down, m->x_act, c.d_ff, c.d_model, c.d_ff};
+            SPEC_TRY(launch_gemm(m, g, dn, 2, st));
+        }
+    }
+    return SPEC_OK;
+}
+
+static int run_head(spec_model* m, spec_kv* kv, const HeadSpec& hs, cudaStream_t st) {
+    const spec_model_config& c = m->cfg;
+    EpiParams e = base_epi(m, kv, hs.T);
+    e.kind = EPI_HEAD;
+    e.r0 = hs.r0;
+    e.N = c.vocab;
+    e.logits = hs.logits;
+    e.logits_stride = hs.logits_stride;
+    e.logits_row0 = hs.logits_row0;
+    e.user_stats = hs.user_stats;
+    e.head_mode = hs.mode;
+    e.cand = hs.cand;
+    e.cand_stride = hs.cand_stride;
+    e.cand_col = hs.cand_col;
+    e.tokens = hs.tokens;
+    e.tok_stride = hs.tok_stride;
+    e.acc_len = hs.acc_len;
+    e.next_tok = hs.next_tok;
+    e.path = hs.path;
+    e.batch = hs.batch;
+    GemmLaunch g{&m->tm_head, nullptr, m->head, m->x_in, c.d_model, c.vocab, c.d_model};
+    return launch_gemm(m, g, e, 0, st);
+}
+
+static int launch_plan(spec_model* m, const PlanParams& p, int T, const int* len, cudaStream_t st) {
+    PlanArgs a{};
+    a.p = p;
+    int r = 0;
+    for (int b = 0; b < p.batch; ++b) {
+        a.row0[b] = r;
+        r += (p.mode == 2) ? 1 : p.n_rows[b];
+    }
+    const int n = std::max(std::max(T, p.batch), kMaxSeqRows);
+    plan_kernel<<<(n + 127) / 128, 128, 0, st>>>(a, m->plan, len, T);
+    ++m->launches;
+    return check_cuda(cudaGetLastError(), "plan launch");
+}
+
+static int launch_prologue(spec_model* m, int T, const float* h_in, int h_stride, const int* tok, int tok_stride,
+                           int tok_col, int layer_lo, cudaStream_t st) {
+    const spec_model_config& c = m->cfg;
+    const float* gain = layer_lo < c.n_layers ? m->layers[layer_lo].attn_g : m->final_g;
+    if (m->bf16)
+        prologue_kernel<__nv_bfloat16><<<T, 128, 0, st>>>(h_in, h_stride, tok, tok_stride, tok_col,
+                                                         (const __nv_bfloat16*)m->embed, m->plan, c.d_model, c.vocab,
+                                                         gain, m->h, (__nv_bfloat16*)m->x_in, m->ss_part, c.max_rows,
+                                                         m->err);
+    else
+        prologue_kernel<float><<<T, 128, 0, st>>>(h_in, h_stride, tok, tok_stride, tok_col, (const float*)m->embed,
+                                                 m->plan, c.d_model, c.vocab, gain, m->h, (float*)m->x_in,
+                                                 m->ss_part, c.max_rows, m->err);
+    ++m->launches;
+    return check_cuda(cudaGetLastError(), "prologue launch");
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace spec
+
+using namespace spec;
+
+// ---------------------------------------------------------------------------
+extern "C" const char* spec_last_error(void) { return g_err.c_str(); }
+
+extern "C" int spec_device_info(int32_t* num_sms, int32_t* cc_major, int32_t* cc_minor) {
+    int dev = 0;
+    SPEC_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    int v = 0;
+    if (num_sms) { SPEC_CUDA(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev), "attr"); *num_sms = v; }
+    if (cc_major) { SPEC_CUDA(cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, dev), "attr"); *cc_major = v; }
+    if (cc_minor) { SPEC_CUDA(cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev), "attr"); *cc_minor = v; }
+    return SPEC_OK;
+}
+
+extern "C" void spec_model_destroy(spec_model* m) {
+    if (!m) return;
+    for (cudaEvent_t e : m->prof_ev) cudaEventDestroy(e);
+    cudaFree(m->wmem);
+    cudaFree(m->ws);
+    delete m;
+}
+
+extern "C" int spec_model_create(const spec_model_config* cfg, const void* const* weights, void* stream,
+                                 spec_model** out) {
+    if (!cfg || !weights || !out) return set_error(SPEC_ERR_ARG, "spec_model_create: null pointer");
+    *out = nullptr;
+    const spec_model_config c = *cfg;
+    if (c.n_layers < 1 || c.d_model < 1 || c.n_heads < 1 || c.n_kv_heads < 1 || c.head_dim < 1 || c.d_ff < 1 ||
+        c.vocab < 2 || c.max_rows < 1 || c.max_batch < 1 || c.max_position < 1 || !(c.rms_eps >= 0.f) ||
+        !(c.rope_theta > 0.f))
+        return set_error(SPEC_ERR_ARG, "spec_model_create: non-positive size");
+    if (c.exit_layer < 0 || c.exit_layer >= c.n_layers) return set_error(SPEC_ERR_ARG, "exit_layer must be in [0, N)");
+    if (c.dtype != SPEC_DTYPE_F32 && c.dtype != SPEC_DTYPE_BF16) return set_error(SPEC_ERR_ARG, "unknown dtype");
+    if (c.head_dim != 64 && c.head_dim != 128) return set_error(SPEC_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (c.n_heads % c.n_kv_heads) return set_error(SPEC_ERR_UNSUPPORTED, "n_heads must be a multiple of n_kv_heads");
+    if (c.d_model % 64 || (c.n_heads * c.head_dim) % 64 || c.d_ff % 64)
+        return set_error(SPEC_ERR_UNSUPPORTED, "d_model, n_heads*head_dim and d_ff must be multiples of 64");
+    if (c.max_rows > 4096 || c.max_batch > kMaxPlanBatch)
+        return set_error(SPEC_ERR_CAPACITY, "max_rows <= 4096 and max_batch <= 256");
+    for (int i = 0; i < SPEC_W_COUNT(c.n_layers); ++i)
+        if (!weights[i]) return set_error(SPEC_ERR_ARG, "spec_model_create: null weight pointer");
+
+    spec_model* m = new spec_model();
+    m->cfg = c;
+    cudaStream_t st = (cudaStream_t)stream;
+    auto fail = [&](int rc) { spec_model_destroy(m); return rc; };
+    int rc;
+    if ((rc = check_cuda(cudaGetDevice(&m->device), "cudaGetDevice"))) return fail(rc);
+    if ((rc = check_cuda(cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device), "attr")))
+        return fail(rc);
+    m->bf16 = c.dtype == SPEC_DTYPE_BF16;
+    m->elem = m->bf16 ? 2 : 4;
+    if (m->bf16) {
+        int major = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, m->device);
+        if (major < 10) return fail(set_error(SPEC_ERR_UNSUPPORTED, "bf16 path needs a Blackwell (sm_10x) GPU"));
+    }
+    const size_t E = m->elem;
+    const int d = c.d_model, qdim = c.n_heads * c.head_dim, F = c.d_ff, V = c.vocab;
+    const int gu_blocks = (F + 63) / 64;
+    m->qkv_n = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+    m->gu_n = gu_blocks * 128;
+    m->max_rows_pad = (c.max_rows + 15) / 16 * 16;
+    const int half = c.head_dim / 2;
+
+    // ---- packed weights
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    const size_t o_embed = take((size_t)V * d * E), o_head = take((size_t)V * d * E), o_fg = take((size_t)d * 4);
+    std::vector<size_t> o_l(c.n_layers * 6);
+    for (int l = 0; l < c.n_layers; ++l) {
+        o_l[l * 6 + 0] = take((size_t)m->qkv_n * d * E);
+        o_l[l * 6 + 1] = take((size_t)d * qdim * E);
+        o_l[l * 6 + 2] = take((size_t)m->gu_n * d * E);
+        o_l[l * 6 + 3] = take((size_t)d * F * E);
+        o_l[l * 6 + 4] = take((size_t)d * 4);
+        o_l[l * 6 + 5] = take((size_t)d * 4);
+    }
+    const size_t o_cos = take((size_t)c.max_position * half * 4), o_sin = take((size_t)c.max_position * half * 4);
+    if ((rc = check_cuda(cudaMalloc(&m->wmem, off), "cudaMalloc(weights)"))) return fail(rc);
+    char* W = m->wmem;
+    m->embed = W + o_embed;
+    m->head = W + o_head;
+    m->final_g = (float*)(W + o_fg);
+    m->rope_cos = (float*)(W + o_cos);
+    m->rope_sin = (float*)(W + o_sin);
+    auto cp = [&](void* dst, const void* src, size_t bytes) {
+        return check_cuda(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st), "weight copy");
+    };
+    auto gain = [&](float* dst, const void* src) {
+        if (m->bf16) to_f32_kernel<__nv_bfloat16><<<(d + 255) / 256, 256, 0, st>>>((const __nv_bfloat16*)src, dst, d);
+        else to_f32_kernel<float><<<(d + 255) / 256, 256, 0, st>>>((const float*)src, dst, d);
+        return check_cuda(cudaGetLastError(), "gain copy");
+    };
+    if ((rc = cp(m->embed, weights[SPEC_W_EMBED], (size_t)V * d * E))) return fail(rc);
+    if ((rc = cp(m->head, weights[SPEC_W_LM_HEAD], (size_t)V * d * E))) return fail(rc);
+    if ((rc = gain(m->final_g, weights[SPEC_W_FINAL_NORM]))) return fail(rc);
+    m->layers.resize(c.n_layers);
+    const size_t row = (size_t)d * E;
+    for (int l = 0; l < c.n_layers; ++l) {
+        const void* const* wl = weights + SPEC_W_LAYER0 + 9 * l;
+        LayerWeights& L = m->layers[l];
+        L.qkv = W + o_l[l * 6 + 0];
+        L.o = W + o_l[l * 6 + 1];
+        L.gu = W + o_l[l * 6 + 2];
+        L.down = W + o_l[l * 6 + 3];
+        L.attn_g = (float*)(W + o_l[l * 6 + 4]);
+        L.ffn_g = (float*)(W + o_l[l * 6 + 5]);
+        char* qkv = (char*)L.qkv;
+        if ((rc = cp(qkv, wl[SPEC_WL_Q], (size_t)qdim * row))) return fail(rc);
+        if ((rc = cp(qkv + (size_t)qdim * row, wl[SPEC_WL_K], (size_t)c.n_kv_heads * c.head_dim * row))) return fail(rc);
+        if ((rc = cp(qkv + (size_t)(qdim + c.n_kv_heads * c.head_dim) * row, wl[SPEC_WL_V],
+                     (size_t)c.n_kv_heads * c.head_dim * row))) return fail(rc);
+        if ((rc = cp(L.o, wl[SPEC_WL_O], (size_t)d * qdim * E))) return fail(rc);
+        // gate/up: per block of 64 features, 64 gate rows then 64 up rows
+        if ((rc = check_cuda(cudaMemcpy2DAsync(L.gu, 128 * row, wl[SPEC_WL_GATE], 64 * row, 64 * row, F / 64,
+                                               cudaMemcpyDeviceToDevice, st), "gate pack"))) return fail(rc);
+        if ((rc = check_cuda(cudaMemcpy2DAsync((char*)L.gu + 64 * row, 128 * row, wl[SPEC_WL_UP], 64 * row, 64 * row,
+                                               F / 64, cudaMemcpyDeviceToDevice, st), "up pack"))) return fail(rc);
+        if ((rc = cp(L.down, wl[SPEC_WL_DOWN], (size_t)d * F * E))) return fail(rc);
+        if ((rc = gain(L.attn_g, wl[SPEC_WL_ATTN_NORM]))) return fail(rc);
+        if ((rc = gain(L.ffn_g, wl[SPEC_WL_FFN_NORM]))) return fail(rc);
+    }
+    {
+        const long long n = (long long)c.max_position * half;
+        rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(m->rope_cos, m->rope_sin, c.max_position, half,
+                                                                       (double)c.rope_theta);
+        if ((rc = check_cuda(cudaGetLastError(), "rope table"))) return fail(rc);
+    }
+
+    // ---- workspace
+    const int R = c.max_rows, Rp = m->max_rows_pad;
+    const int t_pad_max = m->bf16 ? std::min(kMaxTPad, Rp) : 32;
+    size_t part = 0;
+    const int shapes[5][2] = {{m->qkv_n, d}, {d, qdim}, {m->gu_n, d}, {d, F}, {V, d}};
+    int max_tiles = 0;
+    for (auto& s : shapes) {
+        part = std::max(part, gemm_partial_floats_needed(m, s[0], s[1], t_pad_max));
+        max_tiles = std::max(max_tiles, (s[0] + kTileN - 1) / kTileN);
+    }
+    m->gemm_part_floats = part;
+    m->n_counters = max_tiles + 1;
+    const int rows_per_seq = std::min(kMaxSeqRows, R);
+    m->attn_part_floats = attn_partial_floats_needed(m, c.max_batch, rows_per_seq);
+    const int G = c.n_heads / c.n_kv_heads;
+    m->n_attn_counters = c.max_batch * c.n_kv_heads * ((rows_per_seq * G + 15) / 16);
+    off = 0;
+    const size_t w_h = take((size_t)R * d * 4);
+    const size_t w_xin = take((size_t)Rp * d * E), w_xat = take((size_t)Rp * qdim * E), w_xac = take((size_t)Rp * F * E);
+    const size_t w_q = take((size_t)R * qdim * 4);
+    const size_t w_ss = take((size_t)((d + 127) / 128) * R * 4);
+    const size_t w_sp = take((size_t)((V + 127) / 128) * R * sizeof(spec_row_stats));
+    const size_t w_rs = take((size_t)R * sizeof(spec_row_stats));
+    const size_t w_gp = take(part * 4);
+    const size_t w_cnt = take((size_t)m->n_counters * 4);
+    const size_t w_ap = take(m->attn_part_floats * 4);
+    const size_t w_ac = take((size_t)m->n_attn_counters * 4);
+    const size_t w_err = take(64);
+    const size_t w_plan = take((size_t)(4 * R + 3 * c.max_batch + 2 * kMaxSeqRows + 64) * 4);
+    m->ws_bytes = off;
+    if ((rc = check_cuda(cudaMalloc(&m->ws, off), "cudaMalloc(workspace)"))) return fail(rc);
+    if ((rc = check_cuda(cudaMemsetAsync(m->ws, 0, off, st), "workspace clear"))) return fail(rc);
+    char* S = m->ws;
+    m->h = (float*)(S + w_h);
+    m->x_in = S + w_xin;
+    m->x_attn = S + w_xat;
+    m->x_act = S + w_xac;
+    m->q = (float*)(S + w_q);
+    m->ss_part = (float*)(S + w_ss);
+    m->stat_part = (spec_row_stats*)(S + w_sp);
+    m->row_stats = (spec_row_stats*)(S + w_rs);
+    m->gemm_part = (float*)(S + w_gp);
+    m->counters = (int*)(S + w_cnt);
+    m->attn_part = (float*)(S + w_ap);
+    m->attn_counters = (int*)(S + w_ac);
+    m->err = (int*)(S + w_err);
+    int* pl = (int*)(S + w_plan);
+    m->plan.row_seq = pl; pl += R;
+    m->plan.row_slot = pl; pl += R;
+    m->plan.row_pos = pl; pl += R;
+    m->plan.row_local = pl; pl += R;
+    m->plan.seq_row0 = pl; pl += c.max_batch;
+    m->plan.seq_nrows = pl; pl += c.max_batch;
+    m->plan.seq_base = pl; pl += c.max_batch;
+    m->plan.tree_parent = pl; pl += kMaxSeqRows;
+    m->plan.tree_depth = pl; pl += kMaxSeqRows;
+
+    // ---- tensor maps (bf16 path)
+    if (m->bf16) {
+        bool ok = true;
+        for (int l = 0; l < c.n_layers; ++l) {
+            LayerWeights& L = m->layers[l];
+            ok &= make_tmap_2d(&L.tm_qkv, L.qkv, d, m->qkv_n, (uint64_t)d * 2, kTileK, kTileN);
+            ok &= make_tmap_2d(&L.tm_o, L.o, qdim, d, (uint64_t)qdim * 2, kTileK, kTileN);
+            ok &= make_tmap_2d(&L.tm_gu, L.gu, d, m->gu_n, (uint64_t)d * 2, kTileK, kTileN);
+            ok &= make_tmap_2d(&L.tm_down, L.down, F, d, (uint64_t)F * 2, kTileK, kTileN);
+        }
+        ok &= make_tmap_2d(&m->tm_head, m->head, d, V, (uint64_t)d * 2, kTileK, kTileN);
+        const void* xb[3] = {m->x_in, m->x_attn, m->x_act};
+        const int xk[3] = {d, qdim, F};
+        for (int i = 0; i < 3; ++i)
+            for (int tp = 16; tp <= t_pad_max; tp += 16)
+                ok &= make_tmap_2d(&m->tm_x[i][tp / 16 - 1], xb[i], xk[i], Rp, (uint64_t)xk[i] * 2, kTileK, tp);
+        if (!ok) return fail(set_error(SPEC_ERR_CUDA, "cuTensorMapEncodeTiled failed"));
+    }
+    if ((rc = check_cuda(cudaStreamSynchronize(st), "spec_model_create sync"))) return fail(rc);
+    *out = m;
+    return SPEC_OK;
+}
+
+extern "C" int spec_device_error(spec_model* m, int32_t* host_bits) {
+    if (!m || !host_bits) return set_error(SPEC_ERR_ARG, "spec_device_error: null pointer");
+    int v = 0;
+    SPEC_CUDA(cudaMemcpy(&v, m->err, 4, cudaMemcpyDeviceToHost), "read device error");
+    SPEC_CUDA(cudaMemset(m->err, 0, 4), "clear device error");
+    *host_bits = v;
+    return SPEC_OK;
+}
+
+extern "C" int spec_kv_create(spec_model* m, int32_t batch, int32_t max_ctx, spec_kv** out) {
+    if (!m || !out) return set_error(SPEC_ERR_ARG, "spec_kv_create: null pointer");
+    *out = nullptr;
+    if (batch < 1 || max_ctx < 1) return set_error(SPEC_ERR_ARG, "spec_kv_create: bad sizes");
+    if (batch > m->cfg.max_batch) return set_error(SPEC_ERR_CAPACITY, "spec_kv_create: batch > max_batch");
+    spec_kv* kv = new spec_kv();
+    kv->m = m;
+    kv->batch = batch;
+    kv->max_ctx = max_ctx;
+    const size_t bytes = (size_t)m->cfg.n_layers * batch * m->cfg.n_kv_heads * max_ctx * m->cfg.head_dim * m->elem;
+    int rc = check_cuda(cudaMalloc(&kv->k, bytes), "cudaMalloc(K cache)");
+    if (!rc) rc = check_cuda(cudaMalloc(&kv->v, bytes), "cudaMalloc(V cache)");
+    if (!rc) rc = check_cuda(cudaMalloc(&kv->len, (size_t)batch * 4), "cudaMalloc(lengths)");
+    if (!rc) rc = check_cuda(cudaMemset(kv->k, 0, bytes), "clear K");
+    if (!rc) rc = check_cuda(cudaMemset(kv->v, 0, bytes), "clear V");
+    if (!rc) rc = check_cuda(cudaMemset(kv->len, 0, (size_t)batch * 4), "clear lengths");
+    if (rc) {
+        cudaFree(kv->k); cudaFree(kv->v); cudaFree(kv->len);
+        delete kv;
+        return rc;
+    }
+    *out = kv;
+    return SPEC_OK;
+}
+
+extern "C" void spec_kv_destroy(spec_kv* kv) {
+    if (!kv) return;
+    cudaFree(kv->k);
+    cudaFree(kv->v);
+    cudaFree(kv->len);
+    delete kv;
+}
+
+extern "C" int spec_kv_set_lengths(spec_kv* kv, const int32_t* host_len, void* stream) {
+    if (!kv || !host_len) return set_error(SPEC_ERR_ARG, "spec_kv_set_lengths: null pointer");
+    for (int b = 0; b < kv->batch; ++b)
+        if (host_len[b] < 0 || host_len[b] > kv->max_ctx) return set_error(SPEC_ERR_CAPACITY, "length beyond max_ctx");
+    SPEC_CUDA(cudaMemcpyAsync(kv->len, host_len, (size_t)kv->batch * 4, cudaMemcpyHostToDevice, (cudaStream_t)stream),
+              "set lengths");
+    SPEC_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "set lengths sync");
+    return SPEC_OK;
+}
+
+extern "C" int spec_kv_get_lengths(spec_kv* kv, int32_t* host_len, void* stream) {
+    if (!kv || !host_len) return set_error(SPEC_ERR_ARG, "spec_kv_get_lengths: null pointer");
+    SPEC_CUDA(cudaMemcpyAsync(host_len, kv->len, (size_t)kv->batch * 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream),
+              "get lengths");
+    SPEC_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "get lengths sync");
+    return SPEC_OK;
+}
+
+static int kv_copy(spec_kv* kv, int32_t seq, int32_t layer0, int32_t n_layers, int32_t slot0, int32_t n_slots,
+                   void* k, void* v, int to_cache, void* stream) {
+    if (!kv || !k || !v) return set_error(SPEC_ERR_ARG, "spec_kv_import/export: null pointer");
+    spec_model* m = kv->m;
+    const spec_model_config& c = m->cfg;
+    if (seq < 0 || seq >= kv->batch || layer0 < 0 || n_layers < 1 || layer0 + n_layers > c.n_layers || slot0 < 0 ||
+        n_slots < 1 || slot0 + n_slots > kv->max_ctx)
+        return set_error(SPEC_ERR_ARG, "spec_kv_import/export: range outside the cache");
+    cudaStream_t st = (cudaStream_t)stream;
+    for (int which = 0; which < 2; ++which) {
+        void* cache = which ? kv->v : kv->k;
+        void* buf = which ? v : k;
+        if (m->bf16)
+            kv_copy_kernel<__nv_bfloat16><<<1024, 256, 0, st>>>((__nv_bfloat16*)cache, (__nv_bfloat16*)buf, to_cache,
+                                                               seq, layer0, n_layers, slot0, n_slots, kv->batch,
+                                                               c.n_kv_heads, kv->max_ctx, c.head_dim);
+        else
+            kv_copy_kernel<float><<<1024, 256, 0, st>>>((float*)cache, (float*)buf, to_cache, seq, layer0, n_layers,
+                                                       slot0, n_slots, kv->batch, c.n_kv_heads, kv->max_ctx,
+                                                       c.head_dim);
+    }
+    return check_cuda(cudaGetLastError(), "kv copy launch");
+}
+
+extern "C" int spec_kv_import(spec_kv* kv, int32_t seq, int32_t layer0, int32_t n_layers, int32_t slot0,
+                              int32_t n_slots, const void* k, const void* v, void* stream) {
+    return kv_copy(kv, seq, layer0, n_layers, slot0, n_slots, const_cast<void*>(k), const_cast<void*>(v), 1, stream);
+}
+
+extern "C" int spec_kv_export(spec_kv* kv, int32_t seq, int32_t layer0, int32_t n_layers, int32_t slot0,
+                              int32_t n_slots, void* k, void* v, void* stream) {
+    return kv_copy(kv, seq, layer0, n_layers, slot0, n_slots, k, v, 0, stream);
+}
+
+extern "C" int spec_prefill(spec_model* m, spec_kv* kv, int32_t seq, const int32_t* tokens, int32_t n,
+                            float* last_logits, int32_t* next_tok, void* stream) {
+    if (!m || !kv || !tokens) return set_error(SPEC_ERR_ARG, "spec_prefill: null pointer");
+    if (kv->m != m) return set_error(SPEC_ERR_ARG, "spec_prefill: cache of another model");
+    if (seq < 0 || seq >= kv->batch || n < 1) return set_error(SPEC_ERR_ARG, "spec_prefill: bad seq or n");
+    const spec_model_config& c = m->cfg;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int chunk = std::min(kMaxSeqRows, c.max_rows);
+    for (int done = 0; done < n; done += chunk) {
+        const int T = std::min(chunk, n - done);
+        PlanParams p{};
+        p.batch = seq + 1;
+        p.mode = 0;
+        p.n_rows[seq] = T;
+        SPEC_TRY(launch_plan(m, p, T, kv->len, st));
+        SPEC_TRY(launch_prologue(m, T, nullptr, 0, tokens + done, 0, 0, 0, st));
+        const bool last = done + T >= n;
+        const bool head = last && (last_logits || next_tok);
+        SPEC_TRY(run_layers(m, kv, T, seq + 1, T, 0, c.n_layers, 0, head, st));
+        if (head) {
+            HeadSpec hs{};
+            hs.mode = next_tok ? HEAD_DRAFT : HEAD_STATS;
+            hs.T = 1;
+            hs.r0 = T - 1;
+            hs.logits = last_logits;
+            hs.logits_stride = c.vocab;
+            hs.logits_row0 = T - 1;
+            hs.cand = next_tok;
+            hs.cand_stride = 0;
+            hs.cand_col = 0;
+            hs.batch = seq + 1;
+            SPEC_TRY(run_head(m, kv, hs, st));
+        }
+        add_len_kernel<<<1, 32, 0, st>>>(kv->len, seq, T, kv->max_ctx, m->err);
+        ++m->launches;
+        SPEC_CUDA(cudaGetLastError(), "length update");
+    }
+    return SPEC_OK;
+}
+
+extern "C" int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0, int32_t k, int32_t* cand,
+                          float* h_L, float* draft_logits, void* stream) {
+    if (!m || !kv || !t0 || !cand || !h_L) return set_error(SPEC_ERR_ARG, "spec_draft: null pointer");
+    if (kv->m != m) return set_error(SPEC_ERR_ARG, "spec_draft: cache of another model");
+    const spec_model_config& c = m->cfg;
+    if (c.exit_layer < 1) return set_error(SPEC_ERR_ARG, "spec_draft: exit_layer must be >= 1");
+    if (batch < 1 || batch > kv->batch || batch > c.max_rows) return set_error(SPEC_ERR_ARG, "spec_draft: bad batch");
+    if (k < 1 || k + 1 > kMaxSeqRows) return set_error(SPEC_ERR_ARG, "spec_draft: k must be in [1, 63]");
+    cudaStream_t st = (cudaStream_t)stream;
+    set_col0_kernel<<<(batch + 127) / 128, 128, 0, st>>>(t0, cand, k + 1, batch);
+    ++m->launches;
+    SPEC_CUDA(cudaGetLastError(), "draft init");
+    for (int j = 0; j <= k; ++j) {
+        PlanParams p{};
+        p.batch = batch;
+        p.mode = 2;
+        p.pass = j;
+        SPEC_TRY(launch_plan(m, p, batch, kv->len, st));
+        SPEC_TRY(launch_prologue(m, batch, nullptr, 0, cand, k + 1, 0, 0, st));
+        SPEC_TRY(run_layers(m, kv, batch, batch, 1, 0, c.exit_layer, 0, j < k, st));
+        copy_rows_kernel<<<batch, 256, 0, st>>>(m->h, h_L, batch, c.d_model, k + 1, j);
+        ++m->launches;
+        SPEC_CUDA(cudaGetLastError(), "draft state copy");
+        if (j < k) {
+            HeadSpec hs{};
+            hs.mode = HEAD_DRAFT;
+            hs.T = batch;
+            hs.r0 = 0;
+            hs.logits = draft_logits ? draft_logits + (size_t)j * c.vocab : nullptr;
+            hs.logits_stride = k * c.vocab;
+            hs.logits_row0 = 0;
+            hs.cand = cand;
+            hs.cand_stride = k + 1;
+            hs.cand_col = j + 1;
+            hs.batch = batch;
+            SPEC_TRY(run_head(m, kv, hs, st));
+        }
+    }
+    return SPEC_OK;
+}
+
+extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows, const float* h_in,
+                           int32_t h_stride, const int32_t* tokens, int32_t tok_stride, const int32_t* tree_parent,
+                           float* logits, spec_row_stats* stats, int32_t* acc_len, int32_t* next_tok, int32_t* path,
+                           void* stream) {
+    if (!m || !kv || !n_rows || !tokens) return set_error(SPEC_ERR_ARG, "spec_verify: null pointer");
+    if (kv->m != m) return set_error(SPEC_ERR_ARG, "spec_verify: cache of another model");
+    const spec_model_config& c = m->cfg;
+    if (batch < 1 || batch > kv->batch) return set_error(SPEC_ERR_ARG, "spec_verify: bad batch");
+    if ((acc_len == nullptr) != (next_tok == nullptr)) return set_error(SPEC_ERR_ARG, "acc_len and next_tok go together");
+    if (tree_parent && acc_len && !path) return set_error(SPEC_ERR_ARG, "tree acceptance needs path");
+    if (h_in && c.exit_layer < 1) return set_error(SPEC_ERR_ARG, "h_in needs exit_layer >= 1");
+    int T = 0, max_r = 0;
+    PlanParams p{};
+    p.batch = batch;
+    p.mode = tree_parent ? 1 : 0;
+    for (int b = 0; b < batch; ++b) {
+        if (n_rows[b] < 1 || n_rows[b] > kMaxSeqRows) return set_error(SPEC_ERR_ARG, "n_rows[b] must be in [1, 64]");
+        if (h_in && n_rows[b] > h_stride) return set_error(SPEC_ERR_ARG, "n_rows[b] > h_stride");
+        if (n_rows[b] > tok_stride) return set_error(SPEC_ERR_ARG, "n_rows[b] > tok_stride");
+        p.n_rows[b] = n_rows[b];
+        T += n_rows[b];
+        max_r = std::max(max_r, (int)n_rows[b]);
+    }
+    if (T > c.max_rows) return set_error(SPEC_ERR_CAPACITY, "sum of n_rows > max_rows");
+    if (tree_parent) {
+        const int n = n_rows[0];
+        if (tree_parent[0] != -1) return set_error(SPEC_ERR_ARG, "tree_parent[0] must be -1");
+        p.parent[0] = -1;
+        p.depth[0] = 0;
+        for (int i = 1; i < n; ++i) {
+            if (tree_parent[i] < 0 || tree_parent[i] >= i) return set_error(SPEC_ERR_ARG, "tree_parent[i] must be in [0, i)");
+            p.parent[i] = tree_parent[i];
+            p.depth[i] = p.depth[tree_parent[i]] + 1;
+        }
+        for (int b = 0; b < batch; ++b)
+            if (n_rows[b] != n) return set_error(SPEC_ERR_ARG, "tree mode: every sequence has the tree's node count");
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    const int lo = h_in ? c.exit_layer : 0;
+    SPEC_TRY(launch_plan(m, p, T, kv->len, st));
+    SPEC_TRY(launch_prologue(m, T, h_in, h_stride, tokens, tok_stride, 0, lo, st));
+    SPEC_TRY(run_layers(m, kv, T, batch, max_r, lo, c.n_layers, tree_parent ? 1 : 0, true, st));
+    HeadSpec hs{};
+    hs.mode = acc_len ? (tree_parent ? HEAD_ACCEPT_TREE : HEAD_ACCEPT_CHAIN) : HEAD_STATS;
+    hs.T = T;
+    hs.r0 = 0;
+    hs.logits = logits;
+    hs.logits_stride = c.vocab;
+    hs.logits_row0 = 0;
+    hs.user_stats = stats;
+    hs.tokens = tokens;
+    hs.tok_stride = tok_stride;
+    hs.acc_len = acc_len;
+    hs.next_tok = next_tok;
+    hs.path = path;
+    hs.batch = batch;
+    return run_head(m, kv, hs, st);
+}
+
+extern "C" int spec_profile(spec_model* m, int32_t enable) {
+    if (!m) return set_error(SPEC_ERR_ARG, "spec_profile: null model");
+    m->prof_on = enable != 0;
+    if (m->prof_on) m->prof_n = 0;
+    return SPEC_OK;
+}
+
+extern "C" int spec_profile_read(spec_model* m, int32_t kind, double* total_ms, double* bytes, int32_t* launches) {
+    if (!m || !total_ms || !bytes || !launches) return set_error(SPEC_ERR_ARG, "spec_profile_read: null pointer");
+    double ms = 0.0, by = 0.0;
+    int n = 0;
+    for (size_t i = 0; i < m->prof_n; ++i) {
+        if (m->prof_kind[i] != kind) continue;
+        SPEC_CUDA(cudaEventSynchronize(m->prof_ev[2 * i + 1]), "profile sync");
+        float t = 0.f;
+        SPEC_CUDA(cudaEventElapsedTime(&t, m->prof_ev[2 * i], m->prof_ev[2 * i + 1]), "profile elapsed");
+        ms += t;
+        by += m->prof_bytes[i];
+        ++n;
+    }
+    *total_ms = ms;
+    *bytes = by;
+    *launches = n;
+    return SPEC_OK;
+}
+
+extern "C" int spec_launch_count(spec_model* m, int64_t* count) {
+    if (!m || !count) return set_error(SPEC_ERR_ARG, "spec_launch_count: null pointer");
+    *count = m->launches;
+    return SPEC_OK;
+}

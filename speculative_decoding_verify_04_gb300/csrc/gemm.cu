@@ -1,0 +1,628 @@
+// Skinny weight-streaming GEMM  Y[T, N] = X[T, K] * W[N, K]^T  with fused epilogues.
+//
+// Decode-time verification multiplies a handful of rows (T = k+1 .. a few
+// hundred) by every weight matrix, so the kernel is a weight stream: each
+// weight byte is read once from HBM and used T times ("self-speculative
+// decoding" page, section 1.1: decoding is bandwidth bound at ~2 flop/byte;
+// section 1.2: verifying k positions costs one weight pass instead of k).
+//
+// bf16 path (tcgen05): swap-AB -- a 128-row W tile is the MMA's M side and the
+// activation rows are its N side (padded to a multiple of 16), so one
+// tcgen05.mma.kind::f16 of M=128, N=T_pad, K=16 consumes 32 B of every W row.
+// W and X tiles arrive by TMA (128-byte swizzle) into a ring of stages; one
+// thread issues the MMAs, accumulators live in tensor memory.  The work is
+// split stream-K: the (tile, k-block) units are cut into one contiguous range
+// per CTA (one CTA per SM), so every SM streams the same number of bytes.  A
+// tile cut between CTAs is reduced deterministically (fixed order of the
+// partial slots) by the last CTA to finish it, which then runs the epilogue.
+//
+// f32 path (CUDA cores): the same decomposition and epilogues; used by f32
+// models (small correctness configurations).
+//
+// Epilogues (applied once per finished tile, on 16-row chunks in shared memory):
+//   QKV    RMSNorm row scale, rotate-half RoPE on Q and K, Q pre-scaled by
+//          1/sqrt(hd) to f32, K and V appended to the KV cache.
+//   RESID  residual add into the f32 stream, the next GEMM input
+//          x = (h * g_next) in the model dtype, per-tile sums of h^2 for the
+//          next RMSNorm.
+//   SWIGLU RMSNorm row scale, silu(gate) * up.
+//   HEAD   RMSNorm row scale, optional logits, per-tile row summaries
+//          (top1, argmax, top2, sum exp); the last tile of the launch merges
+//          them per row and applies the draft pick or greedy acceptance.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <cudaTypedefs.h>
+
+#include "model.cuh"
+#include "stats.cuh"
+
+namespace spec {
+
+// ---------------------------------------------------------------------------
+// host: tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// split bookkeeping shared by host and device
+struct Split {
+    int n_tiles, kb;      // tiles of 128 features, k-blocks of 64
+    long long units;      // n_tiles * kb
+    int G;                // CTAs
+    int T_pad;            // row stride of the partial tiles
+    int max_slots;
+    float* part;          // [n_tiles][max_slots][T_pad][128]
+    int* counters;        // [n_tiles]
+};
+
+__host__ __device__ inline long long unit_begin(const Split& s, int c) { return (long long)c * s.units / s.G; }
+// CTA whose range holds unit u
+__host__ __device__ inline int cta_of(const Split& s, long long u) {
+    return (int)(((u + 1) * s.G - 1) / s.units);
+}
+
+// ---------------------------------------------------------------------------
+// epilogue shared memory
+struct EpiSmem {
+    float tile[kRowChunk][kTileN + 1];
+    float rs[kRowChunk];
+    int flag;
+    int wait_ok;
+};
+
+SPEC_DEV int etid() { return threadIdx.x & 127; }
+
+// per-chunk RMSNorm row scale
+SPEC_DEV void load_row_scale(const EpiParams& e, int j0, int nr, EpiSmem& sm) {
+    const int t = etid();
+    if (t < nr) {
+        const int r = e.r0 + j0 + t;
+        float s = 0.f;
+        for (int i = 0; i < e.ss_tiles; ++i) s += e.ss_in[(size_t)i * e.ss_stride + r];
+        sm.rs[t] = 1.0f / sqrtf(s * e.inv_d + e.eps);
+    }
+}
+
+template <typename KT>
+SPEC_DEV void apply_qkv(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
+    const int hd = e.head_dim, half = hd >> 1;
+    const int qd = e.n_heads * hd, kvd = e.n_kv_heads * hd;
+    for (int idx = etid(); idx < nr * kTileN; idx += 128) {
+        const int j = idx >> 7, mm = idx & 127;
+        const int n = tile * kTileN + mm;
+        if (n >= e.N) continue;
+        const int r = e.r0 + j0 + j;
+        const float v = sm.tile[j][mm] * sm.rs[j];
+        if (n < qd + kvd) {
+            const int i = n & (hd - 1);
+            const int pm = (i < half) ? mm + half : mm - half;
+            const float pv = sm.tile[j][pm] * sm.rs[j];
+            const int pos = e.plan.row_pos[r];
+            if (pos < 0 || pos >= e.max_position) { dev_error(e.err, SPEC_DEVERR_POSITION); continue; }
+            const int fi = i & (half - 1);
+            const float c = e.rope_cos[(size_t)pos * half + fi], s = e.rope_sin[(size_t)pos * half + fi];
+            const float o = (i < half) ? (v * c - pv * s) : (v * c + pv * s);
+            if (n < qd) {
+                e.q[(size_t)r * qd + n] = o * e.q_scale;
+            } else {
+                const int kvh = (n - qd) / hd;
+                const int seq = e.plan.row_seq[r], slot = e.plan.row_slot[r];
+                if (slot < 0 || slot >= e.kv_ctx) { dev_error(e.err, SPEC_DEVERR_CAPACITY); continue; }
+                const size_t off = ((((size_t)e.layer * e.kv_batch + seq) * e.n_kv_heads + kvh) * e.kv_ctx + slot) * hd + i;
+                static_cast<KT*>(e.kc)[off] = from_f32<KT>(o);
+            }
+        } else {
+            const int i = n & (hd - 1);
+            const int kvh = (n - qd - kvd) / hd;
+            const int seq = e.plan.row_seq[r], slot = e.plan.row_slot[r];
+            if (slot < 0 || slot >= e.kv_ctx) { dev_error(e.err, SPEC_DEVERR_CAPACITY); continue; }
+            const size_t off = ((((size_t)e.layer * e.kv_batch + seq) * e.n_kv_heads + kvh) * e.kv_ctx + slot) * hd + i;
+            static_cast<KT*>(e.vc)[off] = from_f32<KT>(v);
+        }
+    }
+}
+
+template <typename XT>
+SPEC_DEV void apply_resid(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
+    for (int idx = etid(); idx < nr * kTileN; idx += 128) {
+        const int j = idx >> 7, mm = idx & 127;
+        const int n = tile * kTileN + mm;
+        float sq = 0.f;
+        if (n < e.N) {
+            const int r = e.r0 + j0 + j;
+            const size_t o = (size_t)r * e.d_model + n;
+            const float hn = e.h[o] + sm.tile[j][mm];
+            e.h[o] = hn;
+            static_cast<XT*>(e.x_next)[o] = from_f32<XT>(hn * e.gain_next[n]);
+            sq = hn * hn;
+        }
+        sm.tile[j][mm] = sq;
+    }
+    named_bar(1, 128);
+    const int w = etid() >> 5, lane = etid() & 31;
+    for (int j = w; j < nr; j += 4) {
+        float s = sm.tile[j][lane] + sm.tile[j][lane + 32] + sm.tile[j][lane + 64] + sm.tile[j][lane + 96];
+        s = warp_sum(s);
+        if (lane == 0) e.ss_out[(size_t)tile * e.ss_stride + e.r0 + j0 + j] = s;
+    }
+}
+
+template <typename XT>
+SPEC_DEV void apply_swiglu(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
+    for (int idx = etid(); idx < nr * 64; idx += 128) {
+        const int j = idx >> 6, mm = idx & 63;
+        const int f = tile * 64 + mm;
+        if (f >= e.d_ff) continue;
+        const int r = e.r0 + j0 + j;
+        const float g = sm.tile[j][mm] * sm.rs[j];
+        const float u = sm.tile[j][mm + 64] * sm.rs[j];
+        static_cast<XT*>(e.act)[(size_t)r * e.d_ff + f] = from_f32<XT>(g / (1.0f + expf(-g)) * u);
+    }
+}
+
+SPEC_DEV void apply_head(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
+    for (int idx = etid(); idx < nr * kTileN; idx += 128) {
+        const int j = idx >> 7, mm = idx & 127;
+        const int v = tile * kTileN + mm;
+        float l = -INFINITY;
+        if (v < e.vocab) {
+            l = sm.tile[j][mm] * sm.rs[j];
+            if (e.logits) e.logits[(size_t)(e.r0 + j0 + j - e.logits_row0) * e.logits_stride + v] = l;
+        }
+        sm.tile[j][mm] = l;
+    }
+    named_bar(1, 128);
+    const int w = etid() >> 5, lane = etid() & 31;
+    for (int j = w; j < nr; j += 4) {
+        spec_row_stats s = stat_empty();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int mm = lane + 32 * i;
+            const int v = tile * kTileN + mm;
+            const float l = sm.tile[j][mm];
+            if (v < e.vocab) {
+                spec_row_stats one;
+                one.top1 = l; one.top2 = -INFINITY; one.sum_exp = 1.f; one.argmax = v;
+                stat_merge(s, one);
+            }
+        }
+        s = stat_warp_merge(s);
+        if (lane == 0) e.stat_part[(size_t)tile * e.ss_stride + e.r0 + j0 + j] = s;
+    }
+}
+
+template <typename XT>
+SPEC_DEV void apply_chunk(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
+    if (e.kind != EPI_RESID) {
+        load_row_scale(e, j0, nr, sm);
+        named_bar(1, 128);
+    }
+    switch (e.kind) {
+        case EPI_QKV: apply_qkv<XT>(e, tile, j0, nr, sm); break;
+        case EPI_RESID: apply_resid<XT>(e, tile, j0, nr, sm); break;
+        case EPI_SWIGLU: apply_swiglu<XT>(e, tile, j0, nr, sm); break;
+        default: apply_head(e, tile, j0, nr, sm); break;
+    }
+    named_bar(1, 128);
+}
+
+// Last tile of an LM-head launch: merge the per-tile summaries of every row of
+// the launch (warp per row, fixed order), then the draft pick or acceptance.
+SPEC_DEV void head_finalize(const EpiParams& e, int n_tiles) {
+    const int w = etid() >> 5, lane = etid() & 31;
+    for (int j = w; j < e.T; j += 4) {
+        const int r = e.r0 + j;
+        spec_row_stats s = stat_empty();
+        for (int t = lane; t < n_tiles; t += 32) stat_merge(s, e.stat_part[(size_t)t * e.ss_stride + r]);
+        s = stat_warp_merge(s);
+        if (lane == 0) {
+            e.row_stats[r] = s;
+            if (e.user_stats) e.user_stats[r] = s;
+            if (e.head_mode == HEAD_DRAFT) {
+                const int seq = e.plan.row_seq[r];
+                e.cand[(size_t)seq * e.cand_stride + e.cand_col] = s.argmax;
+            }
+        }
+    }
+    if (e.head_mode == HEAD_ACCEPT_CHAIN || e.head_mode == HEAD_ACCEPT_TREE) {
+        __threadfence();
+        named_bar(1, 128);
+        for (int b = etid(); b < e.batch; b += 128) {
+            const int r0 = e.plan.seq_row0[b], n = e.plan.seq_nrows[b];
+            const int* tok = e.tokens + (size_t)b * e.tok_stride;
+            int* path = e.path ? e.path + (size_t)b * kMaxSeqRows : nullptr;
+            if (e.head_mode == HEAD_ACCEPT_CHAIN)
+                accept_chain_one(e.row_stats, r0, n, tok, e.acc_len + b, e.next_tok + b, path);
+            else
+                accept_tree_one(e.row_stats, r0, n, tok, e.plan.tree_parent, e.plan.tree_depth,
+                                e.acc_len + b, e.next_tok + b, path);
+        }
+    }
+}
+
+// Called by all 128 epilogue threads after a tile's epilogue has run.
+SPEC_DEV void head_tile_done(const EpiParams& e, int n_tiles, EpiSmem& sm) {
+    if (e.kind != EPI_HEAD) return;
+    __threadfence();
+    named_bar(1, 128);
+    if (etid() == 0) sm.flag = (atomicAdd(e.done_counter, 1) == n_tiles - 1);
+    named_bar(1, 128);
+    if (sm.flag) {
+        __threadfence();
+        head_finalize(e, n_tiles);
+        if (etid() == 0) *e.done_counter = 0;
+    }
+    named_bar(1, 128);
+}
+
+// One finished segment of a tile.  `load(ch, v)` gives this thread's 16 values
+// (feature mm = etid(), rows ch*16 .. ch*16+15) of the segment's accumulator;
+// `release()` is called once every value has been read.
+template <typename XT, typename Loader>
+SPEC_DEV void finish_segment(const EpiParams& e, const Split& sp, int tile, int slot, int nc,
+                             EpiSmem& sm, Loader& ld) {
+    const int mm = etid();
+    const int nchunks = (e.T + kRowChunk - 1) / kRowChunk;
+    float v[16];
+    if (nc == 1) {
+        for (int ch = 0; ch < nchunks; ++ch) {
+            ld.load(ch, v);
+            const int nr = min(kRowChunk, e.T - ch * kRowChunk);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sm.tile[i][mm] = v[i];
+            named_bar(1, 128);
+            apply_chunk<XT>(e, tile, ch * kRowChunk, nr, sm);
+        }
+        ld.release();
+        head_tile_done(e, sp.n_tiles, sm);
+        return;
+    }
+    float* my = sp.part + ((size_t)tile * sp.max_slots + slot) * sp.T_pad * kTileN;
+    for (int ch = 0; ch < nchunks; ++ch) {
+        ld.load(ch, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int j = ch * kRowChunk + i;
+            if (j < e.T) my[(size_t)j * kTileN + mm] = v[i];
+        }
+    }
+    ld.release();
+    __threadfence();
+    named_bar(1, 128);
+    if (mm == 0) sm.flag = (atomicAdd(sp.counters + tile, 1) == nc - 1);
+    named_bar(1, 128);
+    if (!sm.flag) return;
+    __threadfence();
+    const float* base = sp.part + (size_t)tile * sp.max_slots * sp.T_pad * kTileN;
+    for (int ch = 0; ch < nchunks; ++ch) {
+        const int nr = min(kRowChunk, e.T - ch * kRowChunk);
+        for (int i = 0; i < nr; ++i) {
+            const int j = ch * kRowChunk + i;
+            float s = 0.f;
+            for (int q = 0; q < nc; ++q) s += __ldcg(base + ((size_t)q * sp.T_pad + j) * kTileN + mm);
+            sm.tile[i][mm] = s;
+        }
+        named_bar(1, 128);
+        apply_chunk<XT>(e, tile, ch * kRowChunk, nr, sm);
+    }
+    if (mm == 0) sp.counters[tile] = 0;
+    head_tile_done(e, sp.n_tiles, sm);
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 kernel
+constexpr int kTcThreads = 192;           // warps 0-3 epilogue, 4 TMA, 5 MMA
+constexpr uint32_t kATileBytes = kTileN * kTileK * 2;
+
+struct TcLayout {
+    int stages;
+    uint32_t b_bytes;
+    uint32_t tmem_cols;
+};
+
+__host__ __device__ inline size_t tc_smem_bytes(const TcLayout& L) {
+    return 1024 + (size_t)L.stages * (kATileBytes + L.b_bytes) + 256 + sizeof(EpiSmem) + 64;
+}
+
+struct TmemLoader {
+    uint32_t taddr;
+    uint64_t* acc_empty;
+    SPEC_DEV void load(int ch, float (&v)[16]) { tmem_ld16(taddr + ch * 16, v); }
+    SPEC_DEV void release() {
+        tc_fence_before();
+        mbar_arrive(acc_empty);
+    }
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+               Split sp, TcLayout L, EpiParams e) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = base;
+    uint8_t* sB = sA + (size_t)L.stages * kATileBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)L.stages * L.b_bytes);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + L.stages;
+    uint64_t* acc_full = bars + 2 * L.stages;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* drain = acc_full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 3);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    EpiSmem& sm = *reinterpret_cast<EpiSmem*>(reinterpret_cast<uint8_t*>(bars) + 256);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const long long u_begin = unit_begin(sp, c), u_end = unit_begin(sp, c + 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L.stages; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 128);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, L.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmW);
+            tma_prefetch_desc(&tmX);
+            const uint64_t pw = l2_policy_evict_first(), px = l2_policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            for (long long u = u_begin; u < u_end; ++u) {
+                const int tile = (int)(u / sp.kb), kb = (int)(u % sp.kb);
+                if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, e.err)) break;
+                mbar_arrive_expect_tx(full + stage, kATileBytes + L.b_bytes);
+                tma_load_2d(sA + (size_t)stage * kATileBytes, &tmW, kb * kTileK, tile * kTileN, full + stage, pw);
+                tma_load_2d(sB + (size_t)stage * L.b_bytes, &tmX, kb * kTileK, e.r0, full + stage, px);
+                ++issued;
+                if (++stage == L.stages) { stage = 0; phase ^= 1u; }
+            }
+            if (*abort_flag) {
+                // let copies still in flight land before the CTA exits
+                const long long n = issued < L.stages ? issued : L.stages;
+                for (long long i = 0; i < n; ++i) {
+                    if (--stage < 0) { stage = L.stages - 1; phase ^= 1u; }
+                    mbar_wait(full + stage, phase, nullptr, e.err);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, sp.T_pad);
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (long long u = u_begin; ok && u < u_end;) {
+                const int tile = (int)(u / sp.kb);
+                const long long seg_end = min(u_end, (long long)(tile + 1) * sp.kb);
+                if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, e.err)) break;
+                acc_phase ^= 1u;
+                tc_fence_after();
+                const long long seg_begin = u;
+                for (; u < seg_end; ++u) {
+                    if (!mbar_wait(full + stage, phase, abort_flag, e.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t ad = smem_desc_sw128(smem_u32(sA + (size_t)stage * kATileBytes));
+                    const uint64_t bd = smem_desc_sw128(smem_u32(sB + (size_t)stage * L.b_bytes));
+#pragma unroll
+                    for (int k = 0; k < kTileK / 16; ++k)
+                        tc_mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc, (u > seg_begin || k > 0) ? 1u : 0u);
+                    tc_commit(empty + stage);
+                    if (++stage == L.stages) { stage = 0; phase ^= 1u; }
+                }
+                if (ok) tc_commit(acc_full);
+            }
+            tc_commit(drain);
+            mbar_wait(drain, 0, nullptr, e.err);
+        }
+    } else {
+        TmemLoader ld;
+        ld.taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        ld.acc_empty = acc_empty;
+        uint32_t acc_phase = 0;
+        for (long long u = u_begin; u < u_end;) {
+            const int tile = (int)(u / sp.kb);
+            const long long seg_end = min(u_end, (long long)(tile + 1) * sp.kb);
+            const int first = cta_of(sp, (long long)tile * sp.kb);
+            const int last = cta_of(sp, (long long)(tile + 1) * sp.kb - 1);
+            // one thread waits (bounded) and broadcasts, so all 128 leave together
+            if (etid() == 0) sm.wait_ok = mbar_wait(acc_full, acc_phase, abort_flag, e.err) ? 1 : 0;
+            named_bar(1, 128);
+            const int ok = sm.wait_ok;
+            named_bar(1, 128);
+            if (!ok) break;
+            acc_phase ^= 1u;
+            tc_fence_after();
+            finish_segment<__nv_bfloat16>(e, sp, tile, c - first, last - first + 1, sm, ld);
+            u = seg_end;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L.tmem_cols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// f32 CUDA-core kernel (f32 models)
+constexpr int kSimtMaxT = 32;
+constexpr int kSimtK = 32;
+
+struct SmemTileLoader {
+    const float* acc;   // [kSimtMaxT][129]
+    SPEC_DEV void load(int ch, float (&v)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = acc[(ch * 16 + i) * (kTileN + 1) + etid()];
+    }
+    SPEC_DEV void release() {}
+};
+
+__global__ void __launch_bounds__(128)
+gemm_f32_kernel(const float* __restrict__ W, const float* __restrict__ X, int x_stride, int N, int K,
+                Split sp, EpiParams e) {
+    union WorkSmem {
+        float w[kTileN][kSimtK + 1];               // weight sub-tile
+        float acc[kSimtMaxT * (kTileN + 1)];       // finished segment, rows x features
+    };
+    __shared__ WorkSmem ws;
+    __shared__ float sX[kSimtMaxT][kSimtK + 1];
+    __shared__ EpiSmem sm;
+    const int c = blockIdx.x, t = threadIdx.x;
+    const long long u_begin = unit_begin(sp, c), u_end = unit_begin(sp, c + 1);
+    for (long long u = u_begin; u < u_end;) {
+        const int tile = (int)(u / sp.kb);
+        const long long seg_end = min(u_end, (long long)(tile + 1) * sp.kb);
+        float acc[kSimtMaxT];
+#pragma unroll
+        for (int j = 0; j < kSimtMaxT; ++j) acc[j] = 0.f;
+        for (; u < seg_end; ++u) {
+            const int kb = (int)(u % sp.kb);
+            for (int k0 = 0; k0 < kTileK; k0 += kSimtK) {
+                __syncthreads();
+                for (int i = t; i < kTileN * kSimtK; i += 128) {
+                    const int rr = i / kSimtK, kk = i % kSimtK;
+                    const int n = tile * kTileN + rr, k = kb * kTileK + k0 + kk;
+                    ws.w[rr][kk] = (n < N && k < K) ? W[(size_t)n * K + k] : 0.f;
+                }
+                for (int i = t; i < kSimtMaxT * kSimtK; i += 128) {
+                    const int j = i / kSimtK, kk = i % kSimtK;
+                    const int k = kb * kTileK + k0 + kk;
+                    sX[j][kk] = (j < e.T && k < K) ? X[(size_t)(e.r0 + j) * x_stride + k] : 0.f;
+                }
+                __syncthreads();
+                for (int kk = 0; kk < kSimtK; ++kk) {
+                    const float w = ws.w[t][kk];
+#pragma unroll
+                    for (int j = 0; j < kSimtMaxT; ++j) acc[j] = fmaf(w, sX[j][kk], acc[j]);
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kSimtMaxT; ++j) ws.acc[j * (kTileN + 1) + t] = acc[j];
+        __syncthreads();
+        const int first = cta_of(sp, (long long)tile * sp.kb);
+        const int last = cta_of(sp, (long long)(tile + 1) * sp.kb - 1);
+        SmemTileLoader ld{ws.acc};
+        finish_segment<float>(e, sp, tile, c - first, last - first + 1, sm, ld);
+        __syncthreads();
+        u = seg_end;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host launch
+static int max_slots_of(const Split& s) {
+    int mx = 1;
+    for (int t = 0; t < s.n_tiles; ++t) {
+        const int a = cta_of(s, (long long)t * s.kb), b = cta_of(s, (long long)(t + 1) * s.kb - 1);
+        mx = std::max(mx, b - a + 1);
+    }
+    return mx;
+}
+
+static Split make_split(const spec_model* m, int N, int K, int T_pad) {
+    Split s{};
+    s.n_tiles = (N + kTileN - 1) / kTileN;
+    s.kb = (K + kTileK - 1) / kTileK;
+    s.units = (long long)s.n_tiles * s.kb;
+    s.G = (int)std::min<long long>(m->num_sms, s.units);
+    s.T_pad = T_pad;
+    s.max_slots = max_slots_of(s);
+    return s;
+}
+
+size_t gemm_partial_floats_needed(const spec_model* m, int N, int K, int T_pad) {
+    Split s = make_split(m, N, K, T_pad);
+    return (size_t)s.n_tiles * s.max_slots * T_pad * kTileN;
+}
+
+int gemm_grid(const spec_model* m, int N, int K) { return make_split(m, N, K, 16).G; }
+
+static TcLayout tc_layout(int T_pad) {
+    TcLayout L;
+    L.b_bytes = (uint32_t)T_pad * kTileK * 2;
+    const size_t budget = 225 * 1024 - 1024 - 256 - sizeof(EpiSmem) - 64;
+    L.stages = (int)std::min<size_t>(8, budget / (kATileBytes + L.b_bytes));
+    uint32_t cols = 32;
+    while (cols < (uint32_t)T_pad) cols <<= 1;
+    L.tmem_cols = cols;
+    return L;
+}
+
+int launch_gemm(spec_model* m, const GemmLaunch& g, EpiParams e, int xbuf, cudaStream_t st) {
+    const int T_total = e.T, r_base = e.r0;
+    const int max_t = m->bf16 ? kMaxTPad : kSimtMaxT;
+    for (int done = 0; done < T_total; done += max_t) {
+        EpiParams ec = e;
+        ec.T = std::min(max_t, T_total - done);
+        ec.r0 = r_base + done;
+        if (ec.kind == EPI_HEAD && (e.head_mode == HEAD_ACCEPT_CHAIN || e.head_mode == HEAD_ACCEPT_TREE) &&
+            done + max_t < T_total)
+            ec.head_mode = HEAD_STATS;   // acceptance once every row has its summary
+        const int T_pad = m->bf16 ? ((ec.T + 15) / 16) * 16 : kSimtMaxT;
+        Split s = make_split(m, g.N, g.K, T_pad);
+        s.part = m->gemm_part;
+        s.counters = m->counters;
+        if ((size_t)s.n_tiles * s.max_slots * T_pad * kTileN > m->gemm_part_floats || s.n_tiles > m->n_counters - 1)
+            return set_error(SPEC_ERR_CAPACITY, "GEMM workspace too small for this launch");
+        const int slot = prof_start(m, st);
+        if (m->bf16) {
+            TcLayout L = tc_layout(T_pad);
+            const size_t smem = tc_smem_bytes(L);
+            static bool attr_set = false;
+            if (!attr_set) {
+                cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+                attr_set = true;
+            }
+            gemm_tc_kernel<<<s.G, kTcThreads, smem, st>>>(*g.tmW, m->tm_x[xbuf][T_pad / 16 - 1], s, L, ec);
+        } else {
+            gemm_f32_kernel<<<s.G, 128, 0, st>>>(static_cast<const float*>(g.W), static_cast<const float*>(g.X),
+                                                 g.x_stride, g.N, g.K, s, ec);
+        }
+        ++m->launches;
+        // algorithmic bytes: weights once, activation rows in, output rows out
+        prof_stop(m, slot, st, PROF_GEMM,
+                  (double)g.N * g.K * m->elem + (double)ec.T * g.K * m->elem + (double)ec.T * g.N * m->elem);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return check_cuda(err, "GEMM launch");
+    }
+    return SPEC_OK;
+}
+
+}  // namespace spec

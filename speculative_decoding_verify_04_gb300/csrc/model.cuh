@@ -1,0 +1,222 @@
+// Library-internal structures shared by the translation units of libspec.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace spec {
+
+constexpr int kMaxSeqRows = 64;       // rows of one sequence in one call
+constexpr int kMaxPlanBatch = 256;    // sequences described in one plan
+constexpr int kTileN = 128;           // W rows (output features) per GEMM tile
+constexpr int kTileK = 64;            // K per pipeline stage: 64 bf16 = 128 B rows
+constexpr int kMaxTPad = 256;         // activation rows per tcgen05 pass (MMA N)
+constexpr int kRowChunk = 16;         // epilogue granularity (tcgen05.ld .x16)
+
+enum EpiKind : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_HEAD = 3 };
+enum HeadMode : int { HEAD_STATS = 0, HEAD_DRAFT = 1, HEAD_ACCEPT_CHAIN = 2, HEAD_ACCEPT_TREE = 3 };
+
+// Row plan of one forward call: rows of all sequences back to back.
+struct RowPlan {
+    int* row_seq;      // [max_rows] sequence of the row
+    int* row_slot;     // [max_rows] KV slot written by the row
+    int* row_pos;      // [max_rows] rotary position id
+    int* row_local;    // [max_rows] index of the row within its sequence
+    int* seq_row0;     // [max_batch] first row of the sequence
+    int* seq_nrows;    // [max_batch] rows of the sequence
+    int* seq_base;     // [max_batch] committed length when the plan was made
+    int* tree_parent;  // [kMaxSeqRows] parent of each local row (-1 root); tree mode only
+    int* tree_depth;   // [kMaxSeqRows]
+};
+
+// Parameters of the plan kernel, passed by value.
+struct PlanParams {
+    int batch;
+    int mode;                        // 0 chain, 1 tree, 2 one-row-per-sequence draft pass
+    int pass;                        // draft pass index j (mode 2)
+    int n_rows[kMaxPlanBatch];
+    int parent[kMaxSeqRows];
+    int depth[kMaxSeqRows];
+};
+
+struct LayerWeights {
+    void* qkv;       // [(H + 2 Hkv) hd][d]
+    void* o;         // [d][H hd]
+    void* gu;        // [2 * ceil(F/64) * 64][d]: per 64-block: 64 gate rows then 64 up rows
+    void* down;      // [d][F]
+    float* attn_g;   // [d]
+    float* ffn_g;    // [d]
+    CUtensorMap tm_qkv, tm_o, tm_gu, tm_down;
+};
+
+struct GemmShape {
+    int N;           // output features (rows of W, packed)
+    int K;           // input features
+};
+
+}  // namespace spec
+
+struct spec_model {
+    spec_model_config cfg;
+    int device = 0;
+    int num_sms = 0;
+    bool bf16 = true;
+    size_t elem = 2;                 // bytes per weight / KV element
+    int qkv_n = 0, gu_n = 0;         // packed output widths
+    int max_rows_pad = 0;            // max_rows rounded up to 16
+    int x_cols = 0;                  // widest activation row (d, H hd, F)
+
+    char* wmem = nullptr;            // packed weights (one allocation)
+    void* embed = nullptr;           // [V][d]
+    void* head = nullptr;            // [V][d]
+    float* final_g = nullptr;        // [d]
+    CUtensorMap tm_head;
+    std::vector<spec::LayerWeights> layers;
+    float* rope_cos = nullptr;       // [max_position][hd/2]
+    float* rope_sin = nullptr;
+
+    char* ws = nullptr;              // workspace (one allocation)
+    size_t ws_bytes = 0;
+    float* h = nullptr;              // [max_rows][d] f32 residual stream
+    void* x_in = nullptr;            // [max_rows_pad][d]   GEMM input: gained residual (model dtype)
+    void* x_attn = nullptr;          // [max_rows_pad][H hd] attention output
+    void* x_act = nullptr;           // [max_rows_pad][F]   SwiGLU output
+    float* q = nullptr;              // [max_rows][H hd] rotated, pre-scaled queries
+    float* ss_part = nullptr;        // [d/128][max_rows] per-tile sums of squares of h
+    spec_row_stats* stat_part = nullptr;  // [ceil(V/128)][max_rows]
+    spec_row_stats* row_stats = nullptr;  // [max_rows]
+    float* gemm_part = nullptr;      // split-K partial tiles
+    size_t gemm_part_floats = 0;
+    int* counters = nullptr;         // tile arrival counters (zero between launches)
+    int n_counters = 0;
+    float* attn_part = nullptr;      // attention split partials
+    size_t attn_part_floats = 0;
+    int* attn_counters = nullptr;
+    int n_attn_counters = 0;
+    int* err = nullptr;              // device error word
+    int* scratch_i32 = nullptr;      // small device scratch (path, acc staging)
+    spec::RowPlan plan;
+
+    // X tensor maps by buffer (0 x_in, 1 x_attn, 2 x_act) and T_pad/16 - 1
+    CUtensorMap tm_x[3][spec::kMaxTPad / 16];
+
+    // tracing: kernel launches issued, and (when enabled) CUDA events around
+    // every GEMM / attention launch with the launch's algorithmic bytes
+    long long launches = 0;
+    bool prof_on = false;
+    std::vector<cudaEvent_t> prof_ev;      // start/stop pairs
+    std::vector<int> prof_kind;
+    std::vector<double> prof_bytes;
+    size_t prof_n = 0;
+};
+
+struct spec_kv {
+    spec_model* m = nullptr;
+    int batch = 0;
+    int max_ctx = 0;
+    void* k = nullptr;               // [layer][seq][kvh][slot][hd]
+    void* v = nullptr;
+    int* len = nullptr;              // [batch] committed lengths (device)
+};
+
+namespace spec {
+
+// error reporting (capi.cu)
+int set_error(int code, const std::string& msg);
+int check_cuda(cudaError_t e, const char* what);
+
+// tracing (capi.cu): bracket one kernel launch with events when enabled
+enum ProfKind : int { PROF_GEMM = 0, PROF_ATTN = 1 };
+int prof_start(spec_model* m, cudaStream_t st);
+void prof_stop(spec_model* m, int slot, cudaStream_t st, int kind, double bytes);
+
+// tensor maps (gemm.cu)
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// Epilogue parameters of one GEMM launch (passed by value).
+struct EpiParams {
+    int kind;               // EpiKind
+    int T;                  // rows of this launch
+    int r0;                 // first row (of the plan) of this launch
+    int N;                  // real output features of the GEMM
+    int layer;
+    // RMSNorm row scale: rs[r] = rsqrt(sum_t ss_part[t][r] / d + eps)
+    const float* ss_in;
+    int ss_tiles;
+    int ss_stride;
+    float inv_d, eps;
+    RowPlan plan;
+    int* err;
+    // QKV
+    float* q;
+    void* kc; void* vc;     // cache bases
+    int kv_batch, kv_ctx;   // cache geometry
+    int n_heads, n_kv_heads, head_dim;
+    const float* rope_cos; const float* rope_sin;
+    int max_position;
+    float q_scale;
+    // residual
+    float* h;
+    const float* gain_next;
+    void* x_next;
+    float* ss_out;
+    int d_model;
+    // SwiGLU
+    void* act;
+    int d_ff;
+    // LM head
+    float* logits;          // nullable; row r goes to logits[(r - logits_row0) * logits_stride]
+    int logits_stride, logits_row0;
+    spec_row_stats* stat_part;
+    spec_row_stats* row_stats;
+    spec_row_stats* user_stats;   // nullable
+    int vocab;
+    int head_mode;
+    int* done_counter;
+    // draft / acceptance outputs
+    int* cand; int cand_stride; int cand_col;   // draft: cand[seq*stride + col] = argmax
+    const int* tokens; int tok_stride;           // acceptance: row tokens
+    int* acc_len; int* next_tok; int* path;
+    int batch;
+};
+
+struct GemmLaunch {
+    const CUtensorMap* tmW;
+    const CUtensorMap* tmX;
+    const void* W;          // f32 path
+    const void* X;          // f32 path
+    int x_stride;           // f32 path: elements per X row
+    int N, K;
+};
+
+// gemm.cu
+int launch_gemm(spec_model* m, const GemmLaunch& g, EpiParams e, int xbuf, cudaStream_t st);
+size_t gemm_partial_floats_needed(const spec_model* m, int N, int K, int T_pad);
+int gemm_grid(const spec_model* m, int N, int K);
+
+// attention.cu
+struct AttnParams {
+    const float* q;         // [rows][H hd]
+    const void* kc; const void* vc;
+    void* out;              // [rows][H hd] model dtype (O-projection input)
+    RowPlan plan;
+    int batch, kv_batch, kv_ctx, layer;
+    int n_heads, n_kv_heads, head_dim;
+    int tree;               // 0 chain, 1 tree
+    int splits;
+    float* part;
+    int* counters;
+    int* err;
+};
+int launch_attention(spec_model* m, const AttnParams& a, int max_rows_per_seq, cudaStream_t st);
+size_t attn_partial_floats_needed(const spec_model* m, int batch, int max_rows_per_seq);
+
+// accept.cu
+SPEC_DEV void stat_merge(spec_row_stats& a, const spec_row_stats& b);
+
+}  // namespace spec

@@ -1,0 +1,312 @@
+"""Thin Python binding of libspec.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of its own: it checks shapes, passes raw device pointers of torch
+tensors and the current CUDA stream, and raises :class:`SpecError` with the
+library's message on a non-zero status.  If the compiled library is missing
+the loader raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_double, c_float, c_int32, c_void_p
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libspec.so")
+
+SPEC_DTYPE_F32 = 0
+SPEC_DTYPE_BF16 = 1
+DEVERR_TOKEN, DEVERR_CAPACITY, DEVERR_TIMEOUT, DEVERR_POSITION = 1, 2, 4, 8
+MAX_SEQ_ROWS = 64
+EXPORTS = [
+    "spec_last_error", "spec_device_info", "spec_model_create", "spec_model_destroy", "spec_device_error",
+    "spec_kv_create", "spec_kv_destroy", "spec_kv_set_lengths", "spec_kv_get_lengths", "spec_kv_import",
+    "spec_kv_export", "spec_prefill", "spec_draft", "spec_verify", "spec_accept", "spec_accept_greedy",
+    "kv_commit", "spec_row_probs", "spec_schedule_k", "spec_profile", "spec_profile_read", "spec_launch_count",
+]
+
+
+class SpecError(RuntimeError):
+    pass
+
+
+class ModelConfig(ctypes.Structure):
+    _fields_ = [(n, c_int32) for n in ("n_layers", "d_model", "n_heads", "n_kv_heads", "head_dim", "d_ff",
+                                       "vocab", "exit_layer", "dtype", "max_rows", "max_batch", "max_position")] + \
+               [("rms_eps", c_float), ("rope_theta", c_float)]
+
+
+class KSchedule(ctypes.Structure):
+    _fields_ = [("min_k", c_int32), ("max_k", c_int32), ("low", c_double), ("high", c_double), ("decay", c_double)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libspec.so once; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise SpecError(f"{path} is missing: build it with speculative_decoding_verify_04_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I = c_void_p, c_int32
+    sig = {
+        "spec_last_error": ([], ctypes.c_char_p),
+        "spec_device_info": ([POINTER(I), POINTER(I), POINTER(I)], I),
+        "spec_model_create": ([POINTER(ModelConfig), POINTER(P), P, POINTER(P)], I),
+        "spec_model_destroy": ([P], None),
+        "spec_device_error": ([P, POINTER(I)], I),
+        "spec_kv_create": ([P, I, I, POINTER(P)], I),
+        "spec_kv_destroy": ([P], None),
+        "spec_kv_set_lengths": ([P, POINTER(I), P], I),
+        "spec_kv_get_lengths": ([P, POINTER(I), P], I),
+        "spec_kv_import": ([P, I, I, I, I, I, P, P, P], I),
+        "spec_kv_export": ([P, I, I, I, I, I, P, P, P], I),
+        "spec_prefill": ([P, P, I, P, I, P, P, P], I),
+        "spec_draft": ([P, P, I, P, I, P, P, P, P], I),
+        "spec_verify": ([P, P, I, POINTER(I), P, I, P, I, POINTER(I), P, P, P, P, P, P], I),
+        "spec_accept": ([P, P, P, P, I, I, I, P, P, P], I),
+        "spec_accept_greedy": ([P, P, POINTER(I), I, I, I, P, P, P, P], I),
+        "kv_commit": ([P, I, P, P, I, P], I),
+        "spec_row_probs": ([P, I, P, P], I),
+        "spec_schedule_k": ([P, POINTER(I), P, P, I, POINTER(KSchedule), P, P, P], I),
+        "spec_profile": ([P, I], I),
+        "spec_profile_read": ([P, I, POINTER(c_double), POINTER(c_double), POINTER(I)], I),
+        "spec_launch_count": ([P, POINTER(ctypes.c_int64)], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(rc):
+    if rc != 0:
+        raise SpecError(f"libspec error {rc}: {_lib.spec_last_error().decode()}")
+
+
+def _ptr(t):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return c_void_p(s.cuda_stream)
+
+
+def _i32_array(vals):
+    vals = [int(v) for v in vals]
+    return (c_int32 * len(vals))(*vals)
+
+
+def _need(t, dtype, name, numel=None):
+    if t is None:
+        return
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise SpecError(f"{name}: need a contiguous CUDA {dtype} tensor")
+    if numel is not None and t.numel() < numel:
+        raise SpecError(f"{name}: needs at least {numel} elements, has {t.numel()}")
+
+
+def device_info():
+    lib = load()
+    a, b, c = c_int32(), c_int32(), c_int32()
+    _check(lib.spec_device_info(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+class Model:
+    """A packed model on the current device (owns the library handle)."""
+
+    def __init__(self, shape, weights, max_rows=64, max_batch=8, max_position=8192, stream=None):
+        lib = load()
+        self.shape = shape
+        dt = SPEC_DTYPE_BF16 if shape.dtype == "bf16" else SPEC_DTYPE_F32
+        self.torch_dtype = torch.bfloat16 if dt == SPEC_DTYPE_BF16 else torch.float32
+        cfg = ModelConfig(shape.n_layers if weights is None else len(weights["layers"]), shape.d_model,
+                          shape.n_heads, shape.n_kv_heads, shape.head_dim, shape.d_ff, shape.vocab,
+                          shape.exit_layer, dt, max_rows, max_batch, max_position, shape.rms_eps, shape.rope_theta)
+        self.cfg = cfg
+        order = [weights["embed"], weights["lm_head"], weights["final_norm"]]
+        for lw in weights["layers"]:
+            order += [lw[k] for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")]
+        for t in order:
+            _need(t, self.torch_dtype, "weight")
+        arr = (c_void_p * len(order))(*[t.data_ptr() for t in order])
+        h = c_void_p()
+        _check(lib.spec_model_create(ctypes.byref(cfg), arr, _stream(stream), ctypes.byref(h)))
+        self.handle = h
+        self.n_layers = cfg.n_layers
+
+    def profile(self, enable):
+        _check(load().spec_profile(self.handle, 1 if enable else 0))
+
+    def profile_read(self, kind):
+        """(total ms, algorithmic bytes, launches) of kind 0 = GEMM, 1 = attention."""
+        ms, by, n = c_double(), c_double(), c_int32()
+        _check(load().spec_profile_read(self.handle, kind, ctypes.byref(ms), ctypes.byref(by), ctypes.byref(n)))
+        return ms.value, by.value, n.value
+
+    def launch_count(self):
+        c = ctypes.c_int64()
+        _check(load().spec_launch_count(self.handle, ctypes.byref(c)))
+        return c.value
+
+    def device_error(self):
+        v = c_int32()
+        _check(load().spec_device_error(self.handle, ctypes.byref(v)))
+        return v.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            load().spec_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class KVCache:
+    """KV cache of ``batch`` sequences x ``max_ctx`` slots (owns the library handle)."""
+
+    def __init__(self, model: Model, batch, max_ctx):
+        self.model = model
+        self.batch = batch
+        self.max_ctx = max_ctx
+        h = c_void_p()
+        _check(load().spec_kv_create(model.handle, batch, max_ctx, ctypes.byref(h)))
+        self.handle = h
+
+    def set_lengths(self, lens, stream=None):
+        _check(load().spec_kv_set_lengths(self.handle, _i32_array(lens), _stream(stream)))
+
+    def get_lengths(self, stream=None):
+        arr = (c_int32 * self.batch)()
+        _check(load().spec_kv_get_lengths(self.handle, arr, _stream(stream)))
+        return list(arr)
+
+    def import_rows(self, seq, layer0, k, v, slot0=0, stream=None):
+        """k, v: CUDA tensors [n_layers][n_slots][Hkv][hd] in the model dtype."""
+        _need(k, self.model.torch_dtype, "k")
+        _need(v, self.model.torch_dtype, "v")
+        _check(load().spec_kv_import(self.handle, seq, layer0, k.shape[0], slot0, k.shape[1], _ptr(k), _ptr(v),
+                                     _stream(stream)))
+
+    def export_rows(self, seq, layer0, n_layers, slot0, n_slots, stream=None):
+        s = self.model.shape
+        k = torch.empty((n_layers, n_slots, s.n_kv_heads, s.head_dim), dtype=self.model.torch_dtype, device="cuda")
+        v = torch.empty_like(k)
+        _check(load().spec_kv_export(self.handle, seq, layer0, n_layers, slot0, n_slots, _ptr(k), _ptr(v),
+                                     _stream(stream)))
+        return k, v
+
+    def close(self):
+        if getattr(self, "handle", None):
+            load().spec_kv_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def spec_prefill(model, kv, seq, tokens, last_logits=None, next_tok=None, stream=None):
+    _need(tokens, torch.int32, "tokens")
+    _need(last_logits, torch.float32, "last_logits", model.cfg.vocab)
+    _need(next_tok, torch.int32, "next_tok", 1)
+    _check(load().spec_prefill(model.handle, kv.handle, seq, _ptr(tokens), tokens.numel(), _ptr(last_logits),
+                               _ptr(next_tok), _stream(stream)))
+
+
+def spec_draft(model, kv, t0, k, cand, h_L, draft_logits=None, stream=None):
+    B = t0.numel()
+    _need(t0, torch.int32, "t0")
+    _need(cand, torch.int32, "cand", B * (k + 1))
+    _need(h_L, torch.float32, "h_L", B * (k + 1) * model.cfg.d_model)
+    _need(draft_logits, torch.float32, "draft_logits", B * k * model.cfg.vocab)
+    _check(load().spec_draft(model.handle, kv.handle, B, _ptr(t0), k, _ptr(cand), _ptr(h_L), _ptr(draft_logits),
+                             _stream(stream)))
+
+
+def spec_verify(model, kv, n_rows, tokens, tok_stride, h_in=None, h_stride=0, tree_parent=None, logits=None,
+                stats=None, acc_len=None, next_tok=None, path=None, stream=None):
+    B = len(n_rows)
+    T = sum(int(n) for n in n_rows)
+    _need(tokens, torch.int32, "tokens", B * tok_stride)
+    _need(h_in, torch.float32, "h_in", B * h_stride * model.cfg.d_model if h_in is not None else None)
+    _need(logits, torch.float32, "logits", T * model.cfg.vocab)
+    _need(stats, torch.float32, "stats", T * 4)
+    _need(acc_len, torch.int32, "acc_len", B)
+    _need(next_tok, torch.int32, "next_tok", B)
+    _need(path, torch.int32, "path", B * MAX_SEQ_ROWS)
+    tp = _i32_array(tree_parent) if tree_parent is not None else None
+    _check(load().spec_verify(model.handle, kv.handle, B, _i32_array(n_rows), _ptr(h_in), h_stride, _ptr(tokens),
+                              tok_stride, tp, _ptr(logits), _ptr(stats), _ptr(acc_len), _ptr(next_tok), _ptr(path),
+                              _stream(stream)))
+
+
+def spec_accept(p, q, draft, u, acc_len, next_tok, stream=None):
+    B, k1, V = p.shape
+    k = k1 - 1
+    _need(p, torch.float32, "p")
+    _need(q, torch.float32, "q", B * k * V)
+    _need(draft, torch.int32, "draft", B * k)
+    _need(u, torch.float32, "u", B * (k + 1))
+    _need(acc_len, torch.int32, "acc_len", B)
+    _need(next_tok, torch.int32, "next_tok", B)
+    _check(load().spec_accept(_ptr(p), _ptr(q), _ptr(draft), _ptr(u), B, k, V, _ptr(acc_len), _ptr(next_tok),
+                              _stream(stream)))
+
+
+def spec_accept_greedy(logits, tokens, acc_len, next_tok, tree_parent=None, path=None, stream=None):
+    B, n, V = logits.shape
+    _need(logits, torch.float32, "logits")
+    _need(tokens, torch.int32, "tokens", B * n)
+    _need(path, torch.int32, "path", B * MAX_SEQ_ROWS)
+    tp = _i32_array(tree_parent) if tree_parent is not None else None
+    _check(load().spec_accept_greedy(_ptr(logits), _ptr(tokens), tp, B, n, V, _ptr(acc_len), _ptr(next_tok),
+                                     _ptr(path), _stream(stream)))
+
+
+def kv_commit(kv, acc_len, path=None, path_stride=MAX_SEQ_ROWS, batch=None, stream=None):
+    _need(acc_len, torch.int32, "acc_len")
+    _need(path, torch.int32, "path")
+    B = acc_len.numel() if batch is None else batch
+    _check(load().kv_commit(kv.handle, B, _ptr(acc_len), _ptr(path), path_stride, _stream(stream)))
+
+
+def spec_row_probs(stats, out, rows=None, stream=None):
+    rows = stats.shape[0] if rows is None else rows
+    _need(stats, torch.float32, "stats", rows * 4)
+    _need(out, torch.float64, "out", rows * 2)
+    _check(load().spec_row_probs(_ptr(stats), rows, _ptr(out), _stream(stream)))
+
+
+def spec_schedule_k(top_probs, n_rows, acc_len, ema, k_next, conf=None, min_k=2, max_k=16, low=0.3, high=0.8,
+                    decay=0.9, stream=None):
+    B = len(n_rows)
+    _need(top_probs, torch.float64, "top_probs", 2 * sum(n_rows))
+    _need(acc_len, torch.int32, "acc_len", B)
+    _need(ema, torch.float64, "ema", B)
+    _need(k_next, torch.int32, "k_next", B)
+    _need(conf, torch.float64, "conf", B)
+    sch = KSchedule(min_k, max_k, low, high, decay)
+    _check(load().spec_schedule_k(_ptr(top_probs), _i32_array(n_rows), _ptr(acc_len), _ptr(ema), B,
+                                  ctypes.byref(sch), _ptr(k_next), _ptr(conf), _stream(stream)))
+
+
+def stats_argmax(stats):
+    """argmax column of a [rows, 4] float32 stats tensor (spec_row_stats)."""
+    return stats.view(torch.int32)[:, 3]

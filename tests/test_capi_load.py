@@ -1,0 +1,41 @@
+"""The C-ABI library builds, loads without a GPU and exports every declared symbol."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while")))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("spec_draft", "spec_verify", "spec_accept", "kv_commit", "spec_model_create", "spec_kv_create",
+              "spec_prefill", "spec_schedule_k"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    from speculative_decoding_verify_04_gb300 import build, spec
+    path = build.build()
+    lib = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert sorted(spec.EXPORTS) == declared_functions()
+    spec.load(path)
+    assert spec.load().spec_last_error() == b""
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "speculative_decoding_verify_04_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f

@@ -1,0 +1,166 @@
+"""bf16 models on the tcgen05 path against the float64 oracle.
+
+* tree verification (8 layers, d 1024, 16 query / 4 KV heads x 64, FFN 2816,
+  vocab 32000): prefill of a random prompt, a [4, 2, 2] token tree (28 nodes
+  plus the root, level order, ancestor-only mask, depth position ids) with a
+  planted greedy path, fused greedy longest-path acceptance, KV commit of the
+  path; full size at a 2048-token context, and a 2-layer / 200-token case;
+* layer-skip chain rounds on the 7B layer shape (d 4096, 32 heads x 128,
+  FFN 11008, vocab 32000) with 4 layers and the draft = 2 layers, batch 2
+  with different context lengths.
+
+Logits within 2e-2 absolute; acceptance, next token, path and lengths exact
+unless the oracle's top-1 / top-2 gap is below 1e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _gpu_util import assert_tokens_match, cuda_i32, lib, model_pair, top_gap
+from oracle import accept as A
+from oracle import spec as OS
+from oracle.accept import argmax_lowest
+from synthetic import SHAPES, make_tokens, tree_parents
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+def _tree_case(n_layers, prompt_len, seed):
+    from speculative_decoding_verify_04_gb300 import spec
+    lib()
+    model, dec, shape = model_pair(SHAPES["tree8"], seed=seed, n_layers=n_layers, max_rows=64, max_batch=1,
+                                   max_position=prompt_len + 64)
+    prompt = make_tokens(prompt_len, shape.vocab, seed=seed)
+    ctx = prompt_len + 40
+    kv = spec.KVCache(model, 1, ctx)
+    last = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+    spec.spec_prefill(model, kv, 0, cuda_i32(prompt), last, None)
+    cache = dec.new_cache(ctx)
+    ref = dec.prefill(cache, prompt)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(last.cpu().numpy(), ref, atol=TOL, rtol=0)
+
+    par = tree_parents([4, 2, 2])
+    t0 = argmax_lowest(ref)
+    greedy = OS.generate_greedy_ar(dec, prompt, 4)     # t0 and the next three greedy tokens
+    assert greedy[0] == t0
+    toks = make_tokens(29, shape.vocab, seed=seed + 1)
+    toks[0] = t0
+    toks[3] = greedy[1]          # node 3 (depth 1) -> child 10 (depth 2) -> child 23 (depth 3)
+    toks[10] = greedy[2]
+    toks[23] = greedy[3]
+    s = cache.length
+    d_ref, node_ref, path_ref, nxt_ref, logits_ref = OS.tree_round_greedy(dec, cache, toks, par)
+
+    logits = torch.empty((29, shape.vocab), dtype=torch.float32, device="cuda")
+    stats = torch.empty((29, 4), dtype=torch.float32, device="cuda")
+    acc = torch.empty(1, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+    path = torch.full((1, 64), -1, dtype=torch.int32, device="cuda")
+    tk = cuda_i32(toks)
+    spec.spec_verify(model, kv, [29], tk, 29, tree_parent=list(par), logits=logits, stats=stats, acc_len=acc,
+                     next_tok=nxt, path=path)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    err = np.abs(lg - logits_ref).max()
+    assert err < TOL, err
+    am = spec.stats_argmax(stats).cpu().numpy()
+    np.testing.assert_array_equal(am, lg.argmax(-1))
+    gaps = [top_gap(r) for r in logits_ref]
+    if min(gaps[i] for i in path_ref) >= 1e-2:
+        assert (acc.item(), nxt.item()) == (d_ref, nxt_ref)
+        assert list(path.cpu().numpy()[0, :d_ref + 1]) == path_ref
+        assert d_ref == 3
+    # unfused acceptance on the same logits agrees with the fused one
+    acc2 = torch.empty(1, dtype=torch.int32, device="cuda")
+    nxt2 = torch.empty(1, dtype=torch.int32, device="cuda")
+    path2 = torch.full((1, 64), -1, dtype=torch.int32, device="cuda")
+    spec.spec_accept_greedy(logits.view(1, 29, -1), tk.view(1, 29), acc2, nxt2, tree_parent=list(par), path=path2)
+    torch.cuda.synchronize()
+    assert (acc2.item(), nxt2.item()) == (acc.item(), nxt.item())
+    assert torch.equal(path2[:, :acc.item() + 1], path[:, :acc.item() + 1])
+
+    spec.kv_commit(kv, acc, path)
+    torch.cuda.synchronize()
+    a = acc.item()
+    assert kv.get_lengths() == [s + a + 1]
+    if a == d_ref:
+        kk, vv = kv.export_rows(0, 0, shape.n_layers, 0, s + a + 1)
+        for l in range(shape.n_layers):
+            np.testing.assert_allclose(kk[l].float().cpu().numpy(), cache.k[l][:s + a + 1], atol=TOL)
+            np.testing.assert_allclose(vv[l].float().cpu().numpy(), cache.v[l][:s + a + 1], atol=TOL)
+    assert model.device_error() == 0
+
+
+def test_tree_small():
+    _tree_case(2, 200, seed=31)
+
+
+def test_tree_full_size():
+    """8 layers, 2048-token prefilled context, 29-row tree."""
+    _tree_case(8, 2048, seed=3)
+
+
+def test_layer_skip_rounds_7b_layer_shape():
+    from speculative_decoding_verify_04_gb300 import spec
+    lib()
+    base = SHAPES["llama7b"]
+    import dataclasses
+    shape0 = dataclasses.replace(base, exit_layer=2)
+    model, dec, shape = model_pair(shape0, seed=4, n_layers=4, max_rows=64, max_batch=2, max_position=512)
+    k = 4
+    lens = [37, 150]
+    prompts = [make_tokens(n, shape.vocab, seed=40 + b) for b, n in enumerate(lens)]
+    ctx = 256
+    kv = spec.KVCache(model, 2, ctx)
+    nxt = torch.empty(2, dtype=torch.int32, device="cuda")
+    caches = []
+    t0 = []
+    for b in range(2):
+        spec.spec_prefill(model, kv, b, cuda_i32(prompts[b]), None, nxt[b:b + 1])
+        c = dec.new_cache(ctx)
+        t0.append(argmax_lowest(dec.prefill(c, prompts[b])))
+        caches.append(c)
+    torch.cuda.synchronize()
+    assert kv.get_lengths() == lens
+    t0g = nxt.clone()
+    if list(t0g.cpu().numpy()) != t0:
+        t0g = cuda_i32(t0)        # a near-tie at the first token: continue from the oracle's
+    cand = torch.empty((2, k + 1), dtype=torch.int32, device="cuda")
+    hL = torch.empty((2, k + 1, shape.d_model), dtype=torch.float32, device="cuda")
+    dlog = torch.empty((2, k, shape.vocab), dtype=torch.float32, device="cuda")
+    logits = torch.empty((2 * (k + 1), shape.vocab), dtype=torch.float32, device="cuda")
+    acc = torch.empty(2, dtype=torch.int32, device="cuda")
+    for rnd in range(3):
+        spec.spec_draft(model, kv, t0g, k, cand, hL, dlog)
+        spec.spec_verify(model, kv, [k + 1] * 2, cand, k + 1, h_in=hL, h_stride=k + 1, logits=logits,
+                         acc_len=acc, next_tok=nxt)
+        spec.kv_commit(kv, acc)
+        torch.cuda.synchronize()
+        cg = cand.cpu().numpy()
+        for b in range(2):
+            c = caches[b]
+            s = c.length
+            d_ref, hL_ref, dlog_ref, _ = OS.draft(dec, c, s, int(t0g[b].item()), k)
+            n_ok = assert_tokens_match(list(cg[b, 1:]), d_ref, [top_gap(r) for r in dlog_ref], what="draft")
+            if n_ok < k:
+                return
+            np.testing.assert_allclose(dlog.cpu().numpy()[b], dlog_ref, atol=TOL)
+            np.testing.assert_allclose(hL.cpu().numpy()[b], hL_ref, atol=TOL)
+            vlog_ref = OS.verify(dec, c, s, hL_ref, shape.exit_layer)
+            np.testing.assert_allclose(logits.cpu().numpy()[b * (k + 1):(b + 1) * (k + 1)], vlog_ref, atol=TOL)
+            a_ref, n_ref = A.accept_greedy_chain(d_ref, vlog_ref)
+            if (acc[b].item(), nxt[b].item()) != (a_ref, n_ref):
+                assert min(top_gap(r) for r in vlog_ref[:a_ref + 1]) < 1e-2
+                return
+            c.length = A.commit_chain(s, a_ref)
+        assert kv.get_lengths() == [c.length for c in caches]
+        t0g = nxt.clone()
+    for b in range(2):
+        n = caches[b].length
+        kk, vv = kv.export_rows(b, 0, shape.n_layers, 0, n)
+        for l in range(shape.n_layers):
+            np.testing.assert_allclose(kk[l].float().cpu().numpy(), caches[b].k[l][:n], atol=TOL)
+    assert model.device_error() == 0

@@ -1,0 +1,112 @@
+"""Tiny f32 decoder end to end: prefill, layer-skip greedy rounds, commit.
+
+2 layers, d 256, 4 heads x 64, FFN 1024, vocab 1024, draft = layer 0, k = 4,
+prompt of 32 uniform tokens, 64 generated tokens (the pages' lossless check:
+speculative greedy output equals plain greedy output).
+"""
+import numpy as np
+import pytest
+import torch
+
+from _gpu_util import assert_tokens_match, cuda_i32, lib, model_pair, top_gap
+from oracle import spec as OS
+from oracle.accept import argmax_lowest
+from synthetic import SHAPES, make_tokens
+
+pytestmark = pytest.mark.gpu
+
+K, PROMPT, NEW = 4, 32, 64
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    lib()
+    return model_pair(SHAPES["tiny"], seed=1, max_rows=64, max_batch=4, max_position=256)
+
+
+def test_prefill_logits(tiny):
+    from speculative_decoding_verify_04_gb300 import spec
+    model, dec, shape = tiny
+    prompt = make_tokens(PROMPT, shape.vocab, seed=1)
+    kv = spec.KVCache(model, 1, 128)
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+    nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+    spec.spec_prefill(model, kv, 0, cuda_i32(prompt), logits, nxt)
+    torch.cuda.synchronize()
+    cache = dec.new_cache(128)
+    ref = dec.prefill(cache, prompt)
+    np.testing.assert_allclose(logits.cpu().numpy(), ref, atol=2e-3, rtol=0)
+    assert nxt.item() == argmax_lowest(ref) or top_gap(ref) < 1e-2
+    assert kv.get_lengths() == [PROMPT]
+    k_gpu, v_gpu = kv.export_rows(0, 0, shape.n_layers, 0, PROMPT)
+    for l in range(shape.n_layers):
+        np.testing.assert_allclose(k_gpu[l].cpu().numpy(), cache.k[l][:PROMPT], atol=2e-3)
+        np.testing.assert_allclose(v_gpu[l].cpu().numpy(), cache.v[l][:PROMPT], atol=2e-3)
+    assert model.device_error() == 0
+
+
+def test_greedy_generation_matches_oracle(tiny):
+    """Round by round in lockstep with the oracle: draft tokens, target logits,
+    acceptance, next token, lengths and finally the committed KV rows."""
+    from speculative_decoding_verify_04_gb300 import spec
+    model, dec, shape = tiny
+    prompt = make_tokens(PROMPT, shape.vocab, seed=1)
+    ctx = PROMPT + NEW + K + 8
+    kv = spec.KVCache(model, 1, ctx)
+    nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+    spec.spec_prefill(model, kv, 0, cuda_i32(prompt), None, nxt)
+    cache = dec.new_cache(ctx)
+    ref_logits = dec.prefill(cache, prompt)
+    t0_ref = argmax_lowest(ref_logits)
+    assert nxt.item() == t0_ref
+    ar = OS.generate_greedy_ar(dec, prompt, NEW)
+
+    cand = torch.empty((1, K + 1), dtype=torch.int32, device="cuda")
+    hL = torch.empty((1, K + 1, shape.d_model), dtype=torch.float32, device="cuda")
+    dlog = torch.empty((1, K, shape.vocab), dtype=torch.float32, device="cuda")
+    logits = torch.empty((K + 1, shape.vocab), dtype=torch.float32, device="cuda")
+    stats = torch.empty((K + 1, 4), dtype=torch.float32, device="cuda")
+    acc = torch.empty(1, dtype=torch.int32, device="cuda")
+    out_gpu, out_ref = [t0_ref], [t0_ref]
+    t0 = nxt.clone()
+    rounds = 0
+    while len(out_ref) < NEW:
+        s = cache.length
+        # oracle round
+        d_ref, hL_ref, dlog_ref, _ = OS.draft(dec, cache, s, int(t0.item()), K)
+        vlog_ref = OS.verify(dec, cache, s, hL_ref, shape.exit_layer)
+        from oracle.accept import accept_greedy_chain, commit_chain
+        a_ref, n_ref = accept_greedy_chain(d_ref, vlog_ref)
+        cache.length = commit_chain(s, a_ref)
+        # library round
+        spec.spec_draft(model, kv, t0, K, cand, hL, dlog)
+        spec.spec_verify(model, kv, [K + 1], cand, K + 1, h_in=hL, h_stride=K + 1, logits=logits, stats=stats,
+                         acc_len=acc, next_tok=nxt)
+        spec.kv_commit(kv, acc)
+        torch.cuda.synchronize()
+        c = cand.cpu().numpy()[0]
+        gaps = [top_gap(r) for r in dlog_ref]
+        n_ok = assert_tokens_match(list(c[1:]), d_ref, gaps, what="draft")
+        if n_ok < K:
+            return        # a near-tie in the draft: trajectories may part from here
+        np.testing.assert_allclose(dlog.cpu().numpy()[0], dlog_ref, atol=2e-3)
+        np.testing.assert_allclose(hL.cpu().numpy()[0], hL_ref, atol=2e-3)
+        np.testing.assert_allclose(logits.cpu().numpy(), vlog_ref, atol=2e-3)
+        a_gpu, n_gpu = acc.item(), nxt.item()
+        if (a_gpu, n_gpu) != (a_ref, n_ref):
+            assert min(top_gap(r) for r in vlog_ref[:a_ref + 1]) < 1e-2
+            return
+        assert kv.get_lengths() == [cache.length]
+        out_gpu += list(c[1:a_gpu + 1]) + [n_gpu]
+        out_ref += list(d_ref[:a_ref]) + [n_ref]
+        t0 = nxt.clone()
+        rounds += 1
+    assert out_ref[:NEW] == ar
+    assert out_gpu[:NEW] == ar
+    n = cache.length
+    k_gpu, v_gpu = kv.export_rows(0, 0, shape.n_layers, 0, n)
+    for l in range(shape.n_layers):
+        np.testing.assert_allclose(k_gpu[l].cpu().numpy(), cache.k[l][:n], atol=2e-3)
+        np.testing.assert_allclose(v_gpu[l].cpu().numpy(), cache.v[l][:n], atol=2e-3)
+    assert model.device_error() == 0
+    assert rounds > 0
