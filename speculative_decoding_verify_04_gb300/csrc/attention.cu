@@ -208,7 +208,7 @@ attention_kernel(AttnParams a, int n_rb) {
         }
         const int qg = q0 + qi;
         const int j = qg / G, h = g * G + qg % G;
-        static_cast<KT*>(a.out)[(size_t)(row0 + j) * qdim + h * HD + d] = from_f32<KT>(O / L);
+        store_act(static_cast<KT*>(a.out), (size_t)(row0 + j) * qdim + h * HD + d, a.out_lo, O / L);
     }
     if (t == 0) a.counters[blk] = 0;
 }

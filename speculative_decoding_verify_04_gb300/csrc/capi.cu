@@ -88,14 +88,17 @@ struct PlanArgs {
 
 // Row plan.  mode 0 chain: row j of sequence b at slot / position s_b + j.
 // mode 1 tree: slot s_b + j, position s_b + depth(j).  mode 2 draft pass j:
-// one row per sequence at slot / position s_b + j.
+// one row per sequence at slot / position s_b + j, seeing slots [0, s_b + j]
+// (the earlier passes' rows count as context: base s_b + j, local row 0).
 __global__ void plan_kernel(PlanArgs a, RowPlan plan, const int* __restrict__ len, int T) {
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     const PlanParams& p = a.p;
+    // a draft pass sees the rows of the earlier passes as context: its base is s + j
+    const int extra = (p.mode == 2) ? p.pass : 0;
     if (t < p.batch) {
         plan.seq_row0[t] = (p.mode == 2) ? t : a.row0[t];
         plan.seq_nrows[t] = (p.mode == 2) ? 1 : p.n_rows[t];
-        plan.seq_base[t] = len[t];
+        plan.seq_base[t] = len[t] + extra;
     }
     if (t < kMaxSeqRows) {
         plan.tree_parent[t] = p.parent[t];
@@ -105,7 +108,7 @@ __global__ void plan_kernel(PlanArgs a, RowPlan plan, const int* __restrict__ le
     int b, j;
     if (p.mode == 2) {
         b = t;
-        j = p.pass;
+        j = 0;
     } else {
         int lo = 0, hi = p.batch - 1;      // last sequence with row0 <= t
         while (lo < hi) {
@@ -115,7 +118,7 @@ __global__ void plan_kernel(PlanArgs a, RowPlan plan, const int* __restrict__ le
         b = lo;
         j = t - a.row0[b];
     }
-    const int s = len[b];
+    const int s = len[b] + extra;
     plan.row_seq[t] = b;
     plan.row_local[t] = j;
     plan.row_slot[t] = s + j;
@@ -128,7 +131,7 @@ template <typename WT>
 __global__ void __launch_bounds__(128)
 prologue_kernel(const float* __restrict__ h_in, int h_stride, const int* __restrict__ tok, int tok_stride,
                 int tok_col, const WT* __restrict__ embed, RowPlan plan, int d, int vocab,
-                const float* __restrict__ gain, float* h, WT* x, float* ss, int ss_stride, int* err) {
+                const float* __restrict__ gain, float* h, WT* x, size_t x_lo, float* ss, int ss_stride, int* err) {
     __shared__ float red[4];
     const int r = blockIdx.x, t = threadIdx.x;
     const int b = plan.row_seq[r], j = plan.row_local[r];
@@ -151,7 +154,7 @@ prologue_kernel(const float* __restrict__ h_in, int h_stride, const int* __restr
         if (n < d) {
             v = src_h ? src_h[n] : to_f32<WT>(src_e[n]);
             h[(size_t)r * d + n] = v;
-            x[(size_t)r * d + n] = from_f32<WT>(v * gain[n]);
+            store_act(x, (size_t)r * d + n, x_lo, v * gain[n]);
         }
         float s = warp_sum(v * v);
         if ((t & 31) == 0) red[t >> 5] = s;
@@ -237,6 +240,8 @@ static EpiParams base_epi(spec_model* m, spec_kv* kv, int T) {
     e.d_model = c.d_model;
     e.ss_out = m->ss_part;
     e.act = m->x_act;
+    e.act_lo = (size_t)m->max_rows_pad * c.d_ff;
+    e.x_next_lo = (size_t)m->max_rows_pad * c.d_model;
     e.d_ff = c.d_ff;
     e.vocab = c.vocab;
     e.stat_part = m->stat_part;
@@ -266,6 +271,7 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             a.kc = kv->k;
             a.vc = kv->v;
             a.out = m->x_attn;
+            a.out_lo = (size_t)m->max_rows_pad * qdim;
             a.plan = m->plan;
             a.batch = batch;
             a.kv_batch = kv->batch;
@@ -353,11 +359,12 @@ static int launch_prologue(spec_model* m, int T, const float* h_in, int h_stride
     if (m->bf16)
         prologue_kernel<__nv_bfloat16><<<T, 128, 0, st>>>(h_in, h_stride, tok, tok_stride, tok_col,
                                                          (const __nv_bfloat16*)m->embed, m->plan, c.d_model, c.vocab,
-                                                         gain, m->h, (__nv_bfloat16*)m->x_in, m->ss_part, c.max_rows,
+                                                         gain, m->h, (__nv_bfloat16*)m->x_in,
+                                                         (size_t)m->max_rows_pad * c.d_model, m->ss_part, c.max_rows,
                                                          m->err);
     else
         prologue_kernel<float><<<T, 128, 0, st>>>(h_in, h_stride, tok, tok_stride, tok_col, (const float*)m->embed,
-                                                 m->plan, c.d_model, c.vocab, gain, m->h, (float*)m->x_in,
+                                                 m->plan, c.d_model, c.vocab, gain, m->h, (float*)m->x_in, 0,
                                                  m->ss_part, c.max_rows, m->err);
     ++m->launches;
     return check_cuda(cudaGetLastError(), "prologue launch");
@@ -516,7 +523,8 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
     m->n_attn_counters = c.max_batch * c.n_kv_heads * ((rows_per_seq * G + 15) / 16);
     off = 0;
     const size_t w_h = take((size_t)R * d * 4);
-    const size_t w_xin = take((size_t)Rp * d * E), w_xat = take((size_t)Rp * qdim * E), w_xac = take((size_t)Rp * F * E);
+    const int xr = m->bf16 ? 2 * Rp : Rp;    // bf16: hi rows then lo rows
+    const size_t w_xin = take((size_t)xr * d * E), w_xat = take((size_t)xr * qdim * E), w_xac = take((size_t)xr * F * E);
     const size_t w_q = take((size_t)R * qdim * 4);
     const size_t w_ss = take((size_t)((d + 127) / 128) * R * 4);
     const size_t w_sp = take((size_t)((V + 127) / 128) * R * sizeof(spec_row_stats));
@@ -570,7 +578,7 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
         const int xk[3] = {d, qdim, F};
         for (int i = 0; i < 3; ++i)
             for (int tp = 16; tp <= t_pad_max; tp += 16)
-                ok &= make_tmap_2d(&m->tm_x[i][tp / 16 - 1], xb[i], xk[i], Rp, (uint64_t)xk[i] * 2, kTileK, tp);
+                ok &= make_tmap_2d(&m->tm_x[i][tp / 16 - 1], xb[i], xk[i], 2 * Rp, (uint64_t)xk[i] * 2, kTileK, tp);
         if (!ok) return fail(set_error(SPEC_ERR_CUDA, "cuTensorMapEncodeTiled failed"));
     }
     if ((rc = check_cuda(cudaStreamSynchronize(st), "spec_model_create sync"))) return fail(rc);
@@ -730,7 +738,7 @@ extern "C" int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32
         p.mode = 2;
         p.pass = j;
         SPEC_TRY(launch_plan(m, p, batch, kv->len, st));
-        SPEC_TRY(launch_prologue(m, batch, nullptr, 0, cand, k + 1, 0, 0, st));
+        SPEC_TRY(launch_prologue(m, batch, nullptr, 0, cand, k + 1, j, 0, st));
         SPEC_TRY(run_layers(m, kv, batch, batch, 1, 0, c.exit_layer, 0, j < k, st));
         copy_rows_kernel<<<batch, 256, 0, st>>>(m->h, h_L, batch, c.d_model, k + 1, j);
         ++m->launches;

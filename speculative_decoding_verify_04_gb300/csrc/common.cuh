@@ -29,6 +29,17 @@ template <typename T> SPEC_DEV T from_f32(float x);
 template <> SPEC_DEV float from_f32<float>(float x) { return x; }
 template <> SPEC_DEV __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+// Store a GEMM input value.  f32 models store it as is.  bf16 models store a
+// pair: hi = bf16(v) at base[o] and lo = bf16(v - hi) at base[o + lo_off]; the
+// tensor-core GEMM multiplies both by the same weights into one f32
+// accumulator, so the activation keeps ~16 significant bits instead of 8.
+SPEC_DEV void store_act(float* base, size_t o, size_t, float v) { base[o] = v; }
+SPEC_DEV void store_act(__nv_bfloat16* base, size_t o, size_t lo_off, float v) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    base[o] = hi;
+    base[o + lo_off] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
 // ---------------------------------------------------------------------------
 // shared-memory address of a generic pointer
 SPEC_DEV uint32_t smem_u32(const void* p) {

@@ -10,7 +10,10 @@
 // activation rows are its N side (padded to a multiple of 16), so one
 // tcgen05.mma.kind::f16 of M=128, N=T_pad, K=16 consumes 32 B of every W row.
 // W and X tiles arrive by TMA (128-byte swizzle) into a ring of stages; one
-// thread issues the MMAs, accumulators live in tensor memory.  The work is
+// thread issues the MMAs, accumulators live in tensor memory.  Activations are
+// kept as bf16 hi/lo pairs (x = hi + lo to ~16 bits): each k-step issues one MMA
+// with the hi rows and one with the lo rows into the same f32 accumulator, so
+// weights stream once and the product keeps near-f32 activation precision.  The work is
 // split stream-K: the (tile, k-block) units are cut into one contiguous range
 // per CTA (one CTA per SM), so every SM streams the same number of bytes.  A
 // tile cut between CTAs is reduced deterministically (fixed order of the
@@ -153,7 +156,7 @@ SPEC_DEV void apply_resid(const EpiParams& e, int tile, int j0, int nr, EpiSmem&
             const size_t o = (size_t)r * e.d_model + n;
             const float hn = e.h[o] + sm.tile[j][mm];
             e.h[o] = hn;
-            static_cast<XT*>(e.x_next)[o] = from_f32<XT>(hn * e.gain_next[n]);
+            store_act(static_cast<XT*>(e.x_next), o, e.x_next_lo, hn * e.gain_next[n]);
             sq = hn * hn;
         }
         sm.tile[j][mm] = sq;
@@ -176,7 +179,7 @@ SPEC_DEV void apply_swiglu(const EpiParams& e, int tile, int j0, int nr, EpiSmem
         const int r = e.r0 + j0 + j;
         const float g = sm.tile[j][mm] * sm.rs[j];
         const float u = sm.tile[j][mm + 64] * sm.rs[j];
-        static_cast<XT*>(e.act)[(size_t)r * e.d_ff + f] = from_f32<XT>(g / (1.0f + expf(-g)) * u);
+        store_act(static_cast<XT*>(e.act), (size_t)r * e.d_ff + f, e.act_lo, g / (1.0f + expf(-g)) * u);
     }
 }
 
@@ -336,8 +339,9 @@ constexpr uint32_t kATileBytes = kTileN * kTileK * 2;
 
 struct TcLayout {
     int stages;
-    uint32_t b_bytes;
+    uint32_t b_bytes;     // hi + lo activation tiles of one stage
     uint32_t tmem_cols;
+    int rows_pad;         // first row of the lo half in the X buffers
 };
 
 __host__ __device__ inline size_t tc_smem_bytes(const TcLayout& L) {
@@ -405,7 +409,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, e.err)) break;
                 mbar_arrive_expect_tx(full + stage, kATileBytes + L.b_bytes);
                 tma_load_2d(sA + (size_t)stage * kATileBytes, &tmW, kb * kTileK, tile * kTileN, full + stage, pw);
+                // hi rows, then lo rows (the lo half of the buffer starts at row rows_pad)
                 tma_load_2d(sB + (size_t)stage * L.b_bytes, &tmX, kb * kTileK, e.r0, full + stage, px);
+                tma_load_2d(sB + (size_t)stage * L.b_bytes + L.b_bytes / 2, &tmX, kb * kTileK, L.rows_pad + e.r0,
+                            full + stage, px);
                 ++issued;
                 if (++stage == L.stages) { stage = 0; phase ^= 1u; }
             }
@@ -435,10 +442,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                     if (!mbar_wait(full + stage, phase, abort_flag, e.err)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ad = smem_desc_sw128(smem_u32(sA + (size_t)stage * kATileBytes));
-                    const uint64_t bd = smem_desc_sw128(smem_u32(sB + (size_t)stage * L.b_bytes));
+                    const uint64_t bh = smem_desc_sw128(smem_u32(sB + (size_t)stage * L.b_bytes));
+                    const uint64_t bl = smem_desc_sw128(smem_u32(sB + (size_t)stage * L.b_bytes + L.b_bytes / 2));
 #pragma unroll
-                    for (int k = 0; k < kTileK / 16; ++k)
-                        tc_mma_f16(tmem, ad + 2u * k, bd + 2u * k, idesc, (u > seg_begin || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < kTileK / 16; ++k) {
+                        tc_mma_f16(tmem, ad + 2u * k, bh + 2u * k, idesc, (u > seg_begin || k > 0) ? 1u : 0u);
+                        tc_mma_f16(tmem, ad + 2u * k, bl + 2u * k, idesc, 1u);
+                    }
                     tc_commit(empty + stage);
                     if (++stage == L.stages) { stage = 0; phase ^= 1u; }
                 }
@@ -574,9 +584,10 @@ size_t gemm_partial_floats_needed(const spec_model* m, int N, int K, int T_pad) 
 
 int gemm_grid(const spec_model* m, int N, int K) { return make_split(m, N, K, 16).G; }
 
-static TcLayout tc_layout(int T_pad) {
+static TcLayout tc_layout(int T_pad, int rows_pad) {
     TcLayout L;
-    L.b_bytes = (uint32_t)T_pad * kTileK * 2;
+    L.rows_pad = rows_pad;
+    L.b_bytes = 2u * (uint32_t)T_pad * kTileK * 2;
     const size_t budget = 225 * 1024 - 1024 - 256 - sizeof(EpiSmem) - 64;
     L.stages = (int)std::min<size_t>(8, budget / (kATileBytes + L.b_bytes));
     uint32_t cols = 32;
@@ -603,7 +614,7 @@ int launch_gemm(spec_model* m, const GemmLaunch& g, EpiParams e, int xbuf, cudaS
             return set_error(SPEC_ERR_CAPACITY, "GEMM workspace too small for this launch");
         const int slot = prof_start(m, st);
         if (m->bf16) {
-            TcLayout L = tc_layout(T_pad);
+            TcLayout L = tc_layout(T_pad, m->max_rows_pad);
             const size_t smem = tc_smem_bytes(L);
             static bool attr_set = false;
             if (!attr_set) {

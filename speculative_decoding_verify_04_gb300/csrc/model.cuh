@@ -82,7 +82,8 @@ struct spec_model {
     char* ws = nullptr;              // workspace (one allocation)
     size_t ws_bytes = 0;
     float* h = nullptr;              // [max_rows][d] f32 residual stream
-    void* x_in = nullptr;            // [max_rows_pad][d]   GEMM input: gained residual (model dtype)
+    // GEMM inputs, model dtype; bf16 models keep [2][max_rows_pad][K]: hi rows then lo rows
+    void* x_in = nullptr;            // [max_rows_pad][d]   gained residual
     void* x_attn = nullptr;          // [max_rows_pad][H hd] attention output
     void* x_act = nullptr;           // [max_rows_pad][F]   SwiGLU output
     float* q = nullptr;              // [max_rows][H hd] rotated, pre-scaled queries
@@ -164,10 +165,12 @@ struct EpiParams {
     float* h;
     const float* gain_next;
     void* x_next;
+    size_t x_next_lo;       // element offset of the lo half (bf16 models)
     float* ss_out;
     int d_model;
     // SwiGLU
     void* act;
+    size_t act_lo;
     int d_ff;
     // LM head
     float* logits;          // nullable; row r goes to logits[(r - logits_row0) * logits_stride]
@@ -187,7 +190,7 @@ struct EpiParams {
 
 struct GemmLaunch {
     const CUtensorMap* tmW;
-    const CUtensorMap* tmX;
+    const CUtensorMap* tmX;     // unused: X maps come from the model by buffer index
     const void* W;          // f32 path
     const void* X;          // f32 path
     int x_stride;           // f32 path: elements per X row
@@ -204,6 +207,7 @@ struct AttnParams {
     const float* q;         // [rows][H hd]
     const void* kc; const void* vc;
     void* out;              // [rows][H hd] model dtype (O-projection input)
+    size_t out_lo;          // element offset of the lo half (bf16 models)
     RowPlan plan;
     int batch, kv_batch, kv_ctx, layer;
     int n_heads, n_kv_heads, head_dim;

@@ -103,64 +103,74 @@ def test_tree_full_size():
     _tree_case(8, 2048, seed=3)
 
 
-def test_layer_skip_rounds_7b_layer_shape():
+def _layer_skip_rounds(n_layers, exit_layer, lens, k, rounds, seed):
+    """Greedy layer-skip rounds on the 7B layer shape from a synthetic committed
+    context (seeded KV rows given identically to both sides), lockstep with the oracle."""
     from speculative_decoding_verify_04_gb300 import spec
-    lib()
-    base = SHAPES["llama7b"]
+    from synthetic import make_kv_context
     import dataclasses
-    shape0 = dataclasses.replace(base, exit_layer=2)
-    model, dec, shape = model_pair(shape0, seed=4, n_layers=4, max_rows=64, max_batch=2, max_position=512)
-    k = 4
-    lens = [37, 150]
-    prompts = [make_tokens(n, shape.vocab, seed=40 + b) for b, n in enumerate(lens)]
-    ctx = 256
-    kv = spec.KVCache(model, 2, ctx)
-    nxt = torch.empty(2, dtype=torch.int32, device="cuda")
+    lib()
+    shape0 = dataclasses.replace(SHAPES["llama7b"], exit_layer=exit_layer)
+    B = len(lens)
+    model, dec, shape = model_pair(shape0, seed=seed, n_layers=n_layers, max_rows=64, max_batch=B,
+                                   max_position=max(lens) + rounds * (k + 1) + 16)
+    ctx = max(lens) + rounds * (k + 1) + 8
+    kv = spec.KVCache(model, B, ctx)
     caches = []
-    t0 = []
-    for b in range(2):
-        spec.spec_prefill(model, kv, b, cuda_i32(prompts[b]), None, nxt[b:b + 1])
+    for b in range(B):
+        kc, vc = make_kv_context(shape, 1, lens[b], seed * 100 + b, device="cuda")
+        kv.import_rows(b, 0, kc[:, 0].contiguous(), vc[:, 0].contiguous())
         c = dec.new_cache(ctx)
-        t0.append(argmax_lowest(dec.prefill(c, prompts[b])))
+        c.load(kc[:, 0].float().cpu().numpy(), vc[:, 0].float().cpu().numpy())
         caches.append(c)
-    torch.cuda.synchronize()
-    assert kv.get_lengths() == lens
-    t0g = nxt.clone()
-    if list(t0g.cpu().numpy()) != t0:
-        t0g = cuda_i32(t0)        # a near-tie at the first token: continue from the oracle's
-    cand = torch.empty((2, k + 1), dtype=torch.int32, device="cuda")
-    hL = torch.empty((2, k + 1, shape.d_model), dtype=torch.float32, device="cuda")
-    dlog = torch.empty((2, k, shape.vocab), dtype=torch.float32, device="cuda")
-    logits = torch.empty((2 * (k + 1), shape.vocab), dtype=torch.float32, device="cuda")
-    acc = torch.empty(2, dtype=torch.int32, device="cuda")
-    for rnd in range(3):
+        del kc, vc
+    kv.set_lengths(lens)
+    t0 = make_tokens(B, shape.vocab, seed=seed, name="t0")
+    t0g = cuda_i32(t0)
+    cand = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
+    hL = torch.empty((B, k + 1, shape.d_model), dtype=torch.float32, device="cuda")
+    dlog = torch.empty((B, k, shape.vocab), dtype=torch.float32, device="cuda")
+    logits = torch.empty((B * (k + 1), shape.vocab), dtype=torch.float32, device="cuda")
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    worst = 0.0
+    for rnd in range(rounds):
         spec.spec_draft(model, kv, t0g, k, cand, hL, dlog)
-        spec.spec_verify(model, kv, [k + 1] * 2, cand, k + 1, h_in=hL, h_stride=k + 1, logits=logits,
+        spec.spec_verify(model, kv, [k + 1] * B, cand, k + 1, h_in=hL, h_stride=k + 1, logits=logits,
                          acc_len=acc, next_tok=nxt)
         spec.kv_commit(kv, acc)
         torch.cuda.synchronize()
         cg = cand.cpu().numpy()
-        for b in range(2):
+        for b in range(B):
             c = caches[b]
             s = c.length
             d_ref, hL_ref, dlog_ref, _ = OS.draft(dec, c, s, int(t0g[b].item()), k)
             n_ok = assert_tokens_match(list(cg[b, 1:]), d_ref, [top_gap(r) for r in dlog_ref], what="draft")
             if n_ok < k:
-                return
-            np.testing.assert_allclose(dlog.cpu().numpy()[b], dlog_ref, atol=TOL)
-            np.testing.assert_allclose(hL.cpu().numpy()[b], hL_ref, atol=TOL)
+                return worst
+            e1 = np.abs(dlog.cpu().numpy()[b] - dlog_ref).max()
             vlog_ref = OS.verify(dec, c, s, hL_ref, shape.exit_layer)
-            np.testing.assert_allclose(logits.cpu().numpy()[b * (k + 1):(b + 1) * (k + 1)], vlog_ref, atol=TOL)
+            e2 = np.abs(logits.cpu().numpy()[b * (k + 1):(b + 1) * (k + 1)] - vlog_ref).max()
+            worst = max(worst, e1, e2)
+            assert e1 < TOL and e2 < TOL, (e1, e2)
             a_ref, n_ref = A.accept_greedy_chain(d_ref, vlog_ref)
             if (acc[b].item(), nxt[b].item()) != (a_ref, n_ref):
                 assert min(top_gap(r) for r in vlog_ref[:a_ref + 1]) < 1e-2
-                return
+                return worst
             c.length = A.commit_chain(s, a_ref)
         assert kv.get_lengths() == [c.length for c in caches]
         t0g = nxt.clone()
-    for b in range(2):
+    for b in range(B):
         n = caches[b].length
         kk, vv = kv.export_rows(b, 0, shape.n_layers, 0, n)
         for l in range(shape.n_layers):
-            np.testing.assert_allclose(kk[l].float().cpu().numpy(), caches[b].k[l][:n], atol=TOL)
+            np.testing.assert_allclose(kk[l].float().cpu().numpy(), caches[b].k[l][:n], atol=TOL, rtol=1e-2)
+            np.testing.assert_allclose(vv[l].float().cpu().numpy(), caches[b].v[l][:n], atol=TOL, rtol=1e-2)
     assert model.device_error() == 0
+    return worst
+
+
+def test_layer_skip_rounds_7b_layer_shape():
+    """4 layers of the 7B shape, draft = 2 layers, batch 2 with contexts 150 and 301."""
+    worst = _layer_skip_rounds(4, 2, [150, 301], k=4, rounds=3, seed=4)
+    print(f"max logit error {worst:.3g}")
