@@ -264,6 +264,28 @@ int spec_schedule_k(const double* top_probs, const int32_t* n_rows, const int32_
                     double* ema, int32_t batch, const spec_k_schedule* sch, int32_t* k_next,
                     double* conf, void* stream);
 
+/* spec_verify without any device memory of its own per call: same arguments,
+ * results and stream semantics as spec_verify.  This entry point has no
+ * counterpart in the method the pages describe; it exists for callers that
+ * cannot call cudaMalloc where they verify (for example while another
+ * component is capturing the stream into a CUDA graph, or when all device
+ * memory is already handed to the caller's own pool).  The call's scratch --
+ * the GEMM split-K partial tiles and arrival counters and the attention split
+ * partials and counters -- comes from a 32 MiB static __device__ array that
+ * every GPU loading the library keeps until the process exits.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress) and
+ * caches it; make that first call before any stream capture.  The array is
+ * shared by every call and keeps the last call's contents, so each call clears
+ * the counters it needs on `stream`; calls that overlap on the GPU (other
+ * streams, other threads) race on the array and must not be issued.  Returns
+ * SPEC_ERR_CAPACITY with a message when a call needs more scratch than the
+ * array holds.  Makes no cudaMalloc / cudaFree or other allocating call.  async. */
+int spec_verify_noalloc(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows,
+                        const float* h_in, int32_t h_stride, const int32_t* tokens,
+                        int32_t tok_stride, const int32_t* tree_parent, float* logits,
+                        spec_row_stats* stats, int32_t* acc_len, int32_t* next_tok,
+                        int32_t* path, void* stream);
+
 /* Tracing.  spec_profile(m, 1) starts a fresh record: from then on every GEMM
  * and attention launch of this model is bracketed by CUDA events on its
  * stream, with the launch's algorithmic bytes (weights once, activation rows

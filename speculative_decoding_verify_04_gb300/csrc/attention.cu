@@ -217,6 +217,20 @@ static int rows_blocks(int max_rows_per_seq, int G) {
     return (max_rows_per_seq * G + kQPerCta - 1) / kQPerCta;
 }
 
+// key-range splits per (sequence, kv head, query block): about two CTAs per SM
+int attn_splits(const spec_model* m, int blocks, int kv_ctx) {
+    int s = std::max(1, std::min(32, (2 * m->num_sms + blocks - 1) / blocks));
+    return std::min(s, std::max(1, (kv_ctx + kKeyTile - 1) / kKeyTile));
+}
+
+size_t attn_scratch_floats(const spec_model* m, int batch, int max_rows_per_seq, int kv_ctx, int* n_counters) {
+    const spec_model_config& c = m->cfg;
+    const int n_rb = rows_blocks(max_rows_per_seq, c.n_heads / c.n_kv_heads);
+    const int blocks = batch * c.n_kv_heads * n_rb;
+    *n_counters = blocks;
+    return (size_t)blocks * attn_splits(m, blocks, kv_ctx) * kQPerCta * (c.head_dim + 2);
+}
+
 size_t attn_partial_floats_needed(const spec_model* m, int batch, int max_rows_per_seq) {
     const spec_model_config& c = m->cfg;
     const int G = c.n_heads / c.n_kv_heads;
@@ -229,8 +243,7 @@ int launch_attention(spec_model* m, const AttnParams& a0, int max_rows_per_seq, 
     const int G = a.n_heads / a.n_kv_heads;
     const int n_rb = rows_blocks(max_rows_per_seq, G);
     const int blocks = a.batch * a.n_kv_heads * n_rb;
-    a.splits = std::max(1, std::min(32, (2 * m->num_sms + blocks - 1) / blocks));
-    a.splits = std::min(a.splits, std::max(1, (a.kv_ctx + kKeyTile - 1) / kKeyTile));
+    a.splits = attn_splits(m, blocks, a.kv_ctx);
     if ((size_t)blocks * a.splits * kQPerCta * (a.head_dim + 2) > m->attn_part_floats || blocks > m->n_attn_counters)
         return set_error(SPEC_ERR_CAPACITY, "attention workspace too small");
     a.part = m->attn_part;

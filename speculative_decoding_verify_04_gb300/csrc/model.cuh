@@ -218,6 +218,8 @@ struct AttnParams {
     int* err;
 };
 int launch_attention(spec_model* m, const AttnParams& a, int max_rows_per_seq, cudaStream_t st);
+int attn_splits(const spec_model* m, int blocks, int kv_ctx);
+size_t attn_scratch_floats(const spec_model* m, int batch, int max_rows_per_seq, int kv_ctx, int* n_counters);
 size_t attn_partial_floats_needed(const spec_model* m, int batch, int max_rows_per_seq);
 
 // accept.cu

@@ -26,6 +26,7 @@ EXPORTS = [
     "spec_kv_create", "spec_kv_destroy", "spec_kv_set_lengths", "spec_kv_get_lengths", "spec_kv_import",
     "spec_kv_export", "spec_prefill", "spec_draft", "spec_verify", "spec_accept", "spec_accept_greedy",
     "kv_commit", "spec_row_probs", "spec_schedule_k", "spec_profile", "spec_profile_read", "spec_launch_count",
+    "spec_verify_noalloc",
 ]
 
 
@@ -78,6 +79,7 @@ def load(path: str = LIB_PATH):
         "spec_profile": ([P, I], I),
         "spec_profile_read": ([P, I, POINTER(c_double), POINTER(c_double), POINTER(I)], I),
         "spec_launch_count": ([P, POINTER(ctypes.c_int64)], I),
+        "spec_verify_noalloc": ([P, P, I, POINTER(I), P, I, P, I, POINTER(I), P, P, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -241,7 +243,7 @@ def spec_draft(model, kv, t0, k, cand, h_L, draft_logits=None, stream=None):
 
 
 def spec_verify(model, kv, n_rows, tokens, tok_stride, h_in=None, h_stride=0, tree_parent=None, logits=None,
-                stats=None, acc_len=None, next_tok=None, path=None, stream=None):
+                stats=None, acc_len=None, next_tok=None, path=None, stream=None, _entry="spec_verify"):
     B = len(n_rows)
     T = sum(int(n) for n in n_rows)
     _need(tokens, torch.int32, "tokens", B * tok_stride)
@@ -252,9 +254,15 @@ def spec_verify(model, kv, n_rows, tokens, tok_stride, h_in=None, h_stride=0, tr
     _need(next_tok, torch.int32, "next_tok", B)
     _need(path, torch.int32, "path", B * MAX_SEQ_ROWS)
     tp = _i32_array(tree_parent) if tree_parent is not None else None
-    _check(load().spec_verify(model.handle, kv.handle, B, _i32_array(n_rows), _ptr(h_in), h_stride, _ptr(tokens),
-                              tok_stride, tp, _ptr(logits), _ptr(stats), _ptr(acc_len), _ptr(next_tok), _ptr(path),
-                              _stream(stream)))
+    _check(getattr(load(), _entry)(model.handle, kv.handle, B, _i32_array(n_rows), _ptr(h_in), h_stride,
+                                   _ptr(tokens), tok_stride, tp, _ptr(logits), _ptr(stats), _ptr(acc_len),
+                                   _ptr(next_tok), _ptr(path), _stream(stream)))
+
+
+def spec_verify_noalloc(model, kv, n_rows, tokens, tok_stride, **kw):
+    """spec_verify whose per-call scratch is the library's static device array
+    (for callers that cannot allocate device memory where they verify)."""
+    spec_verify(model, kv, n_rows, tokens, tok_stride, _entry="spec_verify_noalloc", **kw)
 
 
 def spec_accept(p, q, draft, u, acc_len, next_tok, stream=None):
