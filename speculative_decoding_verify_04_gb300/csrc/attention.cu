@@ -213,8 +213,219 @@ attention_kernel(AttnParams a, int n_rb) {
     if (t == 0) a.counters[blk] = 0;
 }
 
+// Register-resident decode attention for up to RB query vectors per (sequence,
+// kv head): the draft passes (one row) and chain verification (k+1 rows).
+// A group of LPK lanes holds one K/V row (16 bytes per lane, read once from
+// global memory with non-coherent 16-byte loads, U row groups in flight per
+// warp); scores are reduced across the group with shuffles and the online
+// softmax state (max, sum, weighted values) of each group lives in registers,
+// updated once per U keys.  Group states merge through shared memory in a
+// fixed order, then splits merge as in the tiled kernel.
+template <typename KT, int HD, int RB>
+__global__ void __launch_bounds__(kAttnThreads)
+attention_decode_kernel(AttnParams a) {
+    constexpr int EPL = 16 / (int)sizeof(KT);        // elements per lane
+    constexpr int LPK = HD / EPL;                    // lanes per key row
+    constexpr int KPW = 32 / LPK;                    // key rows per warp step
+    constexpr int U = (RB <= 2) ? 4 : 2;             // warp steps in flight
+    constexpr int NGRP = (kAttnThreads / 32) * KPW;  // lane groups per CTA
+    extern __shared__ float smf[];
+    float* sState = smf;                             // [NGRP][RB][HD + 2]
+    float* sQ = sState + NGRP * RB * (HD + 2);       // [RB][HD]
+    int* sFlag = reinterpret_cast<int*>(sQ + RB * HD);
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int grp = lane / LPK, lk = lane % LPK;
+    const int G = a.n_heads / a.n_kv_heads;
+    const int T_b = a.plan.seq_nrows[b];
+    const int nq = T_b * G;
+    if (nq == 0) return;
+    const int base = a.plan.seq_base[b];
+    const int n_keys = base + T_b;
+    int chunk = (n_keys + a.splits - 1) / a.splits;
+    chunk = ((chunk + 31) / 32) * 32;
+    const int n_split = (n_keys + chunk - 1) / chunk;
+    if (split >= n_split) return;
+    if (n_keys > a.kv_ctx) { if (t == 0) dev_error(a.err, SPEC_DEVERR_CAPACITY); return; }
+    const int k_begin = split * chunk, k_end = min(n_keys, k_begin + chunk);
+    // contiguous quarter of the chunk per warp
+    const int per_w = (k_end - k_begin + 3) / 4;
+    const int w_begin = k_begin + warp * per_w, w_end = min(k_end, w_begin + per_w);
+
+    const int row0 = a.plan.seq_row0[b];
+    const int qdim = a.n_heads * HD;
+    for (int i = t; i < RB * HD; i += kAttnThreads) {
+        const int r = i / HD, d = i % HD;
+        sQ[i] = (r < nq) ? a.q[(size_t)(row0 + r / G) * qdim + (g * G + r % G) * HD + d] : 0.f;
+    }
+    __syncthreads();
+    unsigned long long mk[RB];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+        mk[r] = 0ull;
+        if (r < nq) {
+            const int j = r / G;
+            if (a.tree) {
+                for (int x = j; x >= 0; x = a.plan.tree_parent[x]) mk[r] |= 1ull << x;
+            } else {
+                mk[r] = (j >= 63) ? ~0ull : ((2ull << j) - 1ull);
+            }
+        }
+    }
+    float m[RB], l[RB], acc[RB][EPL];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[r][e] = 0.f;
+    }
+
+    const size_t head_off = (((size_t)a.layer * a.kv_batch + b) * a.n_kv_heads + g) * a.kv_ctx;
+    const KT* Kg = static_cast<const KT*>(a.kc) + head_off * HD + lk * EPL;
+    const KT* Vg = static_cast<const KT*>(a.vc) + head_off * HD + lk * EPL;
+
+    for (int kb = w_begin; kb < w_end; kb += KPW * U) {
+        uint4 kr[U], vr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int key = kb + u * KPW + grp;
+            if (key < w_end) {
+                kr[u] = __ldg(reinterpret_cast<const uint4*>(Kg + (size_t)key * HD));
+                vr[u] = __ldg(reinterpret_cast<const uint4*>(Vg + (size_t)key * HD));
+            } else {
+                kr[u] = make_uint4(0, 0, 0, 0);
+                vr[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        float sc[U][RB];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const KT* kp = reinterpret_cast<const KT*>(&kr[u]);
+            float kf[EPL];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) kf[e] = to_f32<KT>(kp[e]);
+            const int key = kb + u * KPW + grp;
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                const float* qr = sQ + r * HD + lk * EPL;
+                float d = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) d = fmaf(qr[e], kf[e], d);
+#pragma unroll
+                for (int o = LPK / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                const bool vis = r < nq && key < w_end && (key < base || ((mk[r] >> (key - base)) & 1ull));
+                sc[u][r] = vis ? d : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            float mb = sc[0][r];
+#pragma unroll
+            for (int u = 1; u < U; ++u) mb = fmaxf(mb, sc[u][r]);
+            const float mn = fmaxf(m[r], mb);
+            if (mn == -INFINITY) continue;
+            const float scale = (m[r] == -INFINITY) ? 0.f : expf(m[r] - mn);
+            float p[U], ps = 0.f;
+#pragma unroll
+            for (int u = 0; u < U; ++u) { p[u] = expf(sc[u][r] - mn); ps += p[u]; }
+            l[r] = l[r] * scale + ps;
+            m[r] = mn;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                float x = acc[r][e] * scale;
+#pragma unroll
+                for (int u = 0; u < U; ++u) x = fmaf(p[u], to_f32<KT>(reinterpret_cast<const KT*>(&vr[u])[e]), x);
+                acc[r][e] = x;
+            }
+        }
+    }
+    // group states -> shared, merged in a fixed order
+    const int gi = warp * KPW + grp;
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+        float* st = sState + ((size_t)gi * RB + r) * (HD + 2);
+        if (lk == 0) { st[0] = m[r]; st[1] = l[r]; }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) st[2 + lk * EPL + e] = acc[r][e];
+    }
+    __syncthreads();
+    const int blk = b * a.n_kv_heads + g;
+    float* part = a.part + ((size_t)blk * a.splits + split) * kQPerCta * (HD + 2);
+    for (int i = t; i < nq * HD; i += kAttnThreads) {
+        const int r = i / HD, d = i % HD;
+        float M = -INFINITY;
+        for (int q2 = 0; q2 < NGRP; ++q2) M = fmaxf(M, sState[((size_t)q2 * RB + r) * (HD + 2)]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+            for (int q2 = 0; q2 < NGRP; ++q2) {
+                const float* st = sState + ((size_t)q2 * RB + r) * (HD + 2);
+                if (st[0] == -INFINITY) continue;
+                const float w = expf(st[0] - M);
+                L += st[1] * w;
+                O += st[2 + d] * w;
+            }
+        }
+        part[r * (HD + 2) + 2 + d] = O;
+        if (d == 0) { part[r * (HD + 2)] = M; part[r * (HD + 2) + 1] = L; }
+    }
+    __threadfence();
+    __syncthreads();
+    if (t == 0) sFlag[0] = (atomicAdd(a.counters + blk, 1) == n_split - 1);
+    __syncthreads();
+    if (!sFlag[0]) return;
+    __threadfence();
+    const float* pb = a.part + (size_t)blk * a.splits * kQPerCta * (HD + 2);
+    for (int i = t; i < nq * HD; i += kAttnThreads) {
+        const int r = i / HD, d = i % HD;
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < n_split; ++s2) M = fmaxf(M, __ldcg(pb + ((size_t)s2 * kQPerCta + r) * (HD + 2)));
+        float L = 0.f, O = 0.f;
+        for (int s2 = 0; s2 < n_split; ++s2) {
+            const float* ps2 = pb + ((size_t)s2 * kQPerCta + r) * (HD + 2);
+            const float ms = __ldcg(ps2);
+            if (ms == -INFINITY) continue;
+            const float w = expf(ms - M);
+            L += __ldcg(ps2 + 1) * w;
+            O += __ldcg(ps2 + 2 + d) * w;
+        }
+        const int j = r / G, h = g * G + r % G;
+        store_act(static_cast<KT*>(a.out), (size_t)(row0 + j) * qdim + h * HD + d, a.out_lo, O / L);
+    }
+    if (t == 0) a.counters[blk] = 0;
+}
+
+template <typename KT, int HD, int RB>
+static void launch_decode(const AttnParams& a, dim3 grid, cudaStream_t st) {
+    constexpr int EPL = 16 / (int)sizeof(KT);
+    constexpr int NGRP = (kAttnThreads / 32) * (32 / (HD / EPL));
+    const size_t smem = sizeof(float) * ((size_t)NGRP * RB * (HD + 2) + RB * HD) + 16;
+    static bool set = false;
+    if (!set) {
+        cudaFuncSetAttribute(attention_decode_kernel<KT, HD, RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        set = true;
+    }
+    attention_decode_kernel<KT, HD, RB><<<grid, kAttnThreads, smem, st>>>(a);
+}
+
+template <typename KT, int HD>
+static void launch_decode_rb(const AttnParams& a, int nq, dim3 grid, cudaStream_t st) {
+    if (nq <= 1) launch_decode<KT, HD, 1>(a, grid, st);
+    else if (nq <= 2) launch_decode<KT, HD, 2>(a, grid, st);
+    else if (nq <= 4) launch_decode<KT, HD, 4>(a, grid, st);
+    else launch_decode<KT, HD, 8>(a, grid, st);
+}
+
 static int rows_blocks(int max_rows_per_seq, int G) {
     return (max_rows_per_seq * G + kQPerCta - 1) / kQPerCta;
+}
+
+// key-range splits of the register-resident kernel: about four CTAs per SM
+int decode_splits(const spec_model* m, int blocks, int kv_ctx) {
+    int s = std::max(1, std::min(64, (4 * m->num_sms + blocks - 1) / blocks));
+    return std::min(s, std::max(1, (kv_ctx + 255) / 256));
 }
 
 // key-range splits per (sequence, kv head, query block): about two CTAs per SM
@@ -225,6 +436,11 @@ int attn_splits(const spec_model* m, int blocks, int kv_ctx) {
 
 size_t attn_scratch_floats(const spec_model* m, int batch, int max_rows_per_seq, int kv_ctx, int* n_counters) {
     const spec_model_config& c = m->cfg;
+    if (max_rows_per_seq * (c.n_heads / c.n_kv_heads) <= 8) {
+        const int blocks = batch * c.n_kv_heads;
+        *n_counters = blocks;
+        return (size_t)blocks * decode_splits(m, blocks, kv_ctx) * kQPerCta * (c.head_dim + 2);
+    }
     const int n_rb = rows_blocks(max_rows_per_seq, c.n_heads / c.n_kv_heads);
     const int blocks = batch * c.n_kv_heads * n_rb;
     *n_counters = blocks;
@@ -235,12 +451,38 @@ size_t attn_partial_floats_needed(const spec_model* m, int batch, int max_rows_p
     const spec_model_config& c = m->cfg;
     const int G = c.n_heads / c.n_kv_heads;
     const int n_rb = rows_blocks(max_rows_per_seq, G);
-    return (size_t)batch * c.n_kv_heads * n_rb * 32 * kQPerCta * (c.head_dim + 2);
+    return std::max((size_t)batch * c.n_kv_heads * n_rb * 32, (size_t)batch * c.n_kv_heads * 64) * kQPerCta *
+           (c.head_dim + 2);
 }
 
 int launch_attention(spec_model* m, const AttnParams& a0, int max_rows_per_seq, cudaStream_t st) {
     AttnParams a = a0;
     const int G = a.n_heads / a.n_kv_heads;
+    const int nq_max = max_rows_per_seq * G;
+    if (nq_max <= 8) {
+        // every query vector of a (sequence, kv head) in one register-resident block
+        const int blocks = a.batch * a.n_kv_heads;
+        a.splits = decode_splits(m, blocks, a.kv_ctx);
+        if ((size_t)blocks * a.splits * kQPerCta * (a.head_dim + 2) > m->attn_part_floats ||
+            blocks > m->n_attn_counters)
+            return set_error(SPEC_ERR_CAPACITY, "attention workspace too small");
+        a.part = m->attn_part;
+        a.counters = m->attn_counters;
+        dim3 grid(a.splits, a.n_kv_heads, a.batch);
+        const int slot = prof_start(m, st);
+        if (a.head_dim == 128) {
+            if (m->bf16) launch_decode_rb<__nv_bfloat16, 128>(a, nq_max, grid, st);
+            else launch_decode_rb<float, 128>(a, nq_max, grid, st);
+        } else {
+            if (m->bf16) launch_decode_rb<__nv_bfloat16, 64>(a, nq_max, grid, st);
+            else launch_decode_rb<float, 64>(a, nq_max, grid, st);
+        }
+        ++m->launches;
+        prof_stop(m, slot, st, PROF_ATTN, 0.0);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return check_cuda(e, "attention launch");
+        return SPEC_OK;
+    }
     const int n_rb = rows_blocks(max_rows_per_seq, G);
     const int blocks = a.batch * a.n_kv_heads * n_rb;
     a.splits = attn_splits(m, blocks, a.kv_ctx);
