@@ -31,6 +31,50 @@ struct AttnSmemLayout {
     }
 };
 
+// Merge the split partials of one (sequence, kv head, query block) in split
+// order and write the output rows.  Loads go out in parallel: the splits'
+// (max, sum) pairs into shared memory first, then the normalised split weights,
+// then the weighted values (independent loads, fixed summation order).
+template <typename KT, int HD>
+__device__ void merge_splits(const AttnParams& a, const float* pb, int n_split, int nq, int q0, int G, int g,
+                             int row0, float* sbuf) {
+    const int t = threadIdx.x;
+    float* sw = sbuf;                            // [n_split][kQPerCta] weights
+    float* sm = sbuf + 64 * kQPerCta;            // [n_split][kQPerCta] maxima
+    float* sl = sm + 64 * kQPerCta;              // [n_split][kQPerCta] sums
+    for (int i = t; i < n_split * nq; i += kAttnThreads) {
+        const int s2 = i / nq, qi = i % nq;
+        const float* ps = pb + ((size_t)s2 * kQPerCta + qi) * (HD + 2);
+        sm[s2 * kQPerCta + qi] = __ldcg(ps);
+        sl[s2 * kQPerCta + qi] = __ldcg(ps + 1);
+    }
+    __syncthreads();
+    if (t < nq) {
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < n_split; ++s2) M = fmaxf(M, sm[s2 * kQPerCta + t]);
+        float L = 0.f;
+        for (int s2 = 0; s2 < n_split; ++s2) {
+            const float ms = sm[s2 * kQPerCta + t];
+            const float w = (ms == -INFINITY) ? 0.f : expf(ms - M);
+            sw[s2 * kQPerCta + t] = w;
+            L += sl[s2 * kQPerCta + t] * w;
+        }
+        for (int s2 = 0; s2 < n_split; ++s2) sw[s2 * kQPerCta + t] /= L;
+    }
+    __syncthreads();
+    const int qdim = a.n_heads * HD;
+    for (int i = t; i < nq * HD; i += kAttnThreads) {
+        const int qi = i / HD, d = i % HD;
+        float O = 0.f;
+#pragma unroll 8
+        for (int s2 = 0; s2 < n_split; ++s2)
+            O += sw[s2 * kQPerCta + qi] * __ldcg(pb + ((size_t)s2 * kQPerCta + qi) * (HD + 2) + 2 + d);
+        const int qg = q0 + qi;
+        const int j = qg / G, h = g * G + qg % G;
+        store_act(static_cast<KT*>(a.out), (size_t)(row0 + j) * qdim + h * HD + d, a.out_lo, O);
+    }
+}
+
 template <typename KT, int HD>
 __global__ void __launch_bounds__(kAttnThreads)
 attention_kernel(AttnParams a, int n_rb) {
@@ -193,23 +237,7 @@ attention_kernel(AttnParams a, int n_rb) {
     __threadfence();
     // merge the splits in order
     const float* pb = a.part + (size_t)blk * a.splits * kQPerCta * (HD + 2);
-    for (int i = t; i < nq * HD; i += kAttnThreads) {
-        const int qi = i / HD, d = i % HD;
-        float M = -INFINITY;
-        for (int s = 0; s < n_split; ++s) M = fmaxf(M, __ldcg(pb + ((size_t)s * kQPerCta + qi) * (HD + 2)));
-        float L = 0.f, O = 0.f;
-        for (int s = 0; s < n_split; ++s) {
-            const float* ps = pb + ((size_t)s * kQPerCta + qi) * (HD + 2);
-            const float ms = __ldcg(ps);
-            if (ms == -INFINITY) continue;
-            const float w = expf(ms - M);
-            L += __ldcg(ps + 1) * w;
-            O += __ldcg(ps + 2 + d) * w;
-        }
-        const int qg = q0 + qi;
-        const int j = qg / G, h = g * G + qg % G;
-        store_act(static_cast<KT*>(a.out), (size_t)(row0 + j) * qdim + h * HD + d, a.out_lo, O / L);
-    }
+    merge_splits<KT, HD>(a, pb, n_split, nq, q0, G, g, row0, sK);
     if (t == 0) a.counters[blk] = 0;
 }
 
@@ -377,22 +405,8 @@ attention_decode_kernel(AttnParams a) {
     if (!sFlag[0]) return;
     __threadfence();
     const float* pb = a.part + (size_t)blk * a.splits * kQPerCta * (HD + 2);
-    for (int i = t; i < nq * HD; i += kAttnThreads) {
-        const int r = i / HD, d = i % HD;
-        float M = -INFINITY;
-        for (int s2 = 0; s2 < n_split; ++s2) M = fmaxf(M, __ldcg(pb + ((size_t)s2 * kQPerCta + r) * (HD + 2)));
-        float L = 0.f, O = 0.f;
-        for (int s2 = 0; s2 < n_split; ++s2) {
-            const float* ps2 = pb + ((size_t)s2 * kQPerCta + r) * (HD + 2);
-            const float ms = __ldcg(ps2);
-            if (ms == -INFINITY) continue;
-            const float w = expf(ms - M);
-            L += __ldcg(ps2 + 1) * w;
-            O += __ldcg(ps2 + 2 + d) * w;
-        }
-        const int j = r / G, h = g * G + r % G;
-        store_act(static_cast<KT*>(a.out), (size_t)(row0 + j) * qdim + h * HD + d, a.out_lo, O / L);
-    }
+    __syncthreads();
+    merge_splits<KT, HD>(a, pb, n_split, nq, 0, G, g, row0, sState);
     if (t == 0) a.counters[blk] = 0;
 }
 
@@ -400,7 +414,8 @@ template <typename KT, int HD, int RB>
 static void launch_decode(const AttnParams& a, dim3 grid, cudaStream_t st) {
     constexpr int EPL = 16 / (int)sizeof(KT);
     constexpr int NGRP = (kAttnThreads / 32) * (32 / (HD / EPL));
-    const size_t smem = sizeof(float) * ((size_t)NGRP * RB * (HD + 2) + RB * HD) + 16;
+    const size_t smem = sizeof(float) * (std::max((size_t)NGRP * RB * (HD + 2), (size_t)3 * 64 * kQPerCta) +
+                                         RB * HD) + 16;
     static bool set = false;
     if (!set) {
         cudaFuncSetAttribute(attention_decode_kernel<KT, HD, RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -127,41 +127,35 @@ __global__ void plan_kernel(PlanArgs a, RowPlan plan, const int* __restrict__ le
 
 // First residual rows of a forward: from the layer-L state (h_in) or the token
 // embedding.  Writes h, the gained GEMM input and per-128-feature sums of h^2.
+// One CTA per (row, 128-feature tile).
 template <typename WT>
 __global__ void __launch_bounds__(128)
 prologue_kernel(const float* __restrict__ h_in, int h_stride, const int* __restrict__ tok, int tok_stride,
                 int tok_col, const WT* __restrict__ embed, RowPlan plan, int d, int vocab,
                 const float* __restrict__ gain, float* h, WT* x, size_t x_lo, float* ss, int ss_stride, int* err) {
     __shared__ float red[4];
-    const int r = blockIdx.x, t = threadIdx.x;
+    const int r = blockIdx.x, tile = blockIdx.y, t = threadIdx.x;
     const int b = plan.row_seq[r], j = plan.row_local[r];
-    const float* src_h = nullptr;
-    const WT* src_e = nullptr;
-    if (h_in) {
-        src_h = h_in + ((size_t)b * h_stride + j) * d;
-    } else {
-        int token = tok[(size_t)b * tok_stride + tok_col + j];
-        if (token < 0 || token >= vocab) {
-            if (t == 0) dev_error(err, SPEC_DEVERR_TOKEN);
-            token = 0;
+    const int n = tile * 128 + t;
+    float v = 0.f;
+    if (n < d) {
+        if (h_in) {
+            v = h_in[((size_t)b * h_stride + j) * d + n];
+        } else {
+            int token = tok[(size_t)b * tok_stride + tok_col + j];
+            if (token < 0 || token >= vocab) {
+                if (t == 0 && tile == 0) dev_error(err, SPEC_DEVERR_TOKEN);
+                token = 0;
+            }
+            v = to_f32<WT>(embed[(size_t)token * d + n]);
         }
-        src_e = embed + (size_t)token * d;
+        h[(size_t)r * d + n] = v;
+        store_act(x, (size_t)r * d + n, x_lo, v * gain[n]);
     }
-    const int n_tiles = (d + 127) / 128;
-    for (int tile = 0; tile < n_tiles; ++tile) {
-        const int n = tile * 128 + t;
-        float v = 0.f;
-        if (n < d) {
-            v = src_h ? src_h[n] : to_f32<WT>(src_e[n]);
-            h[(size_t)r * d + n] = v;
-            store_act(x, (size_t)r * d + n, x_lo, v * gain[n]);
-        }
-        float s = warp_sum(v * v);
-        if ((t & 31) == 0) red[t >> 5] = s;
-        __syncthreads();
-        if (t == 0) ss[(size_t)tile * ss_stride + r] = (red[0] + red[1]) + (red[2] + red[3]);
-        __syncthreads();
-    }
+    const float s = warp_sum(v * v);
+    if ((t & 31) == 0) red[t >> 5] = s;
+    __syncthreads();
+    if (t == 0) ss[(size_t)tile * ss_stride + r] = (red[0] + red[1]) + (red[2] + red[3]);
 }
 
 __global__ void copy_rows_kernel(const float* __restrict__ h, float* __restrict__ dst, int rows, int d,
@@ -357,13 +351,13 @@ static int launch_prologue(spec_model* m, int T, const float* h_in, int h_stride
     const spec_model_config& c = m->cfg;
     const float* gain = layer_lo < c.n_layers ? m->layers[layer_lo].attn_g : m->final_g;
     if (m->bf16)
-        prologue_kernel<__nv_bfloat16><<<T, 128, 0, st>>>(h_in, h_stride, tok, tok_stride, tok_col,
+        prologue_kernel<__nv_bfloat16><<<dim3(T, (c.d_model + 127) / 128), 128, 0, st>>>(h_in, h_stride, tok, tok_stride, tok_col,
                                                          (const __nv_bfloat16*)m->embed, m->plan, c.d_model, c.vocab,
                                                          gain, m->h, (__nv_bfloat16*)m->x_in,
                                                          (size_t)m->max_rows_pad * c.d_model, m->ss_part, c.max_rows,
                                                          m->err);
     else
-        prologue_kernel<float><<<T, 128, 0, st>>>(h_in, h_stride, tok, tok_stride, tok_col, (const float*)m->embed,
+        prologue_kernel<float><<<dim3(T, (c.d_model + 127) / 128), 128, 0, st>>>(h_in, h_stride, tok, tok_stride, tok_col, (const float*)m->embed,
                                                  m->plan, c.d_model, c.vocab, gain, m->h, (float*)m->x_in, 0,
                                                  m->ss_part, c.max_rows, m->err);
     ++m->launches;

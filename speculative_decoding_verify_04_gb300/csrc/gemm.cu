@@ -88,22 +88,27 @@ __host__ __device__ inline int cta_of(const Split& s, long long u) {
 // epilogue shared memory
 struct EpiSmem {
     float tile[kRowChunk][kTileN + 1];
-    float rs[kRowChunk];
+    float rs_all[kMaxTPad];     // RMSNorm row scale of every row of the launch
     int flag;
     int wait_ok;
 };
 
 SPEC_DEV int etid() { return threadIdx.x & 127; }
 
-// per-chunk RMSNorm row scale
-SPEC_DEV void load_row_scale(const EpiParams& e, int j0, int nr, EpiSmem& sm) {
-    const int t = etid();
-    if (t < nr) {
-        const int r = e.r0 + j0 + t;
-        float s = 0.f;
-        for (int i = 0; i < e.ss_tiles; ++i) s += e.ss_in[(size_t)i * e.ss_stride + r];
-        sm.rs[t] = 1.0f / sqrtf(s * e.inv_d + e.eps);
+// RMSNorm row scales of all rows of the launch, computed once per CTA by the
+// epilogue threads before the first accumulator is ready (so off the critical
+// path): warp per row, lanes over the per-tile sums of squares.
+SPEC_DEV void load_row_scales(const EpiParams& e, EpiSmem& sm) {
+    if (e.kind != EPI_RESID) {
+        const int w = etid() >> 5, lane = etid() & 31;
+        for (int j = w; j < e.T; j += 4) {
+            float s = 0.f;
+            for (int i = lane; i < e.ss_tiles; i += 32) s += e.ss_in[(size_t)i * e.ss_stride + e.r0 + j];
+            s = warp_sum(s);
+            if (lane == 0) sm.rs_all[j] = 1.0f / sqrtf(s * e.inv_d + e.eps);
+        }
     }
+    named_bar(1, 128);
 }
 
 template <typename KT>
@@ -115,11 +120,11 @@ SPEC_DEV void apply_qkv(const EpiParams& e, int tile, int j0, int nr, EpiSmem& s
         const int n = tile * kTileN + mm;
         if (n >= e.N) continue;
         const int r = e.r0 + j0 + j;
-        const float v = sm.tile[j][mm] * sm.rs[j];
+        const float v = sm.tile[j][mm] * sm.rs_all[j0 + j];
         if (n < qd + kvd) {
             const int i = n & (hd - 1);
             const int pm = (i < half) ? mm + half : mm - half;
-            const float pv = sm.tile[j][pm] * sm.rs[j];
+            const float pv = sm.tile[j][pm] * sm.rs_all[j0 + j];
             const int pos = e.plan.row_pos[r];
             if (pos < 0 || pos >= e.max_position) { dev_error(e.err, SPEC_DEVERR_POSITION); continue; }
             const int fi = i & (half - 1);
@@ -177,8 +182,8 @@ SPEC_DEV void apply_swiglu(const EpiParams& e, int tile, int j0, int nr, EpiSmem
         const int f = tile * 64 + mm;
         if (f >= e.d_ff) continue;
         const int r = e.r0 + j0 + j;
-        const float g = sm.tile[j][mm] * sm.rs[j];
-        const float u = sm.tile[j][mm + 64] * sm.rs[j];
+        const float g = sm.tile[j][mm] * sm.rs_all[j0 + j];
+        const float u = sm.tile[j][mm + 64] * sm.rs_all[j0 + j];
         store_act(static_cast<XT*>(e.act), (size_t)r * e.d_ff + f, e.act_lo, g / (1.0f + expf(-g)) * u);
     }
 }
@@ -189,7 +194,7 @@ SPEC_DEV void apply_head(const EpiParams& e, int tile, int j0, int nr, EpiSmem& 
         const int v = tile * kTileN + mm;
         float l = -INFINITY;
         if (v < e.vocab) {
-            l = sm.tile[j][mm] * sm.rs[j];
+            l = sm.tile[j][mm] * sm.rs_all[j0 + j];
             if (e.logits) e.logits[(size_t)(e.r0 + j0 + j - e.logits_row0) * e.logits_stride + v] = l;
         }
         sm.tile[j][mm] = l;
@@ -216,10 +221,6 @@ SPEC_DEV void apply_head(const EpiParams& e, int tile, int j0, int nr, EpiSmem& 
 
 template <typename XT>
 SPEC_DEV void apply_chunk(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
-    if (e.kind != EPI_RESID) {
-        load_row_scale(e, j0, nr, sm);
-        named_bar(1, 128);
-    }
     switch (e.kind) {
         case EPI_QKV: apply_qkv<XT>(e, tile, j0, nr, sm); break;
         case EPI_RESID: apply_resid<XT>(e, tile, j0, nr, sm); break;
@@ -236,7 +237,16 @@ SPEC_DEV void head_finalize(const EpiParams& e, int n_tiles) {
     for (int j = w; j < e.T; j += 4) {
         const int r = e.r0 + j;
         spec_row_stats s = stat_empty();
-        for (int t = lane; t < n_tiles; t += 32) stat_merge(s, e.stat_part[(size_t)t * e.ss_stride + r]);
+        for (int t0 = lane; t0 < n_tiles; t0 += 32 * 8) {
+            spec_row_stats v[8];             // independent loads first, then the merges
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = t0 + 32 * i;
+                v[i] = t < n_tiles ? e.stat_part[(size_t)t * e.ss_stride + r] : stat_empty();
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) stat_merge(s, v[i]);
+        }
         s = stat_warp_merge(s);
         if (lane == 0) {
             e.row_stats[r] = s;
@@ -319,12 +329,19 @@ SPEC_DEV void finish_segment(const EpiParams& e, const Split& sp, int tile, int 
     const float* base = sp.part + (size_t)tile * sp.max_slots * sp.T_pad * kTileN;
     for (int ch = 0; ch < nchunks; ++ch) {
         const int nr = min(kRowChunk, e.T - ch * kRowChunk);
-        for (int i = 0; i < nr; ++i) {
-            const int j = ch * kRowChunk + i;
-            float s = 0.f;
-            for (int q = 0; q < nc; ++q) s += __ldcg(base + ((size_t)q * sp.T_pad + j) * kTileN + mm);
-            sm.tile[i][mm] = s;
+        float acc[kRowChunk];
+#pragma unroll
+        for (int i = 0; i < kRowChunk; ++i) acc[i] = 0.f;
+        for (int q = 0; q < nc; ++q) {           // slots in a fixed order: deterministic sums
+            const float* src = base + ((size_t)q * sp.T_pad + ch * kRowChunk) * kTileN + mm;
+            float v2[kRowChunk];
+#pragma unroll
+            for (int i = 0; i < kRowChunk; ++i) v2[i] = (i < nr) ? __ldcg(src + (size_t)i * kTileN) : 0.f;
+#pragma unroll
+            for (int i = 0; i < kRowChunk; ++i) acc[i] += v2[i];
         }
+#pragma unroll
+        for (int i = 0; i < kRowChunk; ++i) sm.tile[i][mm] = acc[i];
         named_bar(1, 128);
         apply_chunk<XT>(e, tile, ch * kRowChunk, nr, sm);
     }
@@ -462,6 +479,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         ld.taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         ld.acc_empty = acc_empty;
         uint32_t acc_phase = 0;
+        load_row_scales(e, sm);
         for (long long u = u_begin; u < u_end;) {
             const int tile = (int)(u / sp.kb);
             const long long seg_end = min(u_end, (long long)(tile + 1) * sp.kb);
@@ -514,6 +532,7 @@ gemm_f32_kernel(const float* __restrict__ W, const float* __restrict__ X, int x_
     __shared__ EpiSmem sm;
     const int c = blockIdx.x, t = threadIdx.x;
     const long long u_begin = unit_begin(sp, c), u_end = unit_begin(sp, c + 1);
+    load_row_scales(e, sm);
     for (long long u = u_begin; u < u_end;) {
         const int tile = (int)(u / sp.kb);
         const long long seg_end = min(u_end, (long long)(tile + 1) * sp.kb);
