@@ -43,6 +43,9 @@ def parse():
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="fewer layers of the same shape (small case for profiler captures)")
+    ap.add_argument("--exit-layer", type=int, default=None)
     return ap.parse_args()
 
 
@@ -196,7 +199,11 @@ def main():
     from speculative_decoding_verify_04_gb300 import spec
     from synthetic import SHAPES, make_weights, make_kv_context, make_tokens
 
+    import dataclasses
     shape = SHAPES["llama7b"]
+    if args.layers is not None:
+        shape = dataclasses.replace(shape, n_layers=args.layers,
+                                    exit_layer=args.exit_layer if args.exit_layer is not None else args.layers // 2)
     B, k = args.batch, K_DRAFT
     steps, warm = args.steps, args.warmup
     grow = (steps + warm + 2) * (k + 1) + 8
@@ -241,7 +248,6 @@ def main():
         dist.barrier()
     clocks = Clocks(local)
     clocks.start()
-    model.profile(True)
     n_launch0 = model.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -250,12 +256,20 @@ def main():
         step(i)
     e1.record(stream)
     torch.cuda.synchronize()
-    model.profile(False)
     launches = model.launch_count() - n_launch0
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
     verify_ms = sum(ev_v0[i].elapsed_time(ev_v1[i]) for i in range(steps)) / steps
     accepted = int(acc_log.sum().item())
+    # Instrumented pass of the same rounds: CUDA events around every GEMM and
+    # attention launch (on the library's stream) give the per-launch durations
+    # of the roofline.  Kept out of the timed region above because events
+    # between kernels stop consecutive kernels from overlapping.
+    model.profile(True)
+    for i in range(steps):
+        step()
+    torch.cuda.synchronize()
+    model.profile(False)
     g_ms, g_bytes, g_n = model.profile_read(0)
     a_ms, _, a_n = model.profile_read(1)
     err = model.device_error()
@@ -298,9 +312,9 @@ def main():
     # verify step algorithmic bytes: layers 12..31 + LM head weights + KV of layers 12..31 read once
     d, F, V = shape.d_model, shape.d_ff, shape.vocab
     layer_w = (3 * d * d + d * d + 2 * F * d + d * F) * 2
-    ctx_now = CTX + (warm + steps) * 1  # at least one token per round
-    kv_bytes = 20 * 2 * shape.n_kv_heads * shape.head_dim * 2 * (CTX + k + 1) * B
-    verify_bytes = 20 * layer_w + V * d * 2 + kv_bytes
+    n_ver = shape.n_layers - shape.exit_layer
+    kv_bytes = n_ver * 2 * shape.n_kv_heads * shape.head_dim * 2 * (CTX + k + 1) * B
+    verify_bytes = n_ver * layer_w + V * d * 2 + kv_bytes
     line = {
         "metric": METRIC,
         "value": value,
@@ -314,7 +328,8 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded random-init weights and KV context; no dataset)",
-        "config": {"workload": WORKLOAD, "batch": B, "k": k, "ctx": CTX, "exit_layer": 12, "n_layers": 32,
+        "config": {"workload": WORKLOAD if args.layers is None else WORKLOAD + f" (reduced: {shape.n_layers} layers)",
+                   "batch": B, "k": k, "ctx": CTX, "exit_layer": shape.exit_layer, "n_layers": shape.n_layers,
                    "l2": "inputs larger than L2 (13.5 GB weights re-streamed each round)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "accepted_tokens_per_s": world * (accepted + B * steps) / (ms / 1e3),
@@ -323,12 +338,15 @@ def main():
         "verify_candidate_tokens_per_s": world * cand_per_step / (verify_ms / 1e3),
         "verify_hbm_gbs": verify_bytes / (verify_ms / 1e3) / 1e9,
         "verify_hbm_frac": verify_bytes / (verify_ms / 1e3) / 1e9 / hbm,
-        "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel (tcgen05 skinny GEMM, all launches in the timed region)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "gemm_tc_kernel (tcgen05 skinny GEMM; every launch of an instrumented pass of the "
+                               "same rounds)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": (achieved / hbm) if achieved else None, "traffic": None,
                      "peak_source": peak_kind, "launches": g_n, "avg_launch_us": g_avg_ms * 1e3,
                      "avg_launch_bytes": g_avg_bytes},
         "attention": {"launches": a_n, "total_ms_per_step": a_ms / steps},
+        "pdl": os.environ.get("SPEC_PDL", "1") != "0",
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,

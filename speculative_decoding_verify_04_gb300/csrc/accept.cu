@@ -173,6 +173,8 @@ template <typename KT>
 __global__ void commit_tree_kernel(KT* kc, KT* vc, const int* len, const int* acc_len, const int* path,
                                    int path_stride, int n_layers, int n_kv_heads, int kv_batch, int kv_ctx,
                                    int hd, int* err) {
+    pdl_wait();
+    pdl_trigger();
     const int lh = blockIdx.x, b = blockIdx.y;
     const int layer = lh / n_kv_heads, kvh = lh % n_kv_heads;
     const int s = len[b], a = acc_len[b];
@@ -190,6 +192,8 @@ __global__ void commit_tree_kernel(KT* kc, KT* vc, const int* len, const int* ac
 }
 
 __global__ void commit_len_kernel(int* len, const int* acc_len, int batch, int kv_ctx, int* err) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= batch) return;
     const int n = len[b] + acc_len[b] + 1;
@@ -288,17 +292,18 @@ extern "C" int kv_commit(spec_kv* kv, int32_t batch, const int32_t* acc_len, con
         dim3 grid(m->cfg.n_layers * m->cfg.n_kv_heads, batch);
         const int threads = m->cfg.head_dim;
         if (m->bf16)
-            commit_tree_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
+            launch_k(m->pdl, commit_tree_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st,
                 (__nv_bfloat16*)kv->k, (__nv_bfloat16*)kv->v, kv->len, acc_len, path, path_stride, m->cfg.n_layers,
                 m->cfg.n_kv_heads, kv->batch, kv->max_ctx, m->cfg.head_dim, m->err);
         else
-            commit_tree_kernel<float><<<grid, threads, 0, st>>>((float*)kv->k, (float*)kv->v, kv->len, acc_len, path,
+            launch_k(m->pdl, commit_tree_kernel<float>, grid, dim3(threads), 0, st, (float*)kv->k, (float*)kv->v, kv->len, acc_len, path,
                                                                 path_stride, m->cfg.n_layers, m->cfg.n_kv_heads,
                                                                 kv->batch, kv->max_ctx, m->cfg.head_dim, m->err);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return check_cuda(e, "kv_commit tree launch");
     }
-    commit_len_kernel<<<(batch + 127) / 128, 128, 0, st>>>(kv->len, acc_len, batch, kv->max_ctx, m->err);
+    launch_k(m->pdl, commit_len_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, kv->len, acc_len, batch, kv->max_ctx,
+             m->err);
     m->launches += path ? 2 : 1;
     return check_cuda(cudaGetLastError(), "kv_commit launch");
 }

@@ -78,6 +78,8 @@ __device__ void merge_splits(const AttnParams& a, const float* pb, int n_split, 
 template <typename KT, int HD>
 __global__ void __launch_bounds__(kAttnThreads)
 attention_kernel(AttnParams a, int n_rb) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int QPT = kQPerCta * HD / kAttnThreads;   // queries per thread in the PV step
     extern __shared__ float smf[];
     float* sK = smf;                                     // [64][HD+1]
@@ -252,6 +254,8 @@ attention_kernel(AttnParams a, int n_rb) {
 template <typename KT, int HD, int RB>
 __global__ void __launch_bounds__(kAttnThreads)
 attention_decode_kernel(AttnParams a) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int EPL = 16 / (int)sizeof(KT);        // elements per lane
     constexpr int LPK = HD / EPL;                    // lanes per key row
     constexpr int KPW = 32 / LPK;                    // key rows per warp step
@@ -411,7 +415,7 @@ attention_decode_kernel(AttnParams a) {
 }
 
 template <typename KT, int HD, int RB>
-static void launch_decode(const AttnParams& a, dim3 grid, cudaStream_t st) {
+static void launch_decode(bool pdl, const AttnParams& a, dim3 grid, cudaStream_t st) {
     constexpr int EPL = 16 / (int)sizeof(KT);
     constexpr int NGRP = (kAttnThreads / 32) * (32 / (HD / EPL));
     const size_t smem = sizeof(float) * (std::max((size_t)NGRP * RB * (HD + 2), (size_t)3 * 64 * kQPerCta) +
@@ -422,15 +426,15 @@ static void launch_decode(const AttnParams& a, dim3 grid, cudaStream_t st) {
                              (int)smem);
         set = true;
     }
-    attention_decode_kernel<KT, HD, RB><<<grid, kAttnThreads, smem, st>>>(a);
+    launch_k(pdl, attention_decode_kernel<KT, HD, RB>, grid, dim3(kAttnThreads), smem, st, a);
 }
 
 template <typename KT, int HD>
-static void launch_decode_rb(const AttnParams& a, int nq, dim3 grid, cudaStream_t st) {
-    if (nq <= 1) launch_decode<KT, HD, 1>(a, grid, st);
-    else if (nq <= 2) launch_decode<KT, HD, 2>(a, grid, st);
-    else if (nq <= 4) launch_decode<KT, HD, 4>(a, grid, st);
-    else launch_decode<KT, HD, 8>(a, grid, st);
+static void launch_decode_rb(bool pdl, const AttnParams& a, int nq, dim3 grid, cudaStream_t st) {
+    if (nq <= 1) launch_decode<KT, HD, 1>(pdl, a, grid, st);
+    else if (nq <= 2) launch_decode<KT, HD, 2>(pdl, a, grid, st);
+    else if (nq <= 4) launch_decode<KT, HD, 4>(pdl, a, grid, st);
+    else launch_decode<KT, HD, 8>(pdl, a, grid, st);
 }
 
 static int rows_blocks(int max_rows_per_seq, int G) {
@@ -486,11 +490,11 @@ int launch_attention(spec_model* m, const AttnParams& a0, int max_rows_per_seq, 
         dim3 grid(a.splits, a.n_kv_heads, a.batch);
         const int slot = prof_start(m, st);
         if (a.head_dim == 128) {
-            if (m->bf16) launch_decode_rb<__nv_bfloat16, 128>(a, nq_max, grid, st);
-            else launch_decode_rb<float, 128>(a, nq_max, grid, st);
+            if (m->bf16) launch_decode_rb<__nv_bfloat16, 128>(m->pdl, a, nq_max, grid, st);
+            else launch_decode_rb<float, 128>(m->pdl, a, nq_max, grid, st);
         } else {
-            if (m->bf16) launch_decode_rb<__nv_bfloat16, 64>(a, nq_max, grid, st);
-            else launch_decode_rb<float, 64>(a, nq_max, grid, st);
+            if (m->bf16) launch_decode_rb<__nv_bfloat16, 64>(m->pdl, a, nq_max, grid, st);
+            else launch_decode_rb<float, 64>(m->pdl, a, nq_max, grid, st);
         }
         ++m->launches;
         prof_stop(m, slot, st, PROF_ATTN, 0.0);
@@ -511,18 +515,18 @@ int launch_attention(spec_model* m, const AttnParams& a0, int max_rows_per_seq, 
     if (a.head_dim == 128) {
         if (m->bf16) {
             cudaFuncSetAttribute(attention_kernel<__nv_bfloat16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            attention_kernel<__nv_bfloat16, 128><<<grid, kAttnThreads, smem, st>>>(a, n_rb);
+            launch_k(m->pdl, attention_kernel<__nv_bfloat16, 128>, grid, dim3(kAttnThreads), smem, st, a, n_rb);
         } else {
             cudaFuncSetAttribute(attention_kernel<float, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            attention_kernel<float, 128><<<grid, kAttnThreads, smem, st>>>(a, n_rb);
+            launch_k(m->pdl, attention_kernel<float, 128>, grid, dim3(kAttnThreads), smem, st, a, n_rb);
         }
     } else {
         if (m->bf16) {
             cudaFuncSetAttribute(attention_kernel<__nv_bfloat16, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            attention_kernel<__nv_bfloat16, 64><<<grid, kAttnThreads, smem, st>>>(a, n_rb);
+            launch_k(m->pdl, attention_kernel<__nv_bfloat16, 64>, grid, dim3(kAttnThreads), smem, st, a, n_rb);
         } else {
             cudaFuncSetAttribute(attention_kernel<float, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            attention_kernel<float, 64><<<grid, kAttnThreads, smem, st>>>(a, n_rb);
+            launch_k(m->pdl, attention_kernel<float, 64>, grid, dim3(kAttnThreads), smem, st, a, n_rb);
         }
     }
     ++m->launches;

@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 
@@ -91,6 +92,8 @@ struct PlanArgs {
 // one row per sequence at slot / position s_b + j, seeing slots [0, s_b + j]
 // (the earlier passes' rows count as context: base s_b + j, local row 0).
 __global__ void plan_kernel(PlanArgs a, RowPlan plan, const int* __restrict__ len, int T) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     const PlanParams& p = a.p;
     // a draft pass sees the rows of the earlier passes as context: its base is s + j
@@ -133,6 +136,8 @@ __global__ void __launch_bounds__(128)
 prologue_kernel(const float* __restrict__ h_in, int h_stride, const int* __restrict__ tok, int tok_stride,
                 int tok_col, const WT* __restrict__ embed, RowPlan plan, int d, int vocab,
                 const float* __restrict__ gain, float* h, WT* x, size_t x_lo, float* ss, int ss_stride, int* err) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float red[4];
     const int r = blockIdx.x, tile = blockIdx.y, t = threadIdx.x;
     const int b = plan.row_seq[r], j = plan.row_local[r];
@@ -160,17 +165,23 @@ prologue_kernel(const float* __restrict__ h_in, int h_stride, const int* __restr
 
 __global__ void copy_rows_kernel(const float* __restrict__ h, float* __restrict__ dst, int rows, int d,
                                  int dst_row_stride, int dst_col) {
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x;
     for (int n = threadIdx.x; n < d; n += blockDim.x)
         dst[((size_t)r * dst_row_stride + dst_col) * d + n] = h[(size_t)r * d + n];
 }
 
 __global__ void set_col0_kernel(const int* __restrict__ t0, int* cand, int stride, int batch) {
+    pdl_wait();
+    pdl_trigger();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < batch) cand[(size_t)b * stride] = t0[b];
 }
 
 __global__ void add_len_kernel(int* len, int seq, int n, int cap, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x == 0 && blockIdx.x == 0) {
         const int v = len[seq] + n;
         if (v > cap) dev_error(err, SPEC_DEVERR_CAPACITY);
@@ -341,7 +352,8 @@ static int launch_plan(spec_model* m, const PlanParams& p, int T, const int* len
         r += (p.mode == 2) ? 1 : p.n_rows[b];
     }
     const int n = std::max(std::max(T, p.batch), kMaxSeqRows);
-    plan_kernel<<<(n + 127) / 128, 128, 0, st>>>(a, m->plan, len, T);
+    cudaError_t le = launch_k(m->pdl, plan_kernel, dim3((n + 127) / 128), dim3(128), 0, st, a, m->plan, len, T);
+    if (le != cudaSuccess) return check_cuda(le, "plan launch");
     ++m->launches;
     return check_cuda(cudaGetLastError(), "plan launch");
 }
@@ -351,13 +363,13 @@ static int launch_prologue(spec_model* m, int T, const float* h_in, int h_stride
     const spec_model_config& c = m->cfg;
     const float* gain = layer_lo < c.n_layers ? m->layers[layer_lo].attn_g : m->final_g;
     if (m->bf16)
-        prologue_kernel<__nv_bfloat16><<<dim3(T, (c.d_model + 127) / 128), 128, 0, st>>>(h_in, h_stride, tok, tok_stride, tok_col,
+        launch_k(m->pdl, prologue_kernel<__nv_bfloat16>, dim3(T, (c.d_model + 127) / 128), dim3(128), 0, st, h_in, h_stride, tok, tok_stride, tok_col,
                                                          (const __nv_bfloat16*)m->embed, m->plan, c.d_model, c.vocab,
                                                          gain, m->h, (__nv_bfloat16*)m->x_in,
                                                          (size_t)m->max_rows_pad * c.d_model, m->ss_part, c.max_rows,
                                                          m->err);
     else
-        prologue_kernel<float><<<dim3(T, (c.d_model + 127) / 128), 128, 0, st>>>(h_in, h_stride, tok, tok_stride, tok_col, (const float*)m->embed,
+        launch_k(m->pdl, prologue_kernel<float>, dim3(T, (c.d_model + 127) / 128), dim3(128), 0, st, h_in, h_stride, tok, tok_stride, tok_col, (const float*)m->embed,
                                                  m->plan, c.d_model, c.vocab, gain, m->h, (float*)m->x_in, 0,
                                                  m->ss_part, c.max_rows, m->err);
     ++m->launches;
@@ -420,6 +432,10 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
     if ((rc = check_cuda(cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device), "attr")))
         return fail(rc);
     m->bf16 = c.dtype == SPEC_DTYPE_BF16;
+    {   // SPEC_PDL=0 turns programmatic dependent launch off (kernels then run back to back)
+        const char* e = getenv("SPEC_PDL");
+        m->pdl = !(e && e[0] == '0');
+    }
     m->elem = m->bf16 ? 2 : 4;
     if (m->bf16) {
         int major = 0;
@@ -707,7 +723,7 @@ extern "C" int spec_prefill(spec_model* m, spec_kv* kv, int32_t seq, const int32
             hs.batch = seq + 1;
             SPEC_TRY(run_head(m, kv, hs, st));
         }
-        add_len_kernel<<<1, 32, 0, st>>>(kv->len, seq, T, kv->max_ctx, m->err);
+        launch_k(m->pdl, add_len_kernel, dim3(1), dim3(32), 0, st, kv->len, seq, T, kv->max_ctx, m->err);
         ++m->launches;
         SPEC_CUDA(cudaGetLastError(), "length update");
     }
@@ -723,7 +739,7 @@ extern "C" int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32
     if (batch < 1 || batch > kv->batch || batch > c.max_rows) return set_error(SPEC_ERR_ARG, "spec_draft: bad batch");
     if (k < 1 || k + 1 > kMaxSeqRows) return set_error(SPEC_ERR_ARG, "spec_draft: k must be in [1, 63]");
     cudaStream_t st = (cudaStream_t)stream;
-    set_col0_kernel<<<(batch + 127) / 128, 128, 0, st>>>(t0, cand, k + 1, batch);
+    launch_k(m->pdl, set_col0_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, t0, cand, k + 1, batch);
     ++m->launches;
     SPEC_CUDA(cudaGetLastError(), "draft init");
     for (int j = 0; j <= k; ++j) {
@@ -734,7 +750,7 @@ extern "C" int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32
         SPEC_TRY(launch_plan(m, p, batch, kv->len, st));
         SPEC_TRY(launch_prologue(m, batch, nullptr, 0, cand, k + 1, j, 0, st));
         SPEC_TRY(run_layers(m, kv, batch, batch, 1, 0, c.exit_layer, 0, j < k, st));
-        copy_rows_kernel<<<batch, 256, 0, st>>>(m->h, h_L, batch, c.d_model, k + 1, j);
+        launch_k(m->pdl, copy_rows_kernel, dim3(batch), dim3(256), 0, st, (const float*)m->h, h_L, batch, c.d_model, k + 1, j);
         ++m->launches;
         SPEC_CUDA(cudaGetLastError(), "draft state copy");
         if (j < k) {

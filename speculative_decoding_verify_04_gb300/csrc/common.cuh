@@ -11,6 +11,24 @@
 
 #define SPEC_DEV __device__ __forceinline__
 
+// Launch `kernel` on `st`, with the programmatic-stream-serialization attribute
+// when `pdl` is set (the kernel then overlaps the tail of the previous one).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // device error word
 SPEC_DEV void dev_error(int* err, int bits) {
@@ -185,6 +203,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (static_cast<uint32_t>(N >> 3) << 17)
          | (static_cast<uint32_t>(M >> 4) << 24);
 }
+
+// Programmatic dependent launch: a kernel launched with the PDL attribute may
+// start while the previous kernel on the stream is still running.  It must call
+// pdl_wait() before touching memory the previous kernel reads or writes;
+// pdl_trigger() lets the next kernel launch early.  Both are no-ops when the
+// kernel was launched without the attribute.
+SPEC_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+SPEC_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // named barrier among `count` threads (id 0 is __syncthreads)
 SPEC_DEV void named_bar(int id, int count) {

@@ -412,16 +412,33 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) pdl_trigger();
 
     if (warp == 4) {
         if (lane == 0) {
             tma_prefetch_desc(&tmW);
             tma_prefetch_desc(&tmX);
             const uint64_t pw = l2_policy_evict_first(), px = l2_policy_evict_last();
-            int stage = 0;
-            uint32_t phase = 0;
-            long long issued = 0;
-            for (long long u = u_begin; u < u_end; ++u) {
+            // The first ring of weight tiles does not depend on the previous kernel:
+            // issue it before waiting for that kernel, then the activation tiles.
+            const long long npre = min((long long)L.stages, u_end - u_begin);
+            for (long long i = 0; i < npre; ++i) {
+                const long long u = u_begin + i;
+                const int tile = (int)(u / sp.kb), kb = (int)(u % sp.kb);
+                mbar_arrive_expect_tx(full + i, kATileBytes + L.b_bytes);
+                tma_load_2d(sA + (size_t)i * kATileBytes, &tmW, kb * kTileK, tile * kTileN, full + i, pw);
+            }
+            pdl_wait();
+            for (long long i = 0; i < npre; ++i) {
+                const int kb = (int)((u_begin + i) % sp.kb);
+                tma_load_2d(sB + (size_t)i * L.b_bytes, &tmX, kb * kTileK, e.r0, full + i, px);
+                tma_load_2d(sB + (size_t)i * L.b_bytes + L.b_bytes / 2, &tmX, kb * kTileK, L.rows_pad + e.r0,
+                            full + i, px);
+            }
+            int stage = (int)(npre % L.stages);
+            uint32_t phase = (npre == L.stages) ? 1u : 0u;
+            long long issued = npre;
+            for (long long u = u_begin + npre; u < u_end; ++u) {
                 const int tile = (int)(u / sp.kb), kb = (int)(u % sp.kb);
                 if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, e.err)) break;
                 mbar_arrive_expect_tx(full + stage, kATileBytes + L.b_bytes);
@@ -479,6 +496,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
         ld.taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         ld.acc_empty = acc_empty;
         uint32_t acc_phase = 0;
+        pdl_wait();
         load_row_scales(e, sm);
         for (long long u = u_begin; u < u_end;) {
             const int tile = (int)(u / sp.kb);
@@ -532,6 +550,8 @@ gemm_f32_kernel(const float* __restrict__ W, const float* __restrict__ X, int x_
     __shared__ EpiSmem sm;
     const int c = blockIdx.x, t = threadIdx.x;
     const long long u_begin = unit_begin(sp, c), u_end = unit_begin(sp, c + 1);
+    pdl_wait();
+    pdl_trigger();
     load_row_scales(e, sm);
     for (long long u = u_begin; u < u_end;) {
         const int tile = (int)(u / sp.kb);
@@ -640,9 +660,10 @@ int launch_gemm(spec_model* m, const GemmLaunch& g, EpiParams e, int xbuf, cudaS
                 cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
                 attr_set = true;
             }
-            gemm_tc_kernel<<<s.G, kTcThreads, smem, st>>>(*g.tmW, m->tm_x[xbuf][T_pad / 16 - 1], s, L, ec);
+            launch_k(m->pdl, gemm_tc_kernel, dim3(s.G), dim3(kTcThreads), smem, st, *g.tmW,
+                     m->tm_x[xbuf][T_pad / 16 - 1], s, L, ec);
         } else {
-            gemm_f32_kernel<<<s.G, 128, 0, st>>>(static_cast<const float*>(g.W), static_cast<const float*>(g.X),
+            launch_k(m->pdl, gemm_f32_kernel, dim3(s.G), dim3(128), 0, st, static_cast<const float*>(g.W), static_cast<const float*>(g.X),
                                                  g.x_stride, g.N, g.K, s, ec);
         }
         ++m->launches;

@@ -105,6 +105,8 @@ struct spec_model {
     // X tensor maps by buffer (0 x_in, 1 x_attn, 2 x_act) and T_pad/16 - 1
     CUtensorMap tm_x[3][spec::kMaxTPad / 16];
 
+    bool pdl = true;                 // launch forward kernels with programmatic dependent launch
+
     // tracing: kernel launches issued, and (when enabled) CUDA events around
     // every GEMM / attention launch with the launch's algorithmic bytes
     long long launches = 0;
