@@ -231,12 +231,10 @@ attention_kernel(AttnParams a, int n_rb) {
         part[t * (HD + 2)] = sM[t];
         part[t * (HD + 2) + 1] = sL[t];
     }
-    __threadfence();
     __syncthreads();
-    if (t == 0) sFlag[0] = (atomicAdd(a.counters + blk, 1) == n_split - 1);
+    if (t == 0) sFlag[0] = (atomic_add_acq_rel(a.counters + blk, 1) == n_split - 1);
     __syncthreads();
     if (!sFlag[0]) return;
-    __threadfence();
     // merge the splits in order
     const float* pb = a.part + (size_t)blk * a.splits * kQPerCta * (HD + 2);
     merge_splits<KT, HD>(a, pb, n_split, nq, q0, G, g, row0, sK);
@@ -402,12 +400,10 @@ attention_decode_kernel(AttnParams a) {
         part[r * (HD + 2) + 2 + d] = O;
         if (d == 0) { part[r * (HD + 2)] = M; part[r * (HD + 2) + 1] = L; }
     }
-    __threadfence();
     __syncthreads();
-    if (t == 0) sFlag[0] = (atomicAdd(a.counters + blk, 1) == n_split - 1);
+    if (t == 0) sFlag[0] = (atomic_add_acq_rel(a.counters + blk, 1) == n_split - 1);
     __syncthreads();
     if (!sFlag[0]) return;
-    __threadfence();
     const float* pb = a.part + (size_t)blk * a.splits * kQPerCta * (HD + 2);
     __syncthreads();
     merge_splits<KT, HD>(a, pb, n_split, nq, 0, G, g, row0, sState);

@@ -212,6 +212,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 SPEC_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 SPEC_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Arrival counter of a "last CTA finishes the job" pattern: the caller's CTA
+// has synchronised (bar.sync) after its writes; one thread adds with
+// acquire-release semantics at GPU scope, publishing the CTA's writes and, for
+// the last arrival, making every other CTA's published writes visible (the
+// following bar.sync extends that to the whole CTA).
+SPEC_DEV int atomic_add_acq_rel(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // named barrier among `count` threads (id 0 is __syncthreads)
 SPEC_DEV void named_bar(int id, int count) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");

@@ -258,7 +258,6 @@ SPEC_DEV void head_finalize(const EpiParams& e, int n_tiles) {
         }
     }
     if (e.head_mode == HEAD_ACCEPT_CHAIN || e.head_mode == HEAD_ACCEPT_TREE) {
-        __threadfence();
         named_bar(1, 128);
         for (int b = etid(); b < e.batch; b += 128) {
             const int r0 = e.plan.seq_row0[b], n = e.plan.seq_nrows[b];
@@ -276,12 +275,10 @@ SPEC_DEV void head_finalize(const EpiParams& e, int n_tiles) {
 // Called by all 128 epilogue threads after a tile's epilogue has run.
 SPEC_DEV void head_tile_done(const EpiParams& e, int n_tiles, EpiSmem& sm) {
     if (e.kind != EPI_HEAD) return;
-    __threadfence();
     named_bar(1, 128);
-    if (etid() == 0) sm.flag = (atomicAdd(e.done_counter, 1) == n_tiles - 1);
+    if (etid() == 0) sm.flag = (atomic_add_acq_rel(e.done_counter, 1) == n_tiles - 1);
     named_bar(1, 128);
     if (sm.flag) {
-        __threadfence();
         head_finalize(e, n_tiles);
         if (etid() == 0) *e.done_counter = 0;
     }
@@ -320,12 +317,10 @@ SPEC_DEV void finish_segment(const EpiParams& e, const Split& sp, int tile, int 
         }
     }
     ld.release();
-    __threadfence();
     named_bar(1, 128);
-    if (mm == 0) sm.flag = (atomicAdd(sp.counters + tile, 1) == nc - 1);
+    if (mm == 0) sm.flag = (atomic_add_acq_rel(sp.counters + tile, 1) == nc - 1);
     named_bar(1, 128);
     if (!sm.flag) return;
-    __threadfence();
     const float* base = sp.part + (size_t)tile * sp.max_slots * sp.T_pad * kTileN;
     for (int ch = 0; ch < nchunks; ++ch) {
         const int nr = min(kRowChunk, e.T - ch * kRowChunk);
