@@ -433,6 +433,269 @@ static void launch_decode_rb(bool pdl, const AttnParams& a, int nq, dim3 grid, c
     else launch_decode<KT, HD, 8>(pdl, a, grid, st);
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core decode attention (bf16 K/V, mma.sync m16n8k16, f32 accumulate).
+//
+// A CTA handles 16 query vectors of one (sequence, kv head) -- the M side of
+// the MMAs -- over one key range; its 4 warps take 16-key tiles in turn.
+// Per tile:  S[16 q x 16 keys] = Q K^T  (Q split into bf16 hi + lo, two MMAs
+// per k-step),  online softmax on S,  O += P V.
+// The order of the head dimensions inside a k-step and of the keys inside a
+// tile is free (both sides of each product use the same order), so it is
+// chosen to make every global load a contiguous 16-byte piece of a K or V row
+// and to make the S accumulator fragment the A fragment of P V directly:
+//   QK^T, k-step ks = 2*kp + s: lane (g, c) holds logical k {2c, 2c+1, 2c+8,
+//     2c+9} = head dims 32*kp + 8*c + 4*s + {0, 1, 2, 3};
+//   QK^T, key half h: column n = g is tile key 4*(g/2) + 2*h + g%2, so the S
+//     accumulator of lane (g, c) holds tile keys 4c, 4c+1 (half 0) and 4c+2,
+//     4c+3 (half 1) -- the A fragment of P V for keys {4c .. 4c+3};
+//   P V, n-tile nt: column n = g is head dim (HD/8)*g + nt, so lane (g, c)
+//     reads V rows 4c .. 4c+3 at dims (HD/8)*g .. (HD/8)*g + HD/8 - 1.
+
+SPEC_DEV void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                       uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+SPEC_DEV uint32_t pack_bf16(float lo, float hi) {
+    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return l | (h << 16);
+}
+// residuals of pack_bf16: x - bf16(x) for both halves
+SPEC_DEV uint32_t pack_bf16_lo(float lo, float hi) {
+    return pack_bf16(lo - __bfloat162float(__float2bfloat16_rn(lo)), hi - __bfloat162float(__float2bfloat16_rn(hi)));
+}
+// two bf16 from 16-bit halves of two 32-bit words: (low half of x, low half of y) etc.
+SPEC_DEV uint32_t pair_lo(uint32_t x, uint32_t y) { return __byte_perm(x, y, 0x5410); }
+SPEC_DEV uint32_t pair_hi(uint32_t x, uint32_t y) { return __byte_perm(x, y, 0x7632); }
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads)
+attention_mma_kernel(AttnParams a, int n_qb) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int KP = HD / 32;          // 16-byte pieces of a K row per lane
+    constexpr int KS = HD / 16;          // QK^T k-steps
+    constexpr int VD = HD / 8;           // P V n-tiles = V dims per lane
+    constexpr int VP = VD / 8;           // 16-byte pieces of a V row per lane
+    extern __shared__ float smf[];
+    uint4* sQ = reinterpret_cast<uint4*>(smf);                    // [2][KS][32] fragments (hi, lo)
+    float* sState = smf + 2 * KS * 32 * 4;                        // [4 warps][16][HD + 2]
+    int* sFlag = reinterpret_cast<int*>(sState + 4 * 16 * (HD + 2));
+    unsigned long long* sMask = reinterpret_cast<unsigned long long*>(sFlag + 4);   // [16]
+
+    const int split = blockIdx.x / n_qb, qb = blockIdx.x % n_qb, g = blockIdx.y, b = blockIdx.z;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int gq = lane >> 2, cq = lane & 3;
+    const int G = a.n_heads / a.n_kv_heads;
+    const int T_b = a.plan.seq_nrows[b];
+    const int nq_total = T_b * G;
+    const int q0 = qb * 16;
+    if (q0 >= nq_total) return;
+    const int nq = min(16, nq_total - q0);
+    const int base = a.plan.seq_base[b];
+    const int n_keys = base + T_b;
+    int chunk = (n_keys + a.splits - 1) / a.splits;
+    chunk = ((chunk + 63) / 64) * 64;
+    const int n_split = (n_keys + chunk - 1) / chunk;
+    if (split >= n_split) return;
+    if (n_keys > a.kv_ctx) { if (t == 0) dev_error(a.err, SPEC_DEVERR_CAPACITY); return; }
+    const int k_begin = split * chunk, k_end = min(n_keys, k_begin + chunk);
+    const int row0 = a.plan.seq_row0[b];
+    const int qdim = a.n_heads * HD;
+
+    // Q fragments (pre-scaled f32 -> bf16 hi + lo) in shared memory, in lane order
+    for (int i = t; i < KS * 32; i += kAttnThreads) {
+        const int ks = i / 32, ln = i % 32, fg = ln >> 2, fc = ln & 3;
+        const int kp = ks >> 1, s = ks & 1;
+        const int d0 = 32 * kp + 8 * fc + 4 * s;
+        float x[2][4];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int qi = fg + 8 * rr;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[rr][e] = 0.f;
+            if (qi < nq) {
+                const int qg = q0 + qi;
+                const float* qp = a.q + (size_t)(row0 + qg / G) * qdim + (g * G + qg % G) * HD + d0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[rr][e] = qp[e];
+            }
+        }
+        // A fragment: {row g: k 2c,2c+1} {row g+8: k 2c,2c+1} {row g: k 2c+8,+9} {row g+8: k 2c+8,+9}
+        sQ[i] = make_uint4(pack_bf16(x[0][0], x[0][1]), pack_bf16(x[1][0], x[1][1]), pack_bf16(x[0][2], x[0][3]),
+                           pack_bf16(x[1][2], x[1][3]));
+        sQ[KS * 32 + i] = make_uint4(pack_bf16_lo(x[0][0], x[0][1]), pack_bf16_lo(x[1][0], x[1][1]),
+                                     pack_bf16_lo(x[0][2], x[0][3]), pack_bf16_lo(x[1][2], x[1][3]));
+    }
+    if (t < 16) {
+        unsigned long long mk = 0ull;
+        if (t < nq) {
+            const int j = (q0 + t) / G;
+            if (a.tree) {
+                for (int x = j; x >= 0; x = a.plan.tree_parent[x]) mk |= 1ull << x;
+            } else {
+                mk = (j >= 63) ? ~0ull : ((2ull << j) - 1ull);
+            }
+        }
+        sMask[t] = mk;
+    }
+    __syncthreads();
+
+    const size_t head_off = (((size_t)a.layer * a.kv_batch + b) * a.n_kv_heads + g) * a.kv_ctx;
+    const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(a.kc) + head_off * HD;
+    const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(a.vc) + head_off * HD;
+    const unsigned long long mk0 = sMask[gq], mk1 = sMask[gq + 8];
+
+    float o[VD][4];
+#pragma unroll
+    for (int nt = 0; nt < VD; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+
+    for (int kt = k_begin + 16 * warp; kt < k_end; kt += 64) {
+        uint4 kr[2][KP], vr[4][VP];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int key = min(kt + 4 * (gq >> 1) + 2 * h + (gq & 1), a.kv_ctx - 1);
+            const uint4* row = reinterpret_cast<const uint4*>(Kg + (size_t)key * HD);
+#pragma unroll
+            for (int p = 0; p < KP; ++p) kr[h][p] = __ldg(row + 4 * p + cq);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int key = kt + 4 * cq + r;
+            const uint4* row = reinterpret_cast<const uint4*>(Vg + (size_t)min(key, a.kv_ctx - 1) * HD);
+#pragma unroll
+            for (int p = 0; p < VP; ++p) vr[r][p] = __ldg(row + VP * gq + p);
+        }
+        // S = Q K^T for the two key halves
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const uint4 qh = sQ[ks * 32 + lane], ql = sQ[KS * 32 + ks * 32 + lane];
+            const int kp = ks >> 1, s = ks & 1;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t w[4] = {kr[h][kp].x, kr[h][kp].y, kr[h][kp].z, kr[h][kp].w};
+                const uint32_t b0 = w[2 * s], b1 = w[2 * s + 1];
+                mma16816(sc[h], qh.x, qh.y, qh.z, qh.w, b0, b1);
+                mma16816(sc[h], ql.x, ql.y, ql.z, ql.w, b0, b1);
+            }
+        }
+        // mask: lane holds rows g (sc[h][0..1]) and g+8 (sc[h][2..3]) at tile keys 4c + 2h + {0, 1}
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int key = kt + 4 * cq + 2 * h + e;
+                const bool in = key < k_end;
+                const bool v0 = in && (key < base || ((mk0 >> (key - base)) & 1ull));
+                const bool v1 = in && (key < base || ((mk1 >> (key - base)) & 1ull));
+                if (!v0) sc[h][e] = -INFINITY;
+                if (!v1) sc[h][2 + e] = -INFINITY;
+            }
+        }
+        // online softmax per row (the 16 keys of a row sit in the 4 lanes of a quad)
+        float alpha[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            float mt = fmaxf(fmaxf(sc[0][2 * rr], sc[0][2 * rr + 1]), fmaxf(sc[1][2 * rr], sc[1][2 * rr + 1]));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+            const float mn = fmaxf(m_r[rr], mt);
+            float ps = 0.f;
+            if (mn == -INFINITY) {
+                alpha[rr] = 1.f;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) sc[h][2 * rr] = sc[h][2 * rr + 1] = 0.f;
+            } else {
+                alpha[rr] = (m_r[rr] == -INFINITY) ? 0.f : expf(m_r[rr] - mn);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    sc[h][2 * rr] = expf(sc[h][2 * rr] - mn);
+                    sc[h][2 * rr + 1] = expf(sc[h][2 * rr + 1] - mn);
+                    ps += sc[h][2 * rr] + sc[h][2 * rr + 1];
+                }
+            }
+            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+            l_r[rr] = l_r[rr] * alpha[rr] + ps;
+            m_r[rr] = mn;
+        }
+        // P (A fragment of P V): keys 4c..4c+1 from half 0, 4c+2..4c+3 from half 1
+        const uint32_t pa0 = pack_bf16(sc[0][0], sc[0][1]), pa1 = pack_bf16(sc[0][2], sc[0][3]);
+        const uint32_t pa2 = pack_bf16(sc[1][0], sc[1][1]), pa3 = pack_bf16(sc[1][2], sc[1][3]);
+        // keys past the range contribute p = 0; clear their V rows so stale values cannot reach O
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            if (kt + 4 * cq + r >= k_end)
+#pragma unroll
+                for (int p = 0; p < VP; ++p) vr[r][p] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int nt = 0; nt < VD; ++nt) {
+            const int p = nt >> 3, e = nt & 7, wi = e >> 1;
+            const uint32_t w0 = (&vr[0][p].x)[wi], w1 = (&vr[1][p].x)[wi];
+            const uint32_t w2 = (&vr[2][p].x)[wi], w3 = (&vr[3][p].x)[wi];
+            const uint32_t b0 = (e & 1) ? pair_hi(w0, w1) : pair_lo(w0, w1);
+            const uint32_t b1 = (e & 1) ? pair_hi(w2, w3) : pair_lo(w2, w3);
+            o[nt][0] *= alpha[0];
+            o[nt][1] *= alpha[0];
+            o[nt][2] *= alpha[1];
+            o[nt][3] *= alpha[1];
+            mma16816(o[nt], pa0, pa1, pa2, pa3, b0, b1);
+        }
+    }
+    // warp states -> shared: rows g and g+8, dims VD*2c + nt and VD*(2c+1) + nt
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        float* st = sState + ((size_t)warp * 16 + gq + 8 * rr) * (HD + 2);
+        if (cq == 0) { st[0] = m_r[rr]; st[1] = l_r[rr]; }
+#pragma unroll
+        for (int nt = 0; nt < VD; ++nt) {
+            st[2 + VD * (2 * cq) + nt] = o[nt][2 * rr];
+            st[2 + VD * (2 * cq + 1) + nt] = o[nt][2 * rr + 1];
+        }
+    }
+    __syncthreads();
+    const int blk = ((b * a.n_kv_heads + g) * n_qb) + qb;
+    float* part = a.part + ((size_t)blk * a.splits + split) * kQPerCta * (HD + 2);
+    for (int i = t; i < nq * HD; i += kAttnThreads) {
+        const int r = i / HD, d = i % HD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, sState[((size_t)w * 16 + r) * (HD + 2)]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float* st = sState + ((size_t)w * 16 + r) * (HD + 2);
+                if (st[0] == -INFINITY) continue;
+                const float wt = expf(st[0] - M);
+                L += st[1] * wt;
+                O += st[2 + d] * wt;
+            }
+        }
+        part[r * (HD + 2) + 2 + d] = O;
+        if (d == 0) { part[r * (HD + 2)] = M; part[r * (HD + 2) + 1] = L; }
+    }
+    __syncthreads();
+    if (t == 0) sFlag[0] = (atomic_add_acq_rel(a.counters + blk, 1) == n_split - 1);
+    __syncthreads();
+    if (!sFlag[0]) return;
+    const float* pb = a.part + (size_t)blk * a.splits * kQPerCta * (HD + 2);
+    merge_splits<__nv_bfloat16, HD>(a, pb, n_split, nq, q0, G, g, row0, sState);
+    if (t == 0) a.counters[blk] = 0;
+}
+
+static size_t mma_smem_bytes(int hd) {
+    return sizeof(float) * (2 * (hd / 16) * 32 * 4 + 4 * 16 * (hd + 2)) + 16 + 16 * 8 + 16 * 4 + 64;
+}
+
 static int rows_blocks(int max_rows_per_seq, int G) {
     return (max_rows_per_seq * G + kQPerCta - 1) / kQPerCta;
 }
@@ -449,8 +712,53 @@ int attn_splits(const spec_model* m, int blocks, int kv_ctx) {
     return std::min(s, std::max(1, (kv_ctx + kKeyTile - 1) / kKeyTile));
 }
 
+// Launch shape of one attention call: bf16 models use the tensor-core kernel
+// (query blocks of 16), f32 models the CUDA-core kernels.
+struct AttnShape { int kind; int n_qb; int blocks; int splits; };   // kind 0 mma, 1 decode, 2 tiled
+
+static AttnShape attn_shape(const spec_model* m, int batch, int max_rows_per_seq, int kv_ctx) {
+    const spec_model_config& c = m->cfg;
+    const int G = c.n_heads / c.n_kv_heads;
+    const int nq_max = max_rows_per_seq * G;
+    AttnShape s{};
+    if (m->bf16) {
+        // one wave: as many key splits as resident CTAs allow
+        static int occ[2] = {0, 0};
+        const int hi = c.head_dim == 128;
+        if (!occ[hi]) {
+            int n = 0;
+            if (hi) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_mma_kernel<128>, kAttnThreads,
+                                                                  mma_smem_bytes(128));
+            else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attention_mma_kernel<64>, kAttnThreads,
+                                                               mma_smem_bytes(64));
+            occ[hi] = std::max(1, n);
+        }
+        s.kind = 0;
+        s.n_qb = (nq_max + 15) / 16;
+        s.blocks = batch * c.n_kv_heads * s.n_qb;
+        s.splits = std::max(1, std::min(64, (occ[hi] * m->num_sms) / s.blocks));
+        s.splits = std::min(s.splits, std::max(1, (kv_ctx + 63) / 64));
+    } else if (nq_max <= 8) {
+        s.kind = 1;
+        s.n_qb = 1;
+        s.blocks = batch * c.n_kv_heads;
+        s.splits = decode_splits(m, s.blocks, kv_ctx);
+    } else {
+        s.kind = 2;
+        s.n_qb = rows_blocks(max_rows_per_seq, G);
+        s.blocks = batch * c.n_kv_heads * s.n_qb;
+        s.splits = attn_splits(m, s.blocks, kv_ctx);
+    }
+    return s;
+}
+
 size_t attn_scratch_floats(const spec_model* m, int batch, int max_rows_per_seq, int kv_ctx, int* n_counters) {
     const spec_model_config& c = m->cfg;
+    if (m->bf16) {
+        const AttnShape sh = attn_shape(m, batch, max_rows_per_seq, kv_ctx);
+        *n_counters = sh.blocks;
+        return (size_t)sh.blocks * sh.splits * kQPerCta * (c.head_dim + 2);
+    }
     if (max_rows_per_seq * (c.n_heads / c.n_kv_heads) <= 8) {
         const int blocks = batch * c.n_kv_heads;
         *n_counters = blocks;
@@ -474,6 +782,27 @@ int launch_attention(spec_model* m, const AttnParams& a0, int max_rows_per_seq, 
     AttnParams a = a0;
     const int G = a.n_heads / a.n_kv_heads;
     const int nq_max = max_rows_per_seq * G;
+    if (m->bf16) {
+        const AttnShape sh = attn_shape(m, a.batch, max_rows_per_seq, a.kv_ctx);
+        a.splits = sh.splits;
+        if ((size_t)sh.blocks * a.splits * kQPerCta * (a.head_dim + 2) > m->attn_part_floats ||
+            sh.blocks > m->n_attn_counters)
+            return set_error(SPEC_ERR_CAPACITY, "attention workspace too small");
+        a.part = m->attn_part;
+        a.counters = m->attn_counters;
+        dim3 grid(a.splits * sh.n_qb, a.n_kv_heads, a.batch);
+        const size_t smem = mma_smem_bytes(a.head_dim);
+        const int slot = prof_start(m, st);
+        cudaError_t e;
+        if (a.head_dim == 128)
+            e = launch_k(m->pdl, attention_mma_kernel<128>, grid, dim3(kAttnThreads), smem, st, a, sh.n_qb);
+        else
+            e = launch_k(m->pdl, attention_mma_kernel<64>, grid, dim3(kAttnThreads), smem, st, a, sh.n_qb);
+        ++m->launches;
+        prof_stop(m, slot, st, PROF_ATTN, 0.0);
+        if (e != cudaSuccess) return check_cuda(e, "attention launch");
+        return check_cuda(cudaGetLastError(), "attention launch");
+    }
     if (nq_max <= 8) {
         // every query vector of a (sequence, kv head) in one register-resident block
         const int blocks = a.batch * a.n_kv_heads;
