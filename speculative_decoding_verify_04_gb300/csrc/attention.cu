@@ -439,7 +439,7 @@ static void launch_decode_rb(bool pdl, const AttnParams& a, int nq, dim3 grid, c
 // A CTA handles 16 query vectors of one (sequence, kv head) -- the M side of
 // the MMAs -- over one key range; its 4 warps take 16-key tiles in turn.
 // Per tile:  S[16 q x 16 keys] = Q K^T  (Q split into bf16 hi + lo, two MMAs
-// per k-step),  online softmax on S,  O += P V.
+// per k-step),  online softmax on S,  O += P V  (P split the same way).
 // The order of the head dimensions inside a k-step and of the keys inside a
 // tile is free (both sides of each product use the same order), so it is
 // chosen to make every global load a contiguous 16-byte piece of a K or V row
@@ -627,9 +627,11 @@ attention_mma_kernel(AttnParams a, int n_qb) {
             l_r[rr] = l_r[rr] * alpha[rr] + ps;
             m_r[rr] = mn;
         }
-        // P (A fragment of P V): keys 4c..4c+1 from half 0, 4c+2..4c+3 from half 1
+        // P (A fragment of P V, bf16 hi + lo): keys 4c..4c+1 from half 0, 4c+2..4c+3 from half 1
         const uint32_t pa0 = pack_bf16(sc[0][0], sc[0][1]), pa1 = pack_bf16(sc[0][2], sc[0][3]);
         const uint32_t pa2 = pack_bf16(sc[1][0], sc[1][1]), pa3 = pack_bf16(sc[1][2], sc[1][3]);
+        const uint32_t pl0 = pack_bf16_lo(sc[0][0], sc[0][1]), pl1 = pack_bf16_lo(sc[0][2], sc[0][3]);
+        const uint32_t pl2 = pack_bf16_lo(sc[1][0], sc[1][1]), pl3 = pack_bf16_lo(sc[1][2], sc[1][3]);
         // keys past the range contribute p = 0; clear their V rows so stale values cannot reach O
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -648,6 +650,7 @@ attention_mma_kernel(AttnParams a, int n_qb) {
             o[nt][2] *= alpha[1];
             o[nt][3] *= alpha[1];
             mma16816(o[nt], pa0, pa1, pa2, pa3, b0, b1);
+            mma16816(o[nt], pl0, pl1, pl2, pl3, b0, b1);
         }
     }
     // warp states -> shared: rows g and g+8, dims VD*2c + nt and VD*(2c+1) + nt
