@@ -38,7 +38,7 @@ K_DRAFT, CTX, SEED = 4, 4096, 4
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -47,6 +47,18 @@ def parse():
                     help="fewer layers of the same shape (small case for profiler captures)")
     ap.add_argument("--exit-layer", type=int, default=None)
     return ap.parse_args()
+
+
+def gemm_traffic_per_launch():
+    """DRAM bytes of the average GEMM launch of a round, from the committed ncu
+    summary (profiles/gemm_tc_kernel.llama7b_shapes.md); None if absent."""
+    p = os.path.join(ROOT, "profiles", "gemm_tc_kernel.llama7b_shapes.md")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        if line.startswith("traffic_bytes_per_avg_launch:"):
+            return float(line.split(":")[1])
+    return None
 
 
 def peaks():
@@ -152,7 +164,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={','.join(self.FIELDS)}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -342,7 +354,10 @@ def main():
                      "kernel": "gemm_tc_kernel (tcgen05 skinny GEMM; every launch of an instrumented pass of the "
                                "same rounds)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": (achieved / hbm) if achieved else None, "traffic": None,
+                     "frac": (achieved / hbm) if achieved else None,
+                     "traffic": gemm_traffic_per_launch() if args.layers is None and B == 1 else None,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
+                                       "profiles/gemm_tc_kernel.llama7b_shapes.md",
                      "peak_source": peak_kind, "launches": g_n, "avg_launch_us": g_avg_ms * 1e3,
                      "avg_launch_bytes": g_avg_bytes},
         "attention": {"launches": a_n, "total_ms_per_step": a_ms / steps},
