@@ -63,15 +63,37 @@ __device__ void merge_splits(const AttnParams& a, const float* pb, int n_split, 
     }
     __syncthreads();
     const int qdim = a.n_heads * HD;
-    for (int i = t; i < nq * HD; i += kAttnThreads) {
-        const int qi = i / HD, d = i % HD;
-        float O = 0.f;
-#pragma unroll 8
-        for (int s2 = 0; s2 < n_split; ++s2)
-            O += sw[s2 * kQPerCta + qi] * __ldcg(pb + ((size_t)s2 * kQPerCta + qi) * (HD + 2) + 2 + d);
+    // four consecutive dims per thread; the splits' loads go out in batches of 16
+    for (int i = t; i < nq * (HD / 4); i += kAttnThreads) {
+        const int qi = i / (HD / 4), d = 4 * (i % (HD / 4));
+        float O[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s0 = 0; s0 < n_split; s0 += 16) {
+            float v[16][4];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int s2 = s0 + u;
+                if (s2 < n_split) {
+                    const float* src = pb + ((size_t)s2 * kQPerCta + qi) * (HD + 2) + 2 + d;
+                    // rows of HD + 2 floats: 8-byte aligned, so two 8-byte loads
+                    const float2 x0 = __ldcg(reinterpret_cast<const float2*>(src));
+                    const float2 x1 = __ldcg(reinterpret_cast<const float2*>(src + 2));
+                    v[u][0] = x0.x; v[u][1] = x0.y; v[u][2] = x1.x; v[u][3] = x1.y;
+                } else {
+                    v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float w = (s0 + u < n_split) ? sw[(s0 + u) * kQPerCta + qi] : 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) O[e] += w * v[u][e];
+            }
+        }
         const int qg = q0 + qi;
         const int j = qg / G, h = g * G + qg % G;
-        store_act(static_cast<KT*>(a.out), (size_t)(row0 + j) * qdim + h * HD + d, a.out_lo, O);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            store_act(static_cast<KT*>(a.out), (size_t)(row0 + j) * qdim + h * HD + d + e, a.out_lo, O[e]);
     }
 }
 
