@@ -20,6 +20,7 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--impl referenc
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -51,14 +52,22 @@ def parse():
 
 def gemm_traffic_per_launch():
     """DRAM bytes of the average GEMM launch of a round, from the committed ncu
-    summary (profiles/gemm_tc_kernel.llama7b_shapes.md); None if absent."""
+    summary (profiles/gemm_tc_kernel.llama7b_shapes.md).  None if the summary is
+    absent or was taken on another version of the kernel source (its
+    gemm_cu_sha256 line differs from the current gemm.cu)."""
     p = os.path.join(ROOT, "profiles", "gemm_tc_kernel.llama7b_shapes.md")
+    src = os.path.join(ROOT, "speculative_decoding_verify_04_gb300", "csrc", "gemm.cu")
     if not os.path.exists(p):
         return None
+    fields = {}
     for line in open(p):
-        if line.startswith("traffic_bytes_per_avg_launch:"):
-            return float(line.split(":")[1])
-    return None
+        if ":" in line and line.split(":")[0] in ("traffic_bytes_per_avg_launch", "gemm_cu_sha256"):
+            k, v = line.split(":", 1)
+            fields[k] = v.strip()
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if fields.get("gemm_cu_sha256") != sha or "traffic_bytes_per_avg_launch" not in fields:
+        return None
+    return float(fields["traffic_bytes_per_avg_launch"])
 
 
 def peaks():

@@ -56,11 +56,6 @@ void prof_stop(spec_model* m, int slot, cudaStream_t st, int kind, double bytes)
     m->prof_bytes[slot] = bytes;
 }
 
-#define SPEC_TRY(x)                          \
-    do {                                     \
-        int rc_ = (x);                       \
-        if (rc_ != SPEC_OK) return rc_;      \
-    } while (0)
 #define SPEC_CUDA(x, what) SPEC_TRY(check_cuda((x), what))
 
 // ---------------------------------------------------------------------------
@@ -255,20 +250,51 @@ static EpiParams base_epi(spec_model* m, spec_kv* kv, int T) {
     return e;
 }
 
+static GemmStep head_step(spec_model* m, spec_kv* kv, const HeadSpec& hs) {
+    const spec_model_config& c = m->cfg;
+    EpiParams e = base_epi(m, kv, hs.T);
+    e.kind = EPI_HEAD;
+    e.r0 = hs.r0;
+    e.N = c.vocab;
+    e.logits = hs.logits;
+    e.logits_stride = hs.logits_stride;
+    e.logits_row0 = hs.logits_row0;
+    e.user_stats = hs.user_stats;
+    e.head_mode = hs.mode;
+    e.cand = hs.cand;
+    e.cand_stride = hs.cand_stride;
+    e.cand_col = hs.cand_col;
+    e.tokens = hs.tokens;
+    e.tok_stride = hs.tok_stride;
+    e.acc_len = hs.acc_len;
+    e.next_tok = hs.next_tok;
+    e.path = hs.path;
+    e.batch = hs.batch;
+    return GemmStep{GemmLaunch{&m->tm_head, nullptr, m->head, m->x_in, c.d_model, c.vocab, c.d_model}, e, 0};
+}
+
+// Layers [lo, hi) on the T rows of the current plan, then (head != nullptr) the
+// LM head.  GEMMs between two attentions go out as one chain:
+//   [QKV lo]  attn  [O, gate|up, down, QKV lo+1]  attn  ...  [O, gate|up, down, head]
+// head_follows picks the gain of the last down projection's next-input
+// (the final norm when the LM head reads it).
 static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows_per_seq, int lo, int hi,
-                      int tree, bool head_follows, cudaStream_t st) {
+                      int tree, bool head_follows, const HeadSpec* head, cudaStream_t st) {
     const spec_model_config& c = m->cfg;
     const int qdim = c.n_heads * c.head_dim;
+    GemmStep pend[4];
+    int np = 0;
     for (int l = lo; l < hi; ++l) {
         LayerWeights& L = m->layers[l];
         EpiParams e = base_epi(m, kv, T);
         e.layer = l;
-        {   // Q|K|V
+        {   // Q|K|V (closes the chain of the previous layer's MLP)
             EpiParams q = e;
             q.kind = EPI_QKV;
             q.N = m->qkv_n;
-            GemmLaunch g{&L.tm_qkv, nullptr, L.qkv, m->x_in, c.d_model, m->qkv_n, c.d_model};
-            SPEC_TRY(launch_gemm(m, g, q, 0, st));
+            pend[np++] = GemmStep{GemmLaunch{&L.tm_qkv, nullptr, L.qkv, m->x_in, c.d_model, m->qkv_n, c.d_model}, q, 0};
+            SPEC_TRY(launch_gemm_chain(m, pend, np, st));
+            np = 0;
         }
         {   // attention
             AttnParams a{};
@@ -295,15 +321,13 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             o.N = c.d_model;
             o.gain_next = L.ffn_g;
             o.x_next = m->x_in;
-            GemmLaunch g{&L.tm_o, nullptr, L.o, m->x_attn, qdim, c.d_model, qdim};
-            SPEC_TRY(launch_gemm(m, g, o, 1, st));
+            pend[np++] = GemmStep{GemmLaunch{&L.tm_o, nullptr, L.o, m->x_attn, qdim, c.d_model, qdim}, o, 1};
         }
         {   // gate | up -> SwiGLU
-            EpiParams s = e;
-            s.kind = EPI_SWIGLU;
-            s.N = m->gu_n;
-            GemmLaunch g{&L.tm_gu, nullptr, L.gu, m->x_in, c.d_model, m->gu_n, c.d_model};
-            SPEC_TRY(launch_gemm(m, g, s, 0, st));
+            EpiParams sg = e;
+            sg.kind = EPI_SWIGLU;
+            sg.N = m->gu_n;
+            pend[np++] = GemmStep{GemmLaunch{&L.tm_gu, nullptr, L.gu, m->x_in, c.d_model, m->gu_n, c.d_model}, sg, 0};
         }
         {   // down projection + residual
             EpiParams dn = e;
@@ -312,35 +336,19 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             dn.gain_next = (l + 1 < hi || !head_follows) ? (l + 1 < c.n_layers ? m->layers[l + 1].attn_g : m->final_g)
                                                          : m->final_g;
             dn.x_next = m->x_in;
-            GemmLaunch g{&L.tm_down, nullptr, L.down, m->x_act, c.d_ff, c.d_model, c.d_ff};
-            SPEC_TRY(launch_gemm(m, g, dn, 2, st));
+            pend[np++] = GemmStep{GemmLaunch{&L.tm_down, nullptr, L.down, m->x_act, c.d_ff, c.d_model, c.d_ff}, dn, 2};
         }
     }
+    if (head && np > 0 && head->T == T && head->r0 == 0) {
+        pend[np++] = head_step(m, kv, *head);
+        return launch_gemm_chain(m, pend, np, st);
+    }
+    SPEC_TRY(launch_gemm_chain(m, pend, np, st));
+    if (head) {
+        const GemmStep h = head_step(m, kv, *head);
+        return launch_gemm(m, h.g, h.e, h.xbuf, st);
+    }
     return SPEC_OK;
-}
-
-static int run_head(spec_model* m, spec_kv* kv, const HeadSpec& hs, cudaStream_t st) {
-    const spec_model_config& c = m->cfg;
-    EpiParams e = base_epi(m, kv, hs.T);
-    e.kind = EPI_HEAD;
-    e.r0 = hs.r0;
-    e.N = c.vocab;
-    e.logits = hs.logits;
-    e.logits_stride = hs.logits_stride;
-    e.logits_row0 = hs.logits_row0;
-    e.user_stats = hs.user_stats;
-    e.head_mode = hs.mode;
-    e.cand = hs.cand;
-    e.cand_stride = hs.cand_stride;
-    e.cand_col = hs.cand_col;
-    e.tokens = hs.tokens;
-    e.tok_stride = hs.tok_stride;
-    e.acc_len = hs.acc_len;
-    e.next_tok = hs.next_tok;
-    e.path = hs.path;
-    e.batch = hs.batch;
-    GemmLaunch g{&m->tm_head, nullptr, m->head, m->x_in, c.d_model, c.vocab, c.d_model};
-    return launch_gemm(m, g, e, 0, st);
 }
 
 static int launch_plan(spec_model* m, const PlanParams& p, int T, const int* len, cudaStream_t st) {
@@ -435,6 +443,9 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
     {   // SPEC_PDL=0 turns programmatic dependent launch off (kernels then run back to back)
         const char* e = getenv("SPEC_PDL");
         m->pdl = !(e && e[0] == '0');
+        // SPEC_CHAIN=0 launches every GEMM on its own
+        const char* ce = getenv("SPEC_CHAIN");
+        m->chain = !(ce && ce[0] == '0');
     }
     m->elem = m->bf16 ? 2 : 4;
     if (m->bf16) {
@@ -526,7 +537,7 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
         max_tiles = std::max(max_tiles, (s[0] + kTileN - 1) / kTileN);
     }
     m->gemm_part_floats = part;
-    m->n_counters = max_tiles + 1;
+    m->n_counters = max_tiles + 3;
     const int rows_per_seq = std::min(kMaxSeqRows, R);
     m->attn_part_floats = attn_partial_floats_needed(m, c.max_batch, rows_per_seq);
     const int G = c.n_heads / c.n_kv_heads;
@@ -708,21 +719,18 @@ extern "C" int spec_prefill(spec_model* m, spec_kv* kv, int32_t seq, const int32
         SPEC_TRY(launch_prologue(m, T, nullptr, 0, tokens + done, 0, 0, 0, st));
         const bool last = done + T >= n;
         const bool head = last && (last_logits || next_tok);
-        SPEC_TRY(run_layers(m, kv, T, seq + 1, T, 0, c.n_layers, 0, head, st));
-        if (head) {
-            HeadSpec hs{};
-            hs.mode = next_tok ? HEAD_DRAFT : HEAD_STATS;
-            hs.T = 1;
-            hs.r0 = T - 1;
-            hs.logits = last_logits;
-            hs.logits_stride = c.vocab;
-            hs.logits_row0 = T - 1;
-            hs.cand = next_tok;
-            hs.cand_stride = 0;
-            hs.cand_col = 0;
-            hs.batch = seq + 1;
-            SPEC_TRY(run_head(m, kv, hs, st));
-        }
+        HeadSpec hs{};
+        hs.mode = next_tok ? HEAD_DRAFT : HEAD_STATS;
+        hs.T = 1;
+        hs.r0 = T - 1;
+        hs.logits = last_logits;
+        hs.logits_stride = c.vocab;
+        hs.logits_row0 = T - 1;
+        hs.cand = next_tok;
+        hs.cand_stride = 0;
+        hs.cand_col = 0;
+        hs.batch = seq + 1;
+        SPEC_TRY(run_layers(m, kv, T, seq + 1, T, 0, c.n_layers, 0, head, head ? &hs : nullptr, st));
         launch_k(m->pdl, add_len_kernel, dim3(1), dim3(32), 0, st, kv->len, seq, T, kv->max_ctx, m->err);
         ++m->launches;
         SPEC_CUDA(cudaGetLastError(), "length update");
@@ -749,24 +757,22 @@ extern "C" int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32
         p.pass = j;
         SPEC_TRY(launch_plan(m, p, batch, kv->len, st));
         SPEC_TRY(launch_prologue(m, batch, nullptr, 0, cand, k + 1, j, 0, st));
-        SPEC_TRY(run_layers(m, kv, batch, batch, 1, 0, c.exit_layer, 0, j < k, st));
+        HeadSpec hs{};
+        hs.mode = HEAD_DRAFT;
+        hs.T = batch;
+        hs.r0 = 0;
+        hs.logits = draft_logits ? draft_logits + (size_t)j * c.vocab : nullptr;
+        hs.logits_stride = k * c.vocab;
+        hs.logits_row0 = 0;
+        hs.cand = cand;
+        hs.cand_stride = k + 1;
+        hs.cand_col = j + 1;
+        hs.batch = batch;
+        // the LM head leaves the residual stream alone, so the layer-L state is copied after it
+        SPEC_TRY(run_layers(m, kv, batch, batch, 1, 0, c.exit_layer, 0, j < k, j < k ? &hs : nullptr, st));
         launch_k(m->pdl, copy_rows_kernel, dim3(batch), dim3(256), 0, st, (const float*)m->h, h_L, batch, c.d_model, k + 1, j);
         ++m->launches;
         SPEC_CUDA(cudaGetLastError(), "draft state copy");
-        if (j < k) {
-            HeadSpec hs{};
-            hs.mode = HEAD_DRAFT;
-            hs.T = batch;
-            hs.r0 = 0;
-            hs.logits = draft_logits ? draft_logits + (size_t)j * c.vocab : nullptr;
-            hs.logits_stride = k * c.vocab;
-            hs.logits_row0 = 0;
-            hs.cand = cand;
-            hs.cand_stride = k + 1;
-            hs.cand_col = j + 1;
-            hs.batch = batch;
-            SPEC_TRY(run_head(m, kv, hs, st));
-        }
     }
     return SPEC_OK;
 }
@@ -812,7 +818,6 @@ extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int3
     const int lo = h_in ? c.exit_layer : 0;
     SPEC_TRY(launch_plan(m, p, T, kv->len, st));
     SPEC_TRY(launch_prologue(m, T, h_in, h_stride, tokens, tok_stride, 0, lo, st));
-    SPEC_TRY(run_layers(m, kv, T, batch, max_r, lo, c.n_layers, tree_parent ? 1 : 0, true, st));
     HeadSpec hs{};
     hs.mode = acc_len ? (tree_parent ? HEAD_ACCEPT_TREE : HEAD_ACCEPT_CHAIN) : HEAD_STATS;
     hs.T = T;
@@ -827,7 +832,7 @@ extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int3
     hs.next_tok = next_tok;
     hs.path = path;
     hs.batch = batch;
-    return run_head(m, kv, hs, st);
+    return run_layers(m, kv, T, batch, max_r, lo, c.n_layers, tree_parent ? 1 : 0, true, &hs, st);
 }
 
 extern "C" int spec_profile(spec_model* m, int32_t enable) {

@@ -83,6 +83,16 @@ __host__ __device__ inline long long unit_begin(const Split& s, int c) { return 
 __host__ __device__ inline int cta_of(const Split& s, long long u) {
     return (int)(((u + 1) * s.G - 1) / s.units);
 }
+// units of CTA c; a chain launches as many CTAs as its widest phase, so a
+// narrower phase leaves the CTAs past its own count without work
+__host__ __device__ inline void cta_units(const Split& s, int c, long long& ub, long long& ue) {
+    if (c < s.G) {
+        ub = unit_begin(s, c);
+        ue = unit_begin(s, c + 1);
+    } else {
+        ub = ue = 0;
+    }
+}
 
 // ---------------------------------------------------------------------------
 // epilogue shared memory
@@ -103,7 +113,7 @@ SPEC_DEV void load_row_scales(const EpiParams& e, EpiSmem& sm) {
         const int w = etid() >> 5, lane = etid() & 31;
         for (int j = w; j < e.T; j += 4) {
             float s = 0.f;
-            for (int i = lane; i < e.ss_tiles; i += 32) s += e.ss_in[(size_t)i * e.ss_stride + e.r0 + j];
+            for (int i = lane; i < e.ss_tiles; i += 32) s += __ldcg(e.ss_in + (size_t)i * e.ss_stride + e.r0 + j);
             s = warp_sum(s);
             if (lane == 0) sm.rs_all[j] = 1.0f / sqrtf(s * e.inv_d + e.eps);
         }
@@ -159,7 +169,7 @@ SPEC_DEV void apply_resid(const EpiParams& e, int tile, int j0, int nr, EpiSmem&
         if (n < e.N) {
             const int r = e.r0 + j0 + j;
             const size_t o = (size_t)r * e.d_model + n;
-            const float hn = e.h[o] + sm.tile[j][mm];
+            const float hn = __ldcg(e.h + o) + sm.tile[j][mm];
             e.h[o] = hn;
             store_act(static_cast<XT*>(e.x_next), o, e.x_next_lo, hn * e.gain_next[n]);
             sq = hn * hn;
@@ -230,6 +240,17 @@ SPEC_DEV void apply_chunk(const EpiParams& e, int tile, int j0, int nr, EpiSmem&
     named_bar(1, 128);
 }
 
+// Data written by other CTAs of the same launch is read past L1 (L2 is coherent).
+SPEC_DEV spec_row_stats ldcg_stats(const spec_row_stats* p) {
+    const float4 f = __ldcg(reinterpret_cast<const float4*>(p));
+    spec_row_stats s;
+    s.top1 = f.x;
+    s.top2 = f.y;
+    s.sum_exp = f.z;
+    s.argmax = __float_as_int(f.w);
+    return s;
+}
+
 // Last tile of an LM-head launch: merge the per-tile summaries of every row of
 // the launch (warp per row, fixed order), then the draft pick or acceptance.
 SPEC_DEV void head_finalize(const EpiParams& e, int n_tiles) {
@@ -242,7 +263,7 @@ SPEC_DEV void head_finalize(const EpiParams& e, int n_tiles) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int t = t0 + 32 * i;
-                v[i] = t < n_tiles ? e.stat_part[(size_t)t * e.ss_stride + r] : stat_empty();
+                v[i] = t < n_tiles ? ldcg_stats(e.stat_part + (size_t)t * e.ss_stride + r) : stat_empty();
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) stat_merge(s, v[i]);
@@ -370,9 +391,57 @@ struct TmemLoader {
     }
 };
 
+// One launch runs a chain of up to kMaxPhases GEMMs (for example O projection ->
+// gate/up -> down -> next QKV) separated by grid barriers.  The TMA producer
+// streams the next phase's weight tiles into the ring while the previous phase
+// finishes; only the activation tiles wait for the barrier.  One phase is a
+// plain GEMM launch.
+constexpr int kMaxPhases = 4;
+constexpr int kMaxStages = 8;
+
+struct GemmPhase {
+    CUtensorMap tmW;
+    CUtensorMap tmX;
+    Split sp;
+    EpiParams e;
+};
+
+struct GemmChain {
+    GemmPhase ph[kMaxPhases];
+    int n;
+    int* bar;      // per launch: CTAs that finished a phase, summed over phases
+    int* done;     // CTAs that finished the chain; the last one resets both counters
+};
+
+SPEC_DEV int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+SPEC_DEV void red_release_gpu_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+// orders this thread's generic-proxy global accesses with later async-proxy (TMA) ones
+SPEC_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// bounded wait until every CTA has finished `phases` phases
+SPEC_DEV bool grid_wait(const int* bar, int target, volatile int* abort_flag, int* err) {
+    if (ld_acquire_gpu(bar) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ld_acquire_gpu(bar) >= target) return true;
+        if ((it & 63u) == 0u) {
+            if (abort_flag && *abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                if (abort_flag) *abort_flag = 1;
+                dev_error(err, SPEC_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-               Split sp, TcLayout L, EpiParams e) {
+gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = base;
@@ -388,8 +457,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     EpiSmem& sm = *reinterpret_cast<EpiSmem*>(reinterpret_cast<uint8_t*>(bars) + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.x;
-    const long long u_begin = unit_begin(sp, c), u_end = unit_begin(sp, c + 1);
+    const int c = blockIdx.x, G = gridDim.x;
+    int* err = ch.ph[0].e.err;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < L.stages; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
@@ -411,103 +480,162 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
 
     if (warp == 4) {
         if (lane == 0) {
-            tma_prefetch_desc(&tmW);
-            tma_prefetch_desc(&tmX);
+            for (int p = 0; p < ch.n; ++p) {
+                tma_prefetch_desc(&ch.ph[p].tmW);
+                tma_prefetch_desc(&ch.ph[p].tmX);
+            }
             const uint64_t pw = l2_policy_evict_first(), px = l2_policy_evict_last();
-            // The first ring of weight tiles does not depend on the previous kernel:
-            // issue it before waiting for that kernel, then the activation tiles.
-            const long long npre = min((long long)L.stages, u_end - u_begin);
-            for (long long i = 0; i < npre; ++i) {
-                const long long u = u_begin + i;
-                const int tile = (int)(u / sp.kb), kb = (int)(u % sp.kb);
-                mbar_arrive_expect_tx(full + i, kATileBytes + L.b_bytes);
-                tma_load_2d(sA + (size_t)i * kATileBytes, &tmW, kb * kTileK, tile * kTileN, full + i, pw);
-            }
-            pdl_wait();
-            for (long long i = 0; i < npre; ++i) {
-                const int kb = (int)((u_begin + i) % sp.kb);
-                tma_load_2d(sB + (size_t)i * L.b_bytes, &tmX, kb * kTileK, e.r0, full + i, px);
-                tma_load_2d(sB + (size_t)i * L.b_bytes + L.b_bytes / 2, &tmX, kb * kTileK, L.rows_pad + e.r0,
-                            full + i, px);
-            }
-            int stage = (int)(npre % L.stages);
-            uint32_t phase = (npre == L.stages) ? 1u : 0u;
-            long long issued = npre;
-            for (long long u = u_begin + npre; u < u_end; ++u) {
-                const int tile = (int)(u / sp.kb), kb = (int)(u % sp.kb);
-                if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, e.err)) break;
-                mbar_arrive_expect_tx(full + stage, kATileBytes + L.b_bytes);
-                tma_load_2d(sA + (size_t)stage * kATileBytes, &tmW, kb * kTileK, tile * kTileN, full + stage, pw);
-                // hi rows, then lo rows (the lo half of the buffer starts at row rows_pad)
-                tma_load_2d(sB + (size_t)stage * L.b_bytes, &tmX, kb * kTileK, e.r0, full + stage, px);
-                tma_load_2d(sB + (size_t)stage * L.b_bytes + L.b_bytes / 2, &tmX, kb * kTileK, L.rows_pad + e.r0,
-                            full + stage, px);
-                ++issued;
-                if (++stage == L.stages) { stage = 0; phase ^= 1u; }
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            int def_stage[kMaxStages];
+            int def_kb[kMaxStages];
+            int n_def = 0;
+            bool ok = true;
+            const GemmPhase* P = &ch.ph[0];
+            auto load_x = [&](const GemmPhase& Q, int st, int kbi) {
+                tma_load_2d(sB + (size_t)st * L.b_bytes, &Q.tmX, kbi * kTileK, Q.e.r0, full + st, px);
+                tma_load_2d(sB + (size_t)st * L.b_bytes + L.b_bytes / 2, &Q.tmX, kbi * kTileK,
+                            L.rows_pad + Q.e.r0, full + st, px);
+            };
+            // activation tiles of a phase wait for the previous phase (the previous
+            // kernel for phase 0); its weight tiles do not
+            auto dep_wait = [&](int p) -> bool {
+                if (p == 0) { pdl_wait(); return true; }
+                if (!grid_wait(ch.bar, G * p, abort_flag, err)) return false;
+                fence_proxy_async_global();     // the rows were written by other CTAs' epilogues
+                return true;
+            };
+            for (int p = 0; ok && p < ch.n; ++p) {
+                P = &ch.ph[p];
+                const Split& sp = P->sp;
+                long long ub, ue;
+                cta_units(sp, c, ub, ue);
+                bool dep = false;
+                n_def = 0;
+                for (long long u = ub; u < ue; ++u) {
+                    if (!dep && n_def == L.stages) {
+                        if (!dep_wait(p)) { ok = false; break; }
+                        dep = true;
+                        for (int i = 0; i < n_def; ++i) load_x(*P, def_stage[i], def_kb[i]);
+                        n_def = 0;
+                    }
+                    if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, err)) { ok = false; break; }
+                    const int tile = (int)(u / sp.kb), kbi = (int)(u % sp.kb);
+                    mbar_arrive_expect_tx(full + stage, kATileBytes + L.b_bytes);
+                    tma_load_2d(sA + (size_t)stage * kATileBytes, &P->tmW, kbi * kTileK, tile * kTileN, full + stage,
+                                pw);
+                    if (dep) {
+                        load_x(*P, stage, kbi);
+                    } else {
+                        def_stage[n_def] = stage;
+                        def_kb[n_def] = kbi;
+                        ++n_def;
+                    }
+                    ++issued;
+                    if (++stage == L.stages) { stage = 0; phase ^= 1u; }
+                }
+                if (ok && !dep) {
+                    if (!dep_wait(p)) { ok = false; }
+                    else {
+                        for (int i = 0; i < n_def; ++i) load_x(*P, def_stage[i], def_kb[i]);
+                        n_def = 0;
+                    }
+                }
             }
             if (*abort_flag) {
-                // let copies still in flight land before the CTA exits
+                // complete the deferred stages (their barriers expect the activation bytes), then
+                // let every copy still in flight land before the CTA exits
+                for (int i = 0; i < n_def; ++i) load_x(*P, def_stage[i], def_kb[i]);
                 const long long n = issued < L.stages ? issued : L.stages;
                 for (long long i = 0; i < n; ++i) {
                     if (--stage < 0) { stage = L.stages - 1; phase ^= 1u; }
-                    mbar_wait(full + stage, phase, nullptr, e.err);
+                    mbar_wait(full + stage, phase, nullptr, err);
                 }
             }
         }
     } else if (warp == 5) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(128, sp.T_pad);
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (long long u = u_begin; ok && u < u_end;) {
-                const int tile = (int)(u / sp.kb);
-                const long long seg_end = min(u_end, (long long)(tile + 1) * sp.kb);
-                if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, e.err)) break;
-                acc_phase ^= 1u;
-                tc_fence_after();
-                const long long seg_begin = u;
-                for (; u < seg_end; ++u) {
-                    if (!mbar_wait(full + stage, phase, abort_flag, e.err)) { ok = false; break; }
+            for (int p = 0; ok && p < ch.n; ++p) {
+                const Split& sp = ch.ph[p].sp;
+                const uint32_t idesc = idesc_bf16_f32(128, sp.T_pad);
+                long long ub, ue;
+                cta_units(sp, c, ub, ue);
+                for (long long u = ub; ok && u < ue;) {
+                    const int tile = (int)(u / sp.kb);
+                    const long long seg_end = min(ue, (long long)(tile + 1) * sp.kb);
+                    if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, err)) { ok = false; break; }
+                    acc_phase ^= 1u;
                     tc_fence_after();
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sA + (size_t)stage * kATileBytes));
-                    const uint64_t bh = smem_desc_sw128(smem_u32(sB + (size_t)stage * L.b_bytes));
-                    const uint64_t bl = smem_desc_sw128(smem_u32(sB + (size_t)stage * L.b_bytes + L.b_bytes / 2));
+                    const long long seg_begin = u;
+                    for (; u < seg_end; ++u) {
+                        if (!mbar_wait(full + stage, phase, abort_flag, err)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t ad = smem_desc_sw128(smem_u32(sA + (size_t)stage * kATileBytes));
+                        const uint64_t bh = smem_desc_sw128(smem_u32(sB + (size_t)stage * L.b_bytes));
+                        const uint64_t bl = smem_desc_sw128(smem_u32(sB + (size_t)stage * L.b_bytes + L.b_bytes / 2));
 #pragma unroll
-                    for (int k = 0; k < kTileK / 16; ++k) {
-                        tc_mma_f16(tmem, ad + 2u * k, bh + 2u * k, idesc, (u > seg_begin || k > 0) ? 1u : 0u);
-                        tc_mma_f16(tmem, ad + 2u * k, bl + 2u * k, idesc, 1u);
+                        for (int k = 0; k < kTileK / 16; ++k) {
+                            tc_mma_f16(tmem, ad + 2u * k, bh + 2u * k, idesc, (u > seg_begin || k > 0) ? 1u : 0u);
+                            tc_mma_f16(tmem, ad + 2u * k, bl + 2u * k, idesc, 1u);
+                        }
+                        tc_commit(empty + stage);
+                        if (++stage == L.stages) { stage = 0; phase ^= 1u; }
                     }
-                    tc_commit(empty + stage);
-                    if (++stage == L.stages) { stage = 0; phase ^= 1u; }
+                    if (ok) tc_commit(acc_full);
                 }
-                if (ok) tc_commit(acc_full);
             }
             tc_commit(drain);
-            mbar_wait(drain, 0, nullptr, e.err);
+            mbar_wait(drain, 0, nullptr, err);
         }
     } else {
         TmemLoader ld;
         ld.taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         ld.acc_empty = acc_empty;
         uint32_t acc_phase = 0;
+        bool ok = true;
         pdl_wait();
-        load_row_scales(e, sm);
-        for (long long u = u_begin; u < u_end;) {
-            const int tile = (int)(u / sp.kb);
-            const long long seg_end = min(u_end, (long long)(tile + 1) * sp.kb);
-            const int first = cta_of(sp, (long long)tile * sp.kb);
-            const int last = cta_of(sp, (long long)(tile + 1) * sp.kb - 1);
-            // one thread waits (bounded) and broadcasts, so all 128 leave together
-            if (etid() == 0) sm.wait_ok = mbar_wait(acc_full, acc_phase, abort_flag, e.err) ? 1 : 0;
-            named_bar(1, 128);
-            const int ok = sm.wait_ok;
-            named_bar(1, 128);
-            if (!ok) break;
-            acc_phase ^= 1u;
-            tc_fence_after();
-            finish_segment<__nv_bfloat16>(e, sp, tile, c - first, last - first + 1, sm, ld);
-            u = seg_end;
+        for (int p = 0; ok && p < ch.n; ++p) {
+            const GemmPhase& P = ch.ph[p];
+            const Split& sp = P.sp;
+            if (p > 0) {
+                if (etid() == 0) sm.wait_ok = grid_wait(ch.bar, G * p, abort_flag, err) ? 1 : 0;
+                named_bar(1, 128);
+                const int w_ok = sm.wait_ok;
+                named_bar(1, 128);
+                if (!w_ok) break;
+            }
+            load_row_scales(P.e, sm);
+            long long ub, ue;
+                cta_units(sp, c, ub, ue);
+            for (long long u = ub; u < ue;) {
+                const int tile = (int)(u / sp.kb);
+                const long long seg_end = min(ue, (long long)(tile + 1) * sp.kb);
+                const int first = cta_of(sp, (long long)tile * sp.kb);
+                const int last = cta_of(sp, (long long)(tile + 1) * sp.kb - 1);
+                // one thread waits (bounded) and broadcasts, so all 128 leave together
+                if (etid() == 0) sm.wait_ok = mbar_wait(acc_full, acc_phase, abort_flag, err) ? 1 : 0;
+                named_bar(1, 128);
+                const int w_ok = sm.wait_ok;
+                named_bar(1, 128);
+                if (!w_ok) { ok = false; break; }
+                acc_phase ^= 1u;
+                tc_fence_after();
+                finish_segment<__nv_bfloat16>(P.e, sp, tile, c - first, last - first + 1, sm, ld);
+                u = seg_end;
+            }
+            if (ok && ch.n > 1) {
+                // this CTA's share of phase p is written: count it (release)
+                named_bar(1, 128);
+                if (etid() == 0) {
+                    fence_proxy_async_global();
+                    __threadfence();
+                    red_release_gpu_add(ch.bar, 1);
+                }
+            }
         }
     }
 
@@ -516,6 +644,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, L.tmem_cols);
+    }
+    if (threadIdx.x == 0 && ch.n > 1) {
+        if (atomic_add_acq_rel(ch.done, 1) == G - 1) {
+            *ch.bar = 0;
+            *ch.done = 0;
+        }
     }
 }
 
@@ -630,6 +764,60 @@ static TcLayout tc_layout(int T_pad, int rows_pad) {
     return L;
 }
 
+static_assert(sizeof(GemmChain) + sizeof(TcLayout) <= 4096, "chain parameters exceed the 4 KB kernel parameter space");
+
+// counters past the per-tile ones: chain barrier, chain exit count, LM-head tile count
+static int* chain_bar(spec_model* m) { return m->counters + m->n_counters - 3; }
+static int* chain_done(spec_model* m) { return m->counters + m->n_counters - 2; }
+
+static int check_split(spec_model* m, const Split& s) {
+    if ((size_t)s.n_tiles * s.max_slots * s.T_pad * kTileN > m->gemm_part_floats || s.n_tiles > m->n_counters - 3)
+        return set_error(SPEC_ERR_CAPACITY, "GEMM workspace too small for this launch");
+    return SPEC_OK;
+}
+
+static double algorithmic_bytes(const spec_model* m, const GemmLaunch& g, int T) {
+    // weights once, activation rows in, output rows out
+    return (double)g.N * g.K * m->elem + (double)T * g.K * m->elem + (double)T * g.N * m->elem;
+}
+
+// bf16: one launch of the chain kernel over steps[0..n) (rows T <= kMaxTPad, all
+// phases on the same rows)
+static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStream_t st) {
+    GemmChain ch{};
+    const int T = steps[0].e.T;
+    const int T_pad = ((T + 15) / 16) * 16;
+    int G = 1;
+    double bytes = 0.0;
+    for (int p = 0; p < n; ++p) {
+        GemmPhase& P = ch.ph[p];
+        P.tmW = *steps[p].g.tmW;
+        P.tmX = m->tm_x[steps[p].xbuf][T_pad / 16 - 1];
+        P.sp = make_split(m, steps[p].g.N, steps[p].g.K, T_pad);
+        P.sp.part = m->gemm_part;
+        P.sp.counters = m->counters;
+        SPEC_TRY(check_split(m, P.sp));
+        P.e = steps[p].e;
+        G = std::max(G, P.sp.G);
+        bytes += algorithmic_bytes(m, steps[p].g, T);
+    }
+    ch.n = n;
+    ch.bar = chain_bar(m);
+    ch.done = chain_done(m);
+    TcLayout L = tc_layout(T_pad, m->max_rows_pad);
+    const size_t smem = tc_smem_bytes(L);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        attr_set = true;
+    }
+    const int slot = prof_start(m, st);
+    launch_k(m->pdl, gemm_tc_kernel, dim3(G), dim3(kTcThreads), smem, st, ch, L);
+    ++m->launches;
+    prof_stop(m, slot, st, PROF_GEMM, bytes);
+    return check_cuda(cudaGetLastError(), "GEMM launch");
+}
+
 int launch_gemm(spec_model* m, const GemmLaunch& g, EpiParams e, int xbuf, cudaStream_t st) {
     const int T_total = e.T, r_base = e.r0;
     const int max_t = m->bf16 ? kMaxTPad : kSimtMaxT;
@@ -640,34 +828,34 @@ int launch_gemm(spec_model* m, const GemmLaunch& g, EpiParams e, int xbuf, cudaS
         if (ec.kind == EPI_HEAD && (e.head_mode == HEAD_ACCEPT_CHAIN || e.head_mode == HEAD_ACCEPT_TREE) &&
             done + max_t < T_total)
             ec.head_mode = HEAD_STATS;   // acceptance once every row has its summary
-        const int T_pad = m->bf16 ? ((ec.T + 15) / 16) * 16 : kSimtMaxT;
-        Split s = make_split(m, g.N, g.K, T_pad);
+        if (m->bf16) {
+            GemmStep one{g, ec, xbuf};
+            SPEC_TRY(launch_tc_chain(m, &one, 1, st));
+            continue;
+        }
+        Split s = make_split(m, g.N, g.K, kSimtMaxT);
         s.part = m->gemm_part;
         s.counters = m->counters;
-        if ((size_t)s.n_tiles * s.max_slots * T_pad * kTileN > m->gemm_part_floats || s.n_tiles > m->n_counters - 1)
-            return set_error(SPEC_ERR_CAPACITY, "GEMM workspace too small for this launch");
+        SPEC_TRY(check_split(m, s));
         const int slot = prof_start(m, st);
-        if (m->bf16) {
-            TcLayout L = tc_layout(T_pad, m->max_rows_pad);
-            const size_t smem = tc_smem_bytes(L);
-            static bool attr_set = false;
-            if (!attr_set) {
-                cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-                attr_set = true;
-            }
-            launch_k(m->pdl, gemm_tc_kernel, dim3(s.G), dim3(kTcThreads), smem, st, *g.tmW,
-                     m->tm_x[xbuf][T_pad / 16 - 1], s, L, ec);
-        } else {
-            launch_k(m->pdl, gemm_f32_kernel, dim3(s.G), dim3(128), 0, st, static_cast<const float*>(g.W), static_cast<const float*>(g.X),
-                                                 g.x_stride, g.N, g.K, s, ec);
-        }
+        launch_k(m->pdl, gemm_f32_kernel, dim3(s.G), dim3(128), 0, st, static_cast<const float*>(g.W),
+                 static_cast<const float*>(g.X), g.x_stride, g.N, g.K, s, ec);
         ++m->launches;
-        // algorithmic bytes: weights once, activation rows in, output rows out
-        prof_stop(m, slot, st, PROF_GEMM,
-                  (double)g.N * g.K * m->elem + (double)ec.T * g.K * m->elem + (double)ec.T * g.N * m->elem);
+        prof_stop(m, slot, st, PROF_GEMM, algorithmic_bytes(m, g, ec.T));
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return check_cuda(err, "GEMM launch");
     }
+    return SPEC_OK;
+}
+
+int launch_gemm_chain(spec_model* m, const GemmStep* steps, int n, cudaStream_t st) {
+    if (n <= 0) return SPEC_OK;
+    if (n > kMaxPhases) return set_error(SPEC_ERR_ARG, "GEMM chain longer than kMaxPhases");
+    bool one_launch = m->bf16 && m->chain && n > 1 && steps[0].e.T <= kMaxTPad;
+    for (int p = 1; p < n && one_launch; ++p)
+        one_launch = steps[p].e.T == steps[0].e.T && steps[p].e.r0 == steps[0].e.r0;
+    if (one_launch) return launch_tc_chain(m, steps, n, st);
+    for (int p = 0; p < n; ++p) SPEC_TRY(launch_gemm(m, steps[p].g, steps[p].e, steps[p].xbuf, st));
     return SPEC_OK;
 }
 

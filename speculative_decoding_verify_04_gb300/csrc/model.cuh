@@ -92,7 +92,8 @@ struct spec_model {
     spec_row_stats* row_stats = nullptr;  // [max_rows]
     float* gemm_part = nullptr;      // split-K partial tiles
     size_t gemm_part_floats = 0;
-    int* counters = nullptr;         // tile arrival counters (zero between launches)
+    int* counters = nullptr;         // tile arrival counters, then chain barrier, chain exits, head tiles
+                                     // (all zero between launches)
     int n_counters = 0;
     float* attn_part = nullptr;      // attention split partials
     size_t attn_part_floats = 0;
@@ -106,6 +107,7 @@ struct spec_model {
     CUtensorMap tm_x[3][spec::kMaxTPad / 16];
 
     bool pdl = true;                 // launch forward kernels with programmatic dependent launch
+    bool chain = true;               // bf16: consecutive GEMMs of a layer share one launch
 
     // tracing: kernel launches issued, and (when enabled) CUDA events around
     // every GEMM / attention launch with the launch's algorithmic bytes
@@ -131,6 +133,12 @@ namespace spec {
 // error reporting (capi.cu)
 int set_error(int code, const std::string& msg);
 int check_cuda(cudaError_t e, const char* what);
+// returns the first non-OK status of x from the enclosing function
+#define SPEC_TRY(x)                          \
+    do {                                     \
+        int rc_ = (x);                       \
+        if (rc_ != SPEC_OK) return rc_;      \
+    } while (0)
 
 // tracing (capi.cu): bracket one kernel launch with events when enabled
 enum ProfKind : int { PROF_GEMM = 0, PROF_ATTN = 1 };
@@ -201,6 +209,15 @@ struct GemmLaunch {
 
 // gemm.cu
 int launch_gemm(spec_model* m, const GemmLaunch& g, EpiParams e, int xbuf, cudaStream_t st);
+// One GEMM of a chain: its operands, epilogue and activation buffer index.
+struct GemmStep {
+    GemmLaunch g;
+    EpiParams e;
+    int xbuf;
+};
+// Runs the GEMMs in order.  bf16 models with every step on the same rows
+// (T <= kMaxTPad) run them in one launch separated by grid barriers.
+int launch_gemm_chain(spec_model* m, const GemmStep* steps, int n, cudaStream_t st);
 size_t gemm_partial_floats_needed(const spec_model* m, int N, int K, int T_pad);
 int gemm_grid(const spec_model* m, int N, int K);
 

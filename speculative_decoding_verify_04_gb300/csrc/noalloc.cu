@@ -86,7 +86,7 @@ extern "C" int spec_verify_noalloc(spec_model* m, spec_kv* kv, int32_t batch, co
     }
     int attn_blocks = 0;
     const size_t attn_floats = attn_scratch_floats(m, batch, max_r, kv->max_ctx, &attn_blocks);
-    const int n_counters = tiles + 1;
+    const int n_counters = tiles + 3;     // + chain barrier, chain exits, head tiles
     const size_t cnt_bytes = round256((size_t)(n_counters + attn_blocks) * 4);
     const size_t need = cnt_bytes + round256(gemm_floats * 4) + round256(attn_floats * 4);
     if (need > kScratchBytes)
