@@ -474,27 +474,6 @@ static void launch_decode_rb(bool pdl, const AttnParams& a, int nq, dim3 grid, c
 //   P V, n-tile nt: column n = g is head dim (HD/8)*g + nt, so lane (g, c)
 //     reads V rows 4c .. 4c+3 at dims (HD/8)*g .. (HD/8)*g + HD/8 - 1.
 
-SPEC_DEV void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                       uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-SPEC_DEV uint32_t pack_bf16(float lo, float hi) {
-    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return l | (h << 16);
-}
-// residuals of pack_bf16: x - bf16(x) for both halves
-SPEC_DEV uint32_t pack_bf16_lo(float lo, float hi) {
-    return pack_bf16(lo - __bfloat162float(__float2bfloat16_rn(lo)), hi - __bfloat162float(__float2bfloat16_rn(hi)));
-}
-// two bf16 from 16-bit halves of two 32-bit words: (low half of x, low half of y) etc.
-SPEC_DEV uint32_t pair_lo(uint32_t x, uint32_t y) { return __byte_perm(x, y, 0x5410); }
-SPEC_DEV uint32_t pair_hi(uint32_t x, uint32_t y) { return __byte_perm(x, y, 0x7632); }
 
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads)
@@ -781,8 +760,9 @@ size_t attn_scratch_floats(const spec_model* m, int batch, int max_rows_per_seq,
     const spec_model_config& c = m->cfg;
     if (m->bf16) {
         const AttnShape sh = attn_shape(m, batch, max_rows_per_seq, kv_ctx);
-        *n_counters = sh.blocks;
-        return (size_t)sh.blocks * sh.splits * kQPerCta * (c.head_dim + 2);
+        // also room for the attention phase of the GEMM chain
+        *n_counters = std::max(sh.blocks, batch * c.n_kv_heads);
+        return std::max((size_t)sh.blocks * sh.splits * kQPerCta * (c.head_dim + 2), attn_phase_part_floats(m));
     }
     if (max_rows_per_seq * (c.n_heads / c.n_kv_heads) <= 8) {
         const int blocks = batch * c.n_kv_heads;
@@ -799,8 +779,9 @@ size_t attn_partial_floats_needed(const spec_model* m, int batch, int max_rows_p
     const spec_model_config& c = m->cfg;
     const int G = c.n_heads / c.n_kv_heads;
     const int n_rb = rows_blocks(max_rows_per_seq, G);
-    return std::max((size_t)batch * c.n_kv_heads * n_rb * 32, (size_t)batch * c.n_kv_heads * 64) * kQPerCta *
-           (c.head_dim + 2);
+    const size_t own = std::max((size_t)batch * c.n_kv_heads * n_rb * 32, (size_t)batch * c.n_kv_heads * 64) *
+                       kQPerCta * (c.head_dim + 2);
+    return m->bf16 ? std::max(own, attn_phase_part_floats(m)) : own;
 }
 
 int launch_attention(spec_model* m, const AttnParams& a0, int max_rows_per_seq, cudaStream_t st) {

@@ -282,7 +282,9 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
                       int tree, bool head_follows, const HeadSpec* head, cudaStream_t st) {
     const spec_model_config& c = m->cfg;
     const int qdim = c.n_heads * c.head_dim;
-    GemmStep pend[4];
+    // attention as the first phase of the chain that follows it (one launch per layer)
+    const bool fused = T <= kMaxTPad && attn_phase_ok(m, kv, batch, max_rows_per_seq);
+    GemmStep pend[5];
     int np = 0;
     for (int l = lo; l < hi; ++l) {
         LayerWeights& L = m->layers[l];
@@ -296,7 +298,29 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             SPEC_TRY(launch_gemm_chain(m, pend, np, st));
             np = 0;
         }
-        {   // attention
+        if (fused) {   // attention phase
+            GemmStep at{};
+            at.kind = PH_ATTN;
+            at.g.tmW = &kv->tm_k;
+            at.g.tmX = &kv->tm_v;
+            at.e = e;
+            at.at.q = m->q;
+            at.at.out = m->x_attn;
+            at.at.out_lo = (size_t)m->max_rows_pad * qdim;
+            at.at.plan = m->plan;
+            at.at.batch = batch;
+            at.at.kv_batch = kv->batch;
+            at.at.kv_ctx = kv->max_ctx;
+            at.at.layer = l;
+            at.at.n_heads = c.n_heads;
+            at.at.n_kv_heads = c.n_kv_heads;
+            at.at.head_dim = c.head_dim;
+            at.at.tree = tree;
+            at.at.linear = max_rows_per_seq * (c.n_heads / c.n_kv_heads) <= kAttnSimtQ;
+            at.at.kc = kv->k;
+            at.at.vc = kv->v;
+            pend[np++] = at;
+        } else {   // attention
             AttnParams a{};
             a.q = m->q;
             a.kc = kv->k;
@@ -446,6 +470,13 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
         // SPEC_CHAIN=0 launches every GEMM on its own
         const char* ce = getenv("SPEC_CHAIN");
         m->chain = !(ce && ce[0] == '0');
+        // SPEC_ATTN_PHASE=1 runs attention as the first phase of each layer's GEMM chain
+        // (one launch per layer) instead of its own kernel
+        const char* ae = getenv("SPEC_ATTN_PHASE");
+        m->attn_phase = ae && ae[0] == '1';
+        // SPEC_L2_AHEAD=n: L2 lookahead of the GEMM chain producer, in units (0 turns it off)
+        const char* le = getenv("SPEC_L2_AHEAD");
+        if (le) m->l2_ahead = std::max(0, std::min(64, atoi(le)));
     }
     m->elem = m->bf16 ? 2 : 4;
     if (m->bf16) {
@@ -555,6 +586,7 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
     const size_t w_ap = take(m->attn_part_floats * 4);
     const size_t w_ac = take((size_t)m->n_attn_counters * 4);
     const size_t w_err = take(64);
+    const size_t w_pkv = take(64);
     const size_t w_plan = take((size_t)(4 * R + 3 * c.max_batch + 2 * kMaxSeqRows + 64) * 4);
     m->ws_bytes = off;
     if ((rc = check_cuda(cudaMalloc(&m->ws, off), "cudaMalloc(workspace)"))) return fail(rc);
@@ -573,6 +605,7 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
     m->attn_part = (float*)(S + w_ap);
     m->attn_counters = (int*)(S + w_ac);
     m->err = (int*)(S + w_err);
+    m->prof_kv = (unsigned long long*)(S + w_pkv);
     int* pl = (int*)(S + w_plan);
     m->plan.row_seq = pl; pl += R;
     m->plan.row_slot = pl; pl += R;
@@ -599,7 +632,7 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
         const int xk[3] = {d, qdim, F};
         for (int i = 0; i < 3; ++i)
             for (int tp = 16; tp <= t_pad_max; tp += 16)
-                ok &= make_tmap_2d(&m->tm_x[i][tp / 16 - 1], xb[i], xk[i], 2 * Rp, (uint64_t)xk[i] * 2, kTileK, tp);
+                ok &= make_tmap_x(&m->tm_x[i][tp / 16 - 1], xb[i], xk[i], Rp, tp);
         if (!ok) return fail(set_error(SPEC_ERR_CUDA, "cuTensorMapEncodeTiled failed"));
     }
     if ((rc = check_cuda(cudaStreamSynchronize(st), "spec_model_create sync"))) return fail(rc);
@@ -632,6 +665,7 @@ extern "C" int spec_kv_create(spec_model* m, int32_t batch, int32_t max_ctx, spe
     if (!rc) rc = check_cuda(cudaMemset(kv->k, 0, bytes), "clear K");
     if (!rc) rc = check_cuda(cudaMemset(kv->v, 0, bytes), "clear V");
     if (!rc) rc = check_cuda(cudaMemset(kv->len, 0, (size_t)batch * 4), "clear lengths");
+    if (!rc && !make_kv_tmaps(kv)) rc = set_error(SPEC_ERR_CUDA, "spec_kv_create: K/V tensor maps");
     if (rc) {
         cudaFree(kv->k); cudaFree(kv->v); cudaFree(kv->len);
         delete kv;
@@ -838,7 +872,10 @@ extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int3
 extern "C" int spec_profile(spec_model* m, int32_t enable) {
     if (!m) return set_error(SPEC_ERR_ARG, "spec_profile: null model");
     m->prof_on = enable != 0;
-    if (m->prof_on) m->prof_n = 0;
+    if (m->prof_on) {
+        m->prof_n = 0;
+        SPEC_CUDA(cudaMemset(m->prof_kv, 0, sizeof(unsigned long long)), "profile reset");
+    }
     return SPEC_OK;
 }
 
@@ -854,6 +891,12 @@ extern "C" int spec_profile_read(spec_model* m, int32_t kind, double* total_ms, 
         ms += t;
         by += m->prof_bytes[i];
         ++n;
+    }
+    if (kind == PROF_GEMM && n > 0) {
+        // K/V bytes read by attention phases of the chains (counted on the device)
+        unsigned long long kvb = 0;
+        SPEC_CUDA(cudaMemcpy(&kvb, m->prof_kv, sizeof(kvb), cudaMemcpyDeviceToHost), "profile read");
+        by += (double)kvb;
     }
     *total_ms = ms;
     *bytes = by;

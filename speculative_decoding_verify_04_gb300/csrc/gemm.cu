@@ -37,6 +37,7 @@
 #include <cstring>
 #include <cudaTypedefs.h>
 
+#include "attn_phase.cuh"
 #include "model.cuh"
 #include "stats.cuh"
 
@@ -46,8 +47,7 @@ namespace spec {
 // host: tensor maps
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+static bool load_encoder() {
     if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
         void* fn = nullptr;
@@ -56,6 +56,12 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
             return false;
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
+    return true;
+}
+
+bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    if (!load_encoder()) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
@@ -64,6 +70,56 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Activation buffer of bf16 hi rows then lo rows ([2][rows_pad][K]) as a 3-D
+// map {K, rows_pad, 2}: one box {64, tp, 2} is a k-block of tp rows, hi tile
+// then lo tile, as the MMA's B operand wants them (one copy instead of two).
+bool make_tmap_x(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows_pad, uint32_t tp) {
+    if (!load_encoder()) return false;
+    cuuint64_t dims[3] = {K, rows_pad, 2};
+    cuuint64_t strides[2] = {K * 2, rows_pad * K * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kTileK, tp, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// K and V cache maps of a bf16 cache: {hd, seq * kvh * slot, layer}, boxes of
+// 64 dims x (4096 / hd) slots x 1 layer, 128-byte swizzle (the attention phase
+// reads a unit of 8 KB of K and 8 KB of V per ring slot).
+bool make_kv_tmaps(spec_kv* kv) {
+    const spec_model* m = kv->m;
+    const spec_model_config& c = m->cfg;
+    kv->tmaps = false;
+    if (!m->bf16 || (c.head_dim != 64 && c.head_dim != 128)) return true;
+    const uint64_t rows = (uint64_t)kv->batch * c.n_kv_heads * kv->max_ctx;
+    if (rows >= (1ull << 31)) return true;            // slot coordinates are 32-bit
+    if (!load_encoder()) return false;
+    for (int w = 0; w < 2; ++w) {
+        cuuint64_t dims[3] = {(cuuint64_t)c.head_dim, rows, (cuuint64_t)c.n_layers};
+        cuuint64_t strides[2] = {(cuuint64_t)c.head_dim * 2, rows * c.head_dim * 2};
+        cuuint32_t box[3] = {64, (cuuint32_t)(4096 / c.head_dim), 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = g_encode(w ? &kv->tm_v : &kv->tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w ? kv->v : kv->k, dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return false;
+    }
+    kv->tmaps = true;
+    return true;
+}
+
+size_t attn_phase_part_floats(const spec_model* m) {
+    return (size_t)m->num_sms * 2 * kAttnMaxQ * (m->cfg.head_dim + 2);
+}
+
+bool attn_phase_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq) {
+    const int G = m->cfg.n_heads / m->cfg.n_kv_heads;
+    return m->attn_phase && kv->tmaps && max_rows_per_seq * G <= kAttnMaxQ && batch <= kMaxPlanBatch &&
+           m->attn_part_floats >= attn_phase_part_floats(m) && m->n_attn_counters >= batch * m->cfg.n_kv_heads;
 }
 
 // ---------------------------------------------------------------------------
@@ -375,10 +431,24 @@ struct TcLayout {
     uint32_t b_bytes;     // hi + lo activation tiles of one stage
     uint32_t tmem_cols;
     int rows_pad;         // first row of the lo half in the X buffers
+    uint32_t attn_bytes;  // AttnSmem when the chain has an attention phase, else 0
+    int l2_ahead;         // units the producer prefetches into L2 ahead of its loads
+    int attn_slots;       // attention ring: all 16 KB slots (weight slots, activation region, spare)
+    int attn_nb;          // of which in the activation-tile region
 };
 
+constexpr size_t kEpiSmemBytes = (sizeof(EpiSmem) + 15) & ~size_t(15);
+
+constexpr size_t kBarBytes = 512;     // ring, accumulator and attention-ring barriers, TMEM slot, abort flag
+
+// everything but the attention ring's spare slots
+__host__ __device__ inline size_t tc_smem_core(const TcLayout& L) {
+    return 1024 + (size_t)L.stages * (kATileBytes + L.b_bytes) + kBarBytes + kEpiSmemBytes + L.attn_bytes;
+}
+// spare attention slots start at the next 1 KB boundary after the core
 __host__ __device__ inline size_t tc_smem_bytes(const TcLayout& L) {
-    return 1024 + (size_t)L.stages * (kATileBytes + L.b_bytes) + 256 + sizeof(EpiSmem) + 64;
+    const int spare = L.attn_slots > 0 ? L.attn_slots - L.stages - L.attn_nb : 0;
+    return ((tc_smem_core(L) + 1023) & ~size_t(1023)) + (size_t)spare * kAttnUnitBytes + 64;
 }
 
 struct TmemLoader {
@@ -396,19 +466,24 @@ struct TmemLoader {
 // streams the next phase's weight tiles into the ring while the previous phase
 // finishes; only the activation tiles wait for the barrier.  One phase is a
 // plain GEMM launch.
-constexpr int kMaxPhases = 4;
+constexpr int kMaxPhases = 5;
 constexpr int kMaxStages = 8;
 
+// A GEMM phase uses tmW, tmX, sp and e; an attention phase uses tmW / tmX as
+// the K / V cache maps and `at`.
 struct GemmPhase {
     CUtensorMap tmW;
     CUtensorMap tmX;
     Split sp;
     EpiParams e;
+    AttnPhase at;
+    int kind;      // PhaseKind
 };
 
 struct GemmChain {
     GemmPhase ph[kMaxPhases];
     int n;
+    int attn;      // index of the attention phase, -1 if none (at most one)
     int* bar;      // per launch: CTAs that finished a phase, summed over phases
     int* done;     // CTAs that finished the chain; the last one resets both counters
 };
@@ -452,9 +527,23 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
     uint64_t* acc_full = bars + 2 * L.stages;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* drain = acc_full + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 3);
+    uint64_t* attn_done = acc_full + 3;      // the epilogue warps finished the attention phase
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    EpiSmem& sm = *reinterpret_cast<EpiSmem*>(reinterpret_cast<uint8_t*>(bars) + 256);
+    uint64_t* attn_full = acc_full + 6;
+    uint64_t* attn_empty = attn_full + kAttnMaxSlots;
+    EpiSmem& sm = *reinterpret_cast<EpiSmem*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);
+    AttnSmem& as = *reinterpret_cast<AttnSmem*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes + kEpiSmemBytes);
+    // the attention ring: the weight slots, the activation-tile region, then spare memory
+    AttnRing R;
+    R.a = sA;
+    R.na = L.stages;
+    R.b = sB;
+    R.nb = L.attn_nb;
+    R.x = reinterpret_cast<uint8_t*>(((reinterpret_cast<uintptr_t>(&as) + L.attn_bytes) + 1023) & ~uintptr_t(1023));
+    R.n = L.attn_slots;
+    R.full = attn_full;
+    R.empty = attn_empty;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x, G = gridDim.x;
@@ -465,6 +554,8 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 128);
         mbar_init(drain, 1);
+        mbar_init(attn_done, 1);
+        for (int s = 0; s < L.attn_slots; ++s) { mbar_init(attn_full + s, 1); mbar_init(attn_empty + s, 1); }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -472,11 +563,14 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
         tmem_alloc(tmem_slot, L.tmem_cols);
         tmem_relinquish();
     }
+    // the attention phase's unit table reads the row plan, which a kernel at
+    // least two launches back wrote (every kernel of the stream triggers its
+    // dependants only after its own wait, so that one has completed)
+    if (ch.attn >= 0 && warp == 4) attn_unit_table(ch.ph[ch.attn].at, as);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    if (threadIdx.x == 0) pdl_trigger();
 
     if (warp == 4) {
         if (lane == 0) {
@@ -488,32 +582,135 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
+            int a_slot = 0;           // attention ring position
+            uint32_t a_phase = 0;
+            long long a_issued = 0;
             int def_stage[kMaxStages];
             int def_kb[kMaxStages];
             int n_def = 0;
             bool ok = true;
             const GemmPhase* P = &ch.ph[0];
-            auto load_x = [&](const GemmPhase& Q, int st, int kbi) {
-                tma_load_2d(sB + (size_t)st * L.b_bytes, &Q.tmX, kbi * kTileK, Q.e.r0, full + st, px);
-                tma_load_2d(sB + (size_t)st * L.b_bytes + L.b_bytes / 2, &Q.tmX, kbi * kTileK,
-                            L.rows_pad + Q.e.r0, full + st, px);
+            auto load_x = [&](const GemmPhase& Q, int st, int kbi) {     // hi and lo tiles in one box
+                tma_load_3d(sB + (size_t)st * L.b_bytes, &Q.tmX, kbi * kTileK, Q.e.r0, 0, full + st, px);
             };
-            // activation tiles of a phase wait for the previous phase (the previous
-            // kernel for phase 0); its weight tiles do not
+            // what a phase reads from the previous phase (the previous kernel for
+            // phase 0) waits for it; weight tiles and committed KV slots do not
+            bool dep0 = false;      // the previous kernel has completed
             auto dep_wait = [&](int p) -> bool {
-                if (p == 0) { pdl_wait(); return true; }
+                if (p == 0) { pdl_wait(); dep0 = true; return true; }
                 if (!grid_wait(ch.bar, G * p, abort_flag, err)) return false;
                 fence_proxy_async_global();     // the rows were written by other CTAs' epilogues
                 return true;
             };
+            // L2 lookahead: a second cursor walks the same units (across phases) l2_ahead
+            // units ahead of the loads and prefetches their weight / K / V boxes into
+            // L2, so that more bytes are in flight than the ring holds.  Units holding
+            // rows the previous kernel writes are skipped until it has completed.
+            auto range_of = [&](int q, long long& b0, long long& e0) {
+                if (ch.ph[q].kind == PH_ATTN) attn_range(as.prefix[ch.ph[q].at.batch], G, c, b0, e0);
+                else cta_units(ch.ph[q].sp, c, b0, e0);
+            };
+            int pf_p = 0;
+            long long pf_u, pf_e;
+            range_of(0, pf_u, pf_e);
+            auto prefetch_next = [&]() {
+                if (L.l2_ahead == 0) return;
+                while (pf_p < ch.n && pf_u >= pf_e)
+                    if (++pf_p < ch.n) range_of(pf_p, pf_u, pf_e);
+                if (pf_p >= ch.n) return;
+                const GemmPhase& Q = ch.ph[pf_p];
+                if (Q.kind == PH_ATTN) {
+                    const AttnPhase& A = Q.at;
+                    const AttnUnit au = attn_locate(as, A.batch, A.n_kv_heads, pf_u);
+                    const int ku = attn_keys_per_unit(A.head_dim);
+                    const int key0 = au.tile * ku;
+                    if (key0 + ku <= as.base[au.b] || (pf_p == 0 && dep0)) {
+                        const int row = (au.b * A.n_kv_heads + au.g) * A.kv_ctx + key0;
+                        for (int db = 0; db < A.head_dim / 64; ++db) {
+                            tma_prefetch_l2_3d(&Q.tmW, 64 * db, row, A.layer);
+                            tma_prefetch_l2_3d(&Q.tmX, 64 * db, row, A.layer);
+                        }
+                    }
+                } else {
+                    const int tile = (int)(pf_u / Q.sp.kb), kbi = (int)(pf_u % Q.sp.kb);
+                    tma_prefetch_l2_2d(&Q.tmW, kbi * kTileK, tile * kTileN);
+                }
+                ++pf_u;
+            };
+            for (int i = 0; i < L.l2_ahead; ++i) prefetch_next();
             for (int p = 0; ok && p < ch.n; ++p) {
                 P = &ch.ph[p];
+                n_def = 0;
+                if (P->kind == PH_ATTN) {
+                    const AttnPhase& A = P->at;
+                    long long ub, ue;
+                    attn_range(as.prefix[A.batch], G, c, ub, ue);
+                    const int ku = attn_keys_per_unit(A.head_dim), nbox = A.head_dim / 64;
+                    const uint32_t box = (uint32_t)ku * 128u;
+                    bool dep = false;
+                    // (sequence, head, slot tile) of the current unit, stepped without divisions
+                    const int n_units = (int)(ue - ub);
+                    AttnUnit au = n_units > 0 ? attn_locate(as, A.batch, A.n_kv_heads, ub) : AttnUnit{0, 0, 0, 1};
+                    int seq_base = as.base[au.b];
+                    int seq_keys = min(seq_base + as.nrows[au.b], A.kv_ctx);
+                    for (int i = 0; i < n_units; ++i) {
+                        if (i > 0 && ++au.tile == au.tiles) {
+                            au.tile = 0;
+                            if (++au.g == A.n_kv_heads) {
+                                au.g = 0;
+                                ++au.b;
+                                au.tiles = (as.prefix[au.b + 1] - as.prefix[au.b]) / A.n_kv_heads;
+                                seq_base = as.base[au.b];
+                                seq_keys = min(seq_base + as.nrows[au.b], A.kv_ctx);
+                            }
+                        }
+                        const int key0 = au.tile * ku;
+                        // units holding new (or unused) slots wait for the rows' writer
+                        if (!dep && key0 + ku > seq_base) {
+                            if (!dep_wait(p)) { ok = false; break; }
+                            dep = true;
+                        }
+                        if (!mbar_wait(R.empty + a_slot, a_phase ^ 1u, abort_flag, err)) { ok = false; break; }
+                        uint8_t* dst = R.slot(a_slot);
+                        uint64_t* fb = R.full + a_slot;
+                        if (A.linear) {
+                            // the unit's valid K rows and V rows: two contiguous copies
+                            const uint32_t bytes = (uint32_t)min(ku, seq_keys - key0) * A.head_dim * 2;
+                            const size_t off =
+                                ((((size_t)A.layer * A.kv_batch + au.b) * A.n_kv_heads + au.g) * A.kv_ctx + key0) *
+                                A.head_dim * 2;
+                            mbar_arrive_expect_tx(fb, 2 * bytes);
+                            bulk_load(dst, static_cast<const char*>(A.kc) + off, bytes, fb, pw);
+                            bulk_load(dst + kAttnUnitBytes / 2, static_cast<const char*>(A.vc) + off, bytes, fb, pw);
+                        } else {
+                            mbar_arrive_expect_tx(fb, kAttnUnitBytes);
+                            const int row = (au.b * A.n_kv_heads + au.g) * A.kv_ctx + key0;
+                            for (int db = 0; db < nbox; ++db) {
+                                tma_load_3d(dst + db * box, &P->tmW, 64 * db, row, A.layer, fb, pw);
+                                tma_load_3d(dst + (nbox + db) * box, &P->tmX, 64 * db, row, A.layer, fb, pw);
+                            }
+                        }
+                        prefetch_next();
+                        ++a_issued;
+                        if (++a_slot == R.n) { a_slot = 0; a_phase ^= 1u; }
+                    }
+                    // wait for the dependency even without a dependent unit: the grid
+                    // barrier of the next phase is only meaningful once the previous
+                    // kernel (which resets it) has completed
+                    if (ok && !dep && !dep_wait(p)) ok = false;
+                    // the attention slots overlap the GEMM ring: reuse them once the
+                    // epilogue warps have finished the phase
+                    if (ok && !mbar_wait(attn_done, 0, abort_flag, err)) ok = false;
+                    continue;
+                }
                 const Split& sp = P->sp;
                 long long ub, ue;
                 cta_units(sp, c, ub, ue);
                 bool dep = false;
-                n_def = 0;
-                for (long long u = ub; u < ue; ++u) {
+                // (tile, k-block) of the current unit, stepped without divisions
+                int tile = (int)(ub / sp.kb), kbi = (int)(ub % sp.kb);
+                const int n_units = (int)(ue - ub);
+                for (int i = 0; i < n_units; ++i) {
                     if (!dep && n_def == L.stages) {
                         if (!dep_wait(p)) { ok = false; break; }
                         dep = true;
@@ -521,7 +718,6 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                         n_def = 0;
                     }
                     if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, err)) { ok = false; break; }
-                    const int tile = (int)(u / sp.kb), kbi = (int)(u % sp.kb);
                     mbar_arrive_expect_tx(full + stage, kATileBytes + L.b_bytes);
                     tma_load_2d(sA + (size_t)stage * kATileBytes, &P->tmW, kbi * kTileK, tile * kTileN, full + stage,
                                 pw);
@@ -532,8 +728,10 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                         def_kb[n_def] = kbi;
                         ++n_def;
                     }
+                    prefetch_next();
                     ++issued;
                     if (++stage == L.stages) { stage = 0; phase ^= 1u; }
+                    if (++kbi == sp.kb) { kbi = 0; ++tile; }
                 }
                 if (ok && !dep) {
                     if (!dep_wait(p)) { ok = false; }
@@ -552,6 +750,11 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                     if (--stage < 0) { stage = L.stages - 1; phase ^= 1u; }
                     mbar_wait(full + stage, phase, nullptr, err);
                 }
+                const long long na = a_issued < R.n ? a_issued : R.n;
+                for (long long i = 0; i < na; ++i) {
+                    if (--a_slot < 0) { a_slot = R.n - 1; a_phase ^= 1u; }
+                    mbar_wait(R.full + a_slot, a_phase, nullptr, err);
+                }
             }
         }
     } else if (warp == 5) {
@@ -560,6 +763,7 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int p = 0; ok && p < ch.n; ++p) {
+                if (ch.ph[p].kind == PH_ATTN) continue;    // the epilogue warps run it on the attention ring
                 const Split& sp = ch.ph[p].sp;
                 const uint32_t idesc = idesc_bf16_f32(128, sp.T_pad);
                 long long ub, ue;
@@ -598,9 +802,10 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
         uint32_t acc_phase = 0;
         bool ok = true;
         pdl_wait();
+        // only now may the next kernel launch (see the unit table above)
+        if (etid() == 0) pdl_trigger();
         for (int p = 0; ok && p < ch.n; ++p) {
             const GemmPhase& P = ch.ph[p];
-            const Split& sp = P.sp;
             if (p > 0) {
                 if (etid() == 0) sm.wait_ok = grid_wait(ch.bar, G * p, abort_flag, err) ? 1 : 0;
                 named_bar(1, 128);
@@ -608,24 +813,33 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                 named_bar(1, 128);
                 if (!w_ok) break;
             }
-            load_row_scales(P.e, sm);
-            long long ub, ue;
+            if (P.kind == PH_ATTN) {
+                const AttnPhase& A = P.at;
+                const bool a_ok = A.head_dim == 128 ? consume_attn<128>(A, as, R, c, G, abort_flag, err)
+                                                    : consume_attn<64>(A, as, R, c, G, abort_flag, err);
+                if (etid() == 0) mbar_arrive(attn_done);     // all 128 threads are past their last unit
+                if (!a_ok) { ok = false; break; }
+            } else {
+                const Split& sp = P.sp;
+                load_row_scales(P.e, sm);
+                long long ub, ue;
                 cta_units(sp, c, ub, ue);
-            for (long long u = ub; u < ue;) {
-                const int tile = (int)(u / sp.kb);
-                const long long seg_end = min(ue, (long long)(tile + 1) * sp.kb);
-                const int first = cta_of(sp, (long long)tile * sp.kb);
-                const int last = cta_of(sp, (long long)(tile + 1) * sp.kb - 1);
-                // one thread waits (bounded) and broadcasts, so all 128 leave together
-                if (etid() == 0) sm.wait_ok = mbar_wait(acc_full, acc_phase, abort_flag, err) ? 1 : 0;
-                named_bar(1, 128);
-                const int w_ok = sm.wait_ok;
-                named_bar(1, 128);
-                if (!w_ok) { ok = false; break; }
-                acc_phase ^= 1u;
-                tc_fence_after();
-                finish_segment<__nv_bfloat16>(P.e, sp, tile, c - first, last - first + 1, sm, ld);
-                u = seg_end;
+                for (long long u = ub; u < ue;) {
+                    const int tile = (int)(u / sp.kb);
+                    const long long seg_end = min(ue, (long long)(tile + 1) * sp.kb);
+                    const int first = cta_of(sp, (long long)tile * sp.kb);
+                    const int last = cta_of(sp, (long long)(tile + 1) * sp.kb - 1);
+                    // one thread waits (bounded) and broadcasts, so all 128 leave together
+                    if (etid() == 0) sm.wait_ok = mbar_wait(acc_full, acc_phase, abort_flag, err) ? 1 : 0;
+                    named_bar(1, 128);
+                    const int w_ok = sm.wait_ok;
+                    named_bar(1, 128);
+                    if (!w_ok) { ok = false; break; }
+                    acc_phase ^= 1u;
+                    tc_fence_after();
+                    finish_segment<__nv_bfloat16>(P.e, sp, tile, c - first, last - first + 1, sm, ld);
+                    u = seg_end;
+                }
             }
             if (ok && ch.n > 1) {
                 // this CTA's share of phase p is written: count it (release)
@@ -752,19 +966,34 @@ size_t gemm_partial_floats_needed(const spec_model* m, int N, int K, int T_pad) 
 
 int gemm_grid(const spec_model* m, int N, int K) { return make_split(m, N, K, 16).G; }
 
-static TcLayout tc_layout(int T_pad, int rows_pad) {
+static TcLayout tc_layout(int T_pad, int rows_pad, bool attn) {
     TcLayout L;
     L.rows_pad = rows_pad;
     L.b_bytes = 2u * (uint32_t)T_pad * kTileK * 2;
-    const size_t budget = 225 * 1024 - 1024 - 256 - sizeof(EpiSmem) - 64;
-    L.stages = (int)std::min<size_t>(8, budget / (kATileBytes + L.b_bytes));
+    L.attn_bytes = attn ? (uint32_t)((sizeof(AttnSmem) + 15) & ~size_t(15)) : 0u;
+    L.l2_ahead = 0;
+    const size_t budget = 225 * 1024 - 1024 - kBarBytes - kEpiSmemBytes - L.attn_bytes - 64;
+    L.stages = (int)std::min<size_t>(kMaxStages, budget / (kATileBytes + L.b_bytes));
     uint32_t cols = 32;
     while (cols < (uint32_t)T_pad) cols <<= 1;
     L.tmem_cols = cols;
+    L.attn_slots = 0;
+    L.attn_nb = 0;
+    if (attn) {
+        // attention ring: the weight slots, whole 16 KB slots of the activation region,
+        // then as many spare slots as the 227 KB limit leaves
+        L.attn_nb = (int)((size_t)L.stages * L.b_bytes / kAttnUnitBytes);
+        const size_t core = (tc_smem_core(L) + 1023) & ~size_t(1023);
+        const int spare = (int)((227 * 1024 - 64 - core) / kAttnUnitBytes);
+        L.attn_slots = std::min(kAttnMaxSlots, L.stages + L.attn_nb + std::max(0, spare));
+        L.attn_nb = std::min(L.attn_nb, L.attn_slots - L.stages);
+    }
     return L;
 }
 
-static_assert(sizeof(GemmChain) + sizeof(TcLayout) <= 4096, "chain parameters exceed the 4 KB kernel parameter space");
+// kernel parameters beyond 4 KB need CUDA 12.1+ (all of this code needs 13)
+static_assert(sizeof(GemmChain) + sizeof(TcLayout) <= 32764, "chain parameters exceed the kernel parameter space");
+static_assert(kAttnUnitBytes == kATileBytes, "an attention unit fills one weight slot of the ring");
 
 // counters past the per-tile ones: chain barrier, chain exit count, LM-head tile count
 static int* chain_bar(spec_model* m) { return m->counters + m->n_counters - 3; }
@@ -785,27 +1014,47 @@ static double algorithmic_bytes(const spec_model* m, const GemmLaunch& g, int T)
 // phases on the same rows)
 static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStream_t st) {
     GemmChain ch{};
+    ch.attn = -1;
     const int T = steps[0].e.T;
     const int T_pad = ((T + 15) / 16) * 16;
     int G = 1;
     double bytes = 0.0;
     for (int p = 0; p < n; ++p) {
         GemmPhase& P = ch.ph[p];
+        P.kind = steps[p].kind;
+        P.e = steps[p].e;
+        P.e.err = m->err;
+        if (P.kind == PH_ATTN) {
+            if (ch.attn >= 0) return set_error(SPEC_ERR_ARG, "GEMM chain: one attention phase at most");
+            ch.attn = p;
+            P.tmW = *steps[p].g.tmW;        // K cache map
+            P.tmX = *steps[p].g.tmX;        // V cache map
+            P.at = steps[p].at;
+            P.at.err = m->err;
+            P.at.part = m->attn_part;
+            P.at.counters = m->attn_counters;
+            P.at.kv_bytes = m->prof_on ? m->prof_kv : nullptr;
+            G = std::max(G, m->num_sms);
+            // output rows (K/V bytes are counted on the device)
+            bytes += (double)T * P.at.n_heads * P.at.head_dim * m->elem;
+            continue;
+        }
         P.tmW = *steps[p].g.tmW;
         P.tmX = m->tm_x[steps[p].xbuf][T_pad / 16 - 1];
         P.sp = make_split(m, steps[p].g.N, steps[p].g.K, T_pad);
         P.sp.part = m->gemm_part;
         P.sp.counters = m->counters;
         SPEC_TRY(check_split(m, P.sp));
-        P.e = steps[p].e;
         G = std::max(G, P.sp.G);
         bytes += algorithmic_bytes(m, steps[p].g, T);
     }
     ch.n = n;
     ch.bar = chain_bar(m);
     ch.done = chain_done(m);
-    TcLayout L = tc_layout(T_pad, m->max_rows_pad);
+    TcLayout L = tc_layout(T_pad, m->max_rows_pad, ch.attn >= 0);
+    L.l2_ahead = m->l2_ahead;
     const size_t smem = tc_smem_bytes(L);
+    if (smem > 227 * 1024) return set_error(SPEC_ERR_CAPACITY, "GEMM chain: shared memory layout too large");
     static bool attr_set = false;
     if (!attr_set) {
         cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -851,10 +1100,13 @@ int launch_gemm(spec_model* m, const GemmLaunch& g, EpiParams e, int xbuf, cudaS
 int launch_gemm_chain(spec_model* m, const GemmStep* steps, int n, cudaStream_t st) {
     if (n <= 0) return SPEC_OK;
     if (n > kMaxPhases) return set_error(SPEC_ERR_ARG, "GEMM chain longer than kMaxPhases");
-    bool one_launch = m->bf16 && m->chain && n > 1 && steps[0].e.T <= kMaxTPad;
+    bool has_attn = false;
+    for (int p = 0; p < n; ++p) has_attn |= steps[p].kind == PH_ATTN;
+    bool one_launch = m->bf16 && (m->chain || has_attn) && (n > 1 || has_attn) && steps[0].e.T <= kMaxTPad;
     for (int p = 1; p < n && one_launch; ++p)
         one_launch = steps[p].e.T == steps[0].e.T && steps[p].e.r0 == steps[0].e.r0;
     if (one_launch) return launch_tc_chain(m, steps, n, st);
+    if (has_attn) return set_error(SPEC_ERR_ARG, "attention phase outside a single-launch chain");
     for (int p = 0; p < n; ++p) SPEC_TRY(launch_gemm(m, steps[p].g, steps[p].e, steps[p].xbuf, st));
     return SPEC_OK;
 }

@@ -108,6 +108,8 @@ struct spec_model {
 
     bool pdl = true;                 // launch forward kernels with programmatic dependent launch
     bool chain = true;               // bf16: consecutive GEMMs of a layer share one launch
+    bool attn_phase = false;         // bf16: attention as the first phase of the layer's chain (SPEC_ATTN_PHASE=1)
+    int l2_ahead = 0;                // bf16 chains: units prefetched into L2 ahead of the ring (0: off)
 
     // tracing: kernel launches issued, and (when enabled) CUDA events around
     // every GEMM / attention launch with the launch's algorithmic bytes
@@ -117,6 +119,7 @@ struct spec_model {
     std::vector<int> prof_kind;
     std::vector<double> prof_bytes;
     size_t prof_n = 0;
+    unsigned long long* prof_kv = nullptr;   // device: K/V bytes read by attention phases while profiling
 };
 
 struct spec_kv {
@@ -126,6 +129,12 @@ struct spec_kv {
     void* k = nullptr;               // [layer][seq][kvh][slot][hd]
     void* v = nullptr;
     int* len = nullptr;              // [batch] committed lengths (device)
+    // bf16 caches: 3-D TMA maps {head dim, seq * kvh * slot, layer} with boxes
+    // of 64 dims x (8 KB / 128 B) slots, 128-byte swizzle (attention phase of the
+    // GEMM chain); tmaps is false where the cache is too large to address
+    alignas(64) CUtensorMap tm_k;
+    alignas(64) CUtensorMap tm_v;
+    bool tmaps = false;
 };
 
 namespace spec {
@@ -148,6 +157,7 @@ void prof_stop(spec_model* m, int slot, cudaStream_t st, int kind, double bytes)
 // tensor maps (gemm.cu)
 bool make_tmap_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+bool make_tmap_x(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows_pad, uint32_t tp);
 
 // Epilogue parameters of one GEMM launch (passed by value).
 struct EpiParams {
@@ -209,15 +219,49 @@ struct GemmLaunch {
 
 // gemm.cu
 int launch_gemm(spec_model* m, const GemmLaunch& g, EpiParams e, int xbuf, cudaStream_t st);
-// One GEMM of a chain: its operands, epilogue and activation buffer index.
+// Attention over the KV cache as a phase of the GEMM chain (bf16 caches, at
+// most 16 query vectors per sequence and KV head).  The key range of every
+// (sequence, KV head) is cut into units of 8 KB of K (4096 / hd slots); the
+// units of all pairs are split evenly over the CTAs.
+struct AttnPhase {
+    const float* q;          // [rows][H hd] queries, pre-scaled by 1/sqrt(hd)
+    void* out;               // [rows][H hd] bf16 hi rows, then lo rows at out_lo
+    size_t out_lo;
+    RowPlan plan;
+    int batch, kv_batch, kv_ctx, layer;
+    int n_heads, n_kv_heads, head_dim;
+    int tree;
+    int linear;              // every segment has <= 4 query vectors: K/V arrive by plain bulk copies
+                             // (rows in order) instead of swizzled tensor boxes
+    const void* kc;          // cache bases (bulk copies)
+    const void* vc;
+    float* part;             // [CTAs][2][16][hd + 2] partial softmax states
+    int* counters;           // [batch * n_kv_heads] arrivals (zero between launches)
+    int* err;
+    unsigned long long* kv_bytes;   // nullable: K/V bytes read are added here (profiling)
+};
+
+enum PhaseKind { PH_GEMM = 0, PH_ATTN = 1 };
+constexpr int kAttnMaxQ = 16;    // attention phase: query vectors per (sequence, KV head)
+constexpr int kAttnSimtQ = 4;    // up to this many: CUDA-core path, else tensor-core MMAs
+
+// One step of a chain: a GEMM (operands, epilogue, activation buffer index)
+// or an attention phase.
 struct GemmStep {
     GemmLaunch g;
     EpiParams e;
     int xbuf;
+    int kind = PH_GEMM;
+    AttnPhase at{};
 };
 // Runs the GEMMs in order.  bf16 models with every step on the same rows
 // (T <= kMaxTPad) run them in one launch separated by grid barriers.
 int launch_gemm_chain(spec_model* m, const GemmStep* steps, int n, cudaStream_t st);
+// Attention phase usable for this launch (bf16, cache maps, <= 16 queries per
+// sequence and KV head, workspace large enough)?
+bool attn_phase_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq);
+size_t attn_phase_part_floats(const spec_model* m);
+bool make_kv_tmaps(spec_kv* kv);
 size_t gemm_partial_floats_needed(const spec_model* m, int N, int K, int T_pad);
 int gemm_grid(const spec_model* m, int N, int K);
 
