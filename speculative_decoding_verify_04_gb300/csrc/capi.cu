@@ -474,9 +474,6 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
         // (one launch per layer) instead of its own kernel
         const char* ae = getenv("SPEC_ATTN_PHASE");
         m->attn_phase = ae && ae[0] == '1';
-        // SPEC_L2_AHEAD=n: L2 lookahead of the GEMM chain producer, in units (0 turns it off)
-        const char* le = getenv("SPEC_L2_AHEAD");
-        if (le) m->l2_ahead = std::max(0, std::min(64, atoi(le)));
     }
     m->elem = m->bf16 ? 2 : 4;
     if (m->bf16) {

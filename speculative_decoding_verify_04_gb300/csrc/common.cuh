@@ -138,15 +138,6 @@ SPEC_DEV void tma_load_3d(void* dst, const CUtensorMap* map, int32_t x, int32_t 
            "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
-// bring a box into L2 ahead of its load (no shared memory, no completion)
-SPEC_DEV void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
-}
-SPEC_DEV void tma_prefetch_l2_3d(const CUtensorMap* map, int32_t x, int32_t y, int32_t z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
-                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z) : "memory");
-}
 // contiguous global -> shared copy (both 16-byte aligned, bytes a multiple of 16)
 SPEC_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
     asm volatile(

@@ -216,16 +216,27 @@ SPEC_DEV void apply_qkv(const EpiParams& e, int tile, int j0, int nr, EpiSmem& s
     }
 }
 
+// Residual rows of a chunk for this thread's feature (etid()): loaded ahead of
+// the accumulator so that the load is off the epilogue's critical path.
+SPEC_DEV void load_resid(const EpiParams& e, int tile, int j0, int nr, float (&hv)[kRowChunk]) {
+    const int n = tile * kTileN + etid();
+#pragma unroll
+    for (int j = 0; j < kRowChunk; ++j)
+        hv[j] = (j < nr && n < e.N) ? __ldcg(e.h + (size_t)(e.r0 + j0 + j) * e.d_model + n) : 0.f;
+}
+
 template <typename XT>
-SPEC_DEV void apply_resid(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
-    for (int idx = etid(); idx < nr * kTileN; idx += 128) {
-        const int j = idx >> 7, mm = idx & 127;
+SPEC_DEV void apply_resid(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm, const float (&hv)[kRowChunk]) {
+#pragma unroll
+    for (int j = 0; j < kRowChunk; ++j) {
+        if (j >= nr) break;
+        const int mm = etid();
         const int n = tile * kTileN + mm;
         float sq = 0.f;
         if (n < e.N) {
             const int r = e.r0 + j0 + j;
             const size_t o = (size_t)r * e.d_model + n;
-            const float hn = __ldcg(e.h + o) + sm.tile[j][mm];
+            const float hn = hv[j] + sm.tile[j][mm];
             e.h[o] = hn;
             store_act(static_cast<XT*>(e.x_next), o, e.x_next_lo, hn * e.gain_next[n]);
             sq = hn * hn;
@@ -286,10 +297,10 @@ SPEC_DEV void apply_head(const EpiParams& e, int tile, int j0, int nr, EpiSmem& 
 }
 
 template <typename XT>
-SPEC_DEV void apply_chunk(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
+SPEC_DEV void apply_chunk(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm, const float (&hv)[kRowChunk]) {
     switch (e.kind) {
         case EPI_QKV: apply_qkv<XT>(e, tile, j0, nr, sm); break;
-        case EPI_RESID: apply_resid<XT>(e, tile, j0, nr, sm); break;
+        case EPI_RESID: apply_resid<XT>(e, tile, j0, nr, sm, hv); break;
         case EPI_SWIGLU: apply_swiglu<XT>(e, tile, j0, nr, sm); break;
         default: apply_head(e, tile, j0, nr, sm); break;
     }
@@ -367,18 +378,20 @@ SPEC_DEV void head_tile_done(const EpiParams& e, int n_tiles, EpiSmem& sm) {
 // `release()` is called once every value has been read.
 template <typename XT, typename Loader>
 SPEC_DEV void finish_segment(const EpiParams& e, const Split& sp, int tile, int slot, int nc,
-                             EpiSmem& sm, Loader& ld) {
+                             EpiSmem& sm, Loader& ld, float (&hv)[kRowChunk], bool hv_ready) {
     const int mm = etid();
     const int nchunks = (e.T + kRowChunk - 1) / kRowChunk;
+    const bool resid = e.kind == EPI_RESID;
     float v[16];
     if (nc == 1) {
         for (int ch = 0; ch < nchunks; ++ch) {
+            if (resid && (ch > 0 || !hv_ready)) load_resid(e, tile, ch * kRowChunk, min(kRowChunk, e.T - ch * kRowChunk), hv);
             ld.load(ch, v);
             const int nr = min(kRowChunk, e.T - ch * kRowChunk);
 #pragma unroll
             for (int i = 0; i < 16; ++i) sm.tile[i][mm] = v[i];
             named_bar(1, 128);
-            apply_chunk<XT>(e, tile, ch * kRowChunk, nr, sm);
+            apply_chunk<XT>(e, tile, ch * kRowChunk, nr, sm, hv);
         }
         ld.release();
         head_tile_done(e, sp.n_tiles, sm);
@@ -401,6 +414,8 @@ SPEC_DEV void finish_segment(const EpiParams& e, const Split& sp, int tile, int 
     const float* base = sp.part + (size_t)tile * sp.max_slots * sp.T_pad * kTileN;
     for (int ch = 0; ch < nchunks; ++ch) {
         const int nr = min(kRowChunk, e.T - ch * kRowChunk);
+        // residual rows load alongside the partial slots (independent)
+        if (resid && (ch > 0 || !hv_ready)) load_resid(e, tile, ch * kRowChunk, nr, hv);
         float acc[kRowChunk];
 #pragma unroll
         for (int i = 0; i < kRowChunk; ++i) acc[i] = 0.f;
@@ -415,7 +430,7 @@ SPEC_DEV void finish_segment(const EpiParams& e, const Split& sp, int tile, int 
 #pragma unroll
         for (int i = 0; i < kRowChunk; ++i) sm.tile[i][mm] = acc[i];
         named_bar(1, 128);
-        apply_chunk<XT>(e, tile, ch * kRowChunk, nr, sm);
+        apply_chunk<XT>(e, tile, ch * kRowChunk, nr, sm, hv);
     }
     if (mm == 0) sp.counters[tile] = 0;
     head_tile_done(e, sp.n_tiles, sm);
@@ -432,7 +447,6 @@ struct TcLayout {
     uint32_t tmem_cols;
     int rows_pad;         // first row of the lo half in the X buffers
     uint32_t attn_bytes;  // AttnSmem when the chain has an attention phase, else 0
-    int l2_ahead;         // units the producer prefetches into L2 ahead of its loads
     int attn_slots;       // attention ring: all 16 KB slots (weight slots, activation region, spare)
     int attn_nb;          // of which in the activation-tile region
 };
@@ -515,6 +529,9 @@ SPEC_DEV bool grid_wait(const int* bar, int target, volatile int* abort_flag, in
     }
 }
 
+// ATTN: the chain may hold an attention phase (instantiated only then, so the
+// plain GEMM chains carry none of its code or registers).
+template <bool ATTN>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
     extern __shared__ uint8_t smem_raw[];
@@ -566,7 +583,8 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
     // the attention phase's unit table reads the row plan, which a kernel at
     // least two launches back wrote (every kernel of the stream triggers its
     // dependants only after its own wait, so that one has completed)
-    if (ch.attn >= 0 && warp == 4) attn_unit_table(ch.ph[ch.attn].at, as);
+    if constexpr (ATTN)
+        if (ch.attn >= 0 && warp == 4) attn_unit_table(ch.ph[ch.attn].at, as);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -595,53 +613,16 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
             };
             // what a phase reads from the previous phase (the previous kernel for
             // phase 0) waits for it; weight tiles and committed KV slots do not
-            bool dep0 = false;      // the previous kernel has completed
             auto dep_wait = [&](int p) -> bool {
-                if (p == 0) { pdl_wait(); dep0 = true; return true; }
+                if (p == 0) { pdl_wait(); return true; }
                 if (!grid_wait(ch.bar, G * p, abort_flag, err)) return false;
                 fence_proxy_async_global();     // the rows were written by other CTAs' epilogues
                 return true;
             };
-            // L2 lookahead: a second cursor walks the same units (across phases) l2_ahead
-            // units ahead of the loads and prefetches their weight / K / V boxes into
-            // L2, so that more bytes are in flight than the ring holds.  Units holding
-            // rows the previous kernel writes are skipped until it has completed.
-            auto range_of = [&](int q, long long& b0, long long& e0) {
-                if (ch.ph[q].kind == PH_ATTN) attn_range(as.prefix[ch.ph[q].at.batch], G, c, b0, e0);
-                else cta_units(ch.ph[q].sp, c, b0, e0);
-            };
-            int pf_p = 0;
-            long long pf_u, pf_e;
-            range_of(0, pf_u, pf_e);
-            auto prefetch_next = [&]() {
-                if (L.l2_ahead == 0) return;
-                while (pf_p < ch.n && pf_u >= pf_e)
-                    if (++pf_p < ch.n) range_of(pf_p, pf_u, pf_e);
-                if (pf_p >= ch.n) return;
-                const GemmPhase& Q = ch.ph[pf_p];
-                if (Q.kind == PH_ATTN) {
-                    const AttnPhase& A = Q.at;
-                    const AttnUnit au = attn_locate(as, A.batch, A.n_kv_heads, pf_u);
-                    const int ku = attn_keys_per_unit(A.head_dim);
-                    const int key0 = au.tile * ku;
-                    if (key0 + ku <= as.base[au.b] || (pf_p == 0 && dep0)) {
-                        const int row = (au.b * A.n_kv_heads + au.g) * A.kv_ctx + key0;
-                        for (int db = 0; db < A.head_dim / 64; ++db) {
-                            tma_prefetch_l2_3d(&Q.tmW, 64 * db, row, A.layer);
-                            tma_prefetch_l2_3d(&Q.tmX, 64 * db, row, A.layer);
-                        }
-                    }
-                } else {
-                    const int tile = (int)(pf_u / Q.sp.kb), kbi = (int)(pf_u % Q.sp.kb);
-                    tma_prefetch_l2_2d(&Q.tmW, kbi * kTileK, tile * kTileN);
-                }
-                ++pf_u;
-            };
-            for (int i = 0; i < L.l2_ahead; ++i) prefetch_next();
             for (int p = 0; ok && p < ch.n; ++p) {
                 P = &ch.ph[p];
                 n_def = 0;
-                if (P->kind == PH_ATTN) {
+                if (ATTN && P->kind == PH_ATTN) {
                     const AttnPhase& A = P->at;
                     long long ub, ue;
                     attn_range(as.prefix[A.batch], G, c, ub, ue);
@@ -690,7 +671,6 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                                 tma_load_3d(dst + (nbox + db) * box, &P->tmX, 64 * db, row, A.layer, fb, pw);
                             }
                         }
-                        prefetch_next();
                         ++a_issued;
                         if (++a_slot == R.n) { a_slot = 0; a_phase ^= 1u; }
                     }
@@ -728,7 +708,6 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                         def_kb[n_def] = kbi;
                         ++n_def;
                     }
-                    prefetch_next();
                     ++issued;
                     if (++stage == L.stages) { stage = 0; phase ^= 1u; }
                     if (++kbi == sp.kb) { kbi = 0; ++tile; }
@@ -813,10 +792,12 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                 named_bar(1, 128);
                 if (!w_ok) break;
             }
-            if (P.kind == PH_ATTN) {
+            if (ATTN && P.kind == PH_ATTN) {
                 const AttnPhase& A = P.at;
-                const bool a_ok = A.head_dim == 128 ? consume_attn<128>(A, as, R, c, G, abort_flag, err)
-                                                    : consume_attn<64>(A, as, R, c, G, abort_flag, err);
+                bool a_ok = false;
+                if constexpr (ATTN)
+                    a_ok = A.head_dim == 128 ? consume_attn<128>(A, as, R, c, G, abort_flag, err)
+                                             : consume_attn<64>(A, as, R, c, G, abort_flag, err);
                 if (etid() == 0) mbar_arrive(attn_done);     // all 128 threads are past their last unit
                 if (!a_ok) { ok = false; break; }
             } else {
@@ -829,6 +810,10 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                     const long long seg_end = min(ue, (long long)(tile + 1) * sp.kb);
                     const int first = cta_of(sp, (long long)tile * sp.kb);
                     const int last = cta_of(sp, (long long)(tile + 1) * sp.kb - 1);
+                    // the residual rows of the tile load while its accumulator is computed
+                    float hv[kRowChunk];
+                    const bool hv_ready = P.e.kind == EPI_RESID;
+                    if (hv_ready) load_resid(P.e, tile, 0, min(kRowChunk, P.e.T), hv);
                     // one thread waits (bounded) and broadcasts, so all 128 leave together
                     if (etid() == 0) sm.wait_ok = mbar_wait(acc_full, acc_phase, abort_flag, err) ? 1 : 0;
                     named_bar(1, 128);
@@ -837,7 +822,7 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                     if (!w_ok) { ok = false; break; }
                     acc_phase ^= 1u;
                     tc_fence_after();
-                    finish_segment<__nv_bfloat16>(P.e, sp, tile, c - first, last - first + 1, sm, ld);
+                    finish_segment<__nv_bfloat16>(P.e, sp, tile, c - first, last - first + 1, sm, ld, hv, hv_ready);
                     u = seg_end;
                 }
             }
@@ -931,7 +916,8 @@ gemm_f32_kernel(const float* __restrict__ W, const float* __restrict__ X, int x_
         const int first = cta_of(sp, (long long)tile * sp.kb);
         const int last = cta_of(sp, (long long)(tile + 1) * sp.kb - 1);
         SmemTileLoader ld{ws.acc};
-        finish_segment<float>(e, sp, tile, c - first, last - first + 1, sm, ld);
+        float hv[kRowChunk];
+        finish_segment<float>(e, sp, tile, c - first, last - first + 1, sm, ld, hv, false);
         __syncthreads();
         u = seg_end;
     }
@@ -971,7 +957,6 @@ static TcLayout tc_layout(int T_pad, int rows_pad, bool attn) {
     L.rows_pad = rows_pad;
     L.b_bytes = 2u * (uint32_t)T_pad * kTileK * 2;
     L.attn_bytes = attn ? (uint32_t)((sizeof(AttnSmem) + 15) & ~size_t(15)) : 0u;
-    L.l2_ahead = 0;
     const size_t budget = 225 * 1024 - 1024 - kBarBytes - kEpiSmemBytes - L.attn_bytes - 64;
     L.stages = (int)std::min<size_t>(kMaxStages, budget / (kATileBytes + L.b_bytes));
     uint32_t cols = 32;
@@ -1052,16 +1037,19 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
     ch.bar = chain_bar(m);
     ch.done = chain_done(m);
     TcLayout L = tc_layout(T_pad, m->max_rows_pad, ch.attn >= 0);
-    L.l2_ahead = m->l2_ahead;
     const size_t smem = tc_smem_bytes(L);
     if (smem > 227 * 1024) return set_error(SPEC_ERR_CAPACITY, "GEMM chain: shared memory layout too large");
     static bool attr_set = false;
     if (!attr_set) {
-        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         attr_set = true;
     }
     const int slot = prof_start(m, st);
-    launch_k(m->pdl, gemm_tc_kernel, dim3(G), dim3(kTcThreads), smem, st, ch, L);
+    if (ch.attn >= 0)
+        launch_k(m->pdl, gemm_tc_kernel<true>, dim3(G), dim3(kTcThreads), smem, st, ch, L);
+    else
+        launch_k(m->pdl, gemm_tc_kernel<false>, dim3(G), dim3(kTcThreads), smem, st, ch, L);
     ++m->launches;
     prof_stop(m, slot, st, PROF_GEMM, bytes);
     return check_cuda(cudaGetLastError(), "GEMM launch");

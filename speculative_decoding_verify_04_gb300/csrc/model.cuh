@@ -109,7 +109,6 @@ struct spec_model {
     bool pdl = true;                 // launch forward kernels with programmatic dependent launch
     bool chain = true;               // bf16: consecutive GEMMs of a layer share one launch
     bool attn_phase = false;         // bf16: attention as the first phase of the layer's chain (SPEC_ATTN_PHASE=1)
-    int l2_ahead = 0;                // bf16 chains: units prefetched into L2 ahead of the ring (0: off)
 
     // tracing: kernel launches issued, and (when enabled) CUDA events around
     // every GEMM / attention launch with the launch's algorithmic bytes
