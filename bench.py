@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers of the same shape (small case for profiler captures)")
     ap.add_argument("--exit-layer", type=int, default=None)
+    ap.add_argument("--workload", default="chain", choices=["chain", "adaptive"],
+                    help="chain: k=4, ctx 4096, batch 1 (or --batch); adaptive: batch 32, contexts 512..8192, "
+                         "per-sequence k in [2,16] from the confidence schedule")
     return ap.parse_args()
 
 
@@ -80,7 +83,7 @@ def peaks():
 
 # ---------------------------------------------------------------------------
 # CPU oracle timing (sampled round, scaled)
-def oracle_round_sample(batch, budget_s=20.0):
+def oracle_round_sample(batch, budget_s=20.0, k=K_DRAFT, ctx=CTX):
     """Time the float64 oracle on a bounded sample of one round and scale it.
 
     Sample: one decoder layer of the 7B shape with 1 row (a draft pass) and
@@ -98,15 +101,15 @@ def oracle_round_sample(batch, budget_s=20.0):
     shape = dataclasses.replace(SHAPES["llama7b"], n_layers=1, exit_layer=0)
     w = weights_to_numpy(make_weights(shape, SEED, device="cpu"))
     dec = Decoder(shape, w)
-    k, v = make_kv_context(shape, 1, CTX, SEED, device="cpu")
-    cache = dec.new_cache(CTX + K_DRAFT + 2)
-    cache.load(k[:, 0].float().numpy(), v[:, 0].float().numpy())
+    kc, vc = make_kv_context(shape, 1, ctx, SEED, device="cpu")
+    cache = dec.new_cache(ctx + k + 2)
+    cache.load(kc[:, 0].float().numpy(), vc[:, 0].float().numpy())
     rng = np.random.default_rng(0)
 
     def layer(rows):
         h = rng.standard_normal((rows, shape.d_model)) * 0.02
-        pos = CTX + np.arange(rows)
-        vis = [np.arange(CTX + r + 1) for r in range(rows)]
+        pos = ctx + np.arange(rows)
+        vis = [np.arange(ctx + r + 1) for r in range(rows)]
         t = time.perf_counter()
         dec.layer(0, h, pos, pos, vis, cache)
         return time.perf_counter() - t
@@ -117,8 +120,8 @@ def oracle_round_sample(batch, budget_s=20.0):
         dec.logits(h)
         return time.perf_counter() - t
 
-    t1, t5, h1, h5 = layer(1), layer(K_DRAFT + 1), head(1), head(K_DRAFT + 1)
-    per_seq = (K_DRAFT + 1) * 12 * t1 + K_DRAFT * h1 + 20 * t5 + h5
+    t1, t5, h1, h5 = layer(1), layer(k + 1), head(1), head(k + 1)
+    per_seq = (k + 1) * 12 * t1 + k * h1 + 20 * t5 + h5
     threads = torch.get_num_threads()
     try:
         import threadpoolctl
@@ -126,8 +129,8 @@ def oracle_round_sample(batch, budget_s=20.0):
         threads = max([i.get("num_threads", 1) for i in info] + [1])
     except Exception:
         pass
-    desc = (f"one 7B-shape layer at 1 and {K_DRAFT + 1} rows and the LM head at 1 and {K_DRAFT + 1} rows "
-            f"over a {CTX}-token context, scaled to a round (5x12 + 20 layer passes, 5 heads)")
+    desc = (f"one 7B-shape layer at 1 and {k + 1} rows and the LM head at 1 and {k + 1} rows "
+            f"over a {ctx}-token context, scaled to a round ({k + 1}x12 + 20 layer passes, {k + 1} heads)")
     return per_seq * batch, desc, threads
 
 
@@ -201,6 +204,176 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_max(x, dist, device):
+    """Max over ranks of a per-rank float: the job's time is its slowest rank's."""
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, seconds):
+    """Whole-job throughput: each of `world` ranks processed `units_per_rank` units
+    (independent replicas) within `seconds` (the slowest rank's time)."""
+    return world * units_per_rank / seconds
+
+
+ADAPTIVE = ("llama7b-shape layer-skip self-spec (draft 12/32 layers), batch 32, contexts U{512..8192}, "
+            "per-sequence k in [2,16] from the confidence schedule, greedy")
+B_ADAPT, K_MIN, K_MAX, K_START, EMA_START = 32, 2, 16, 2, 0.5
+
+
+def run_adaptive(args, spec, world, rank, local, dist):
+    """Adaptive-k rounds: every sequence verifies its own k_b + 1 rows; after
+    the fused acceptance, the per-row top-1 / top-2 probabilities feed the
+    schedule, which sets each sequence's next k on the device.  The host reads
+    the new k back each round (the next call's row counts): that round trip is
+    part of the step."""
+    import torch
+    from synthetic import SHAPES, make_weights, make_kv_context, make_tokens, make_ragged_contexts
+    shape = SHAPES["llama7b"]
+    B = B_ADAPT
+    steps, warm = args.steps, args.warmup
+    lens = [int(x) for x in make_ragged_contexts(B, 512, 8192, seed=5 + 1000 * rank)]
+    cap = max(lens) + (steps + warm + 2) * (K_MAX + 1) + 8
+    w = make_weights(shape, SEED + rank, device="cuda")
+    model = spec.Model(shape, w, max_rows=B * (K_MAX + 1), max_batch=B, max_position=cap + 8)
+    del w
+    torch.cuda.empty_cache()
+    kv = spec.KVCache(model, B, cap)
+    for b in range(B):
+        kc, vc = make_kv_context(shape, 1, lens[b], SEED * 1000 + rank * 100 + b, device="cuda")
+        kv.import_rows(b, 0, kc[:, 0].contiguous(), vc[:, 0].contiguous())
+        del kc, vc
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    kv.set_lengths(lens)
+
+    d = shape.d_model
+    R = B * (K_MAX + 1)
+    t0 = torch.from_numpy(make_tokens(B, shape.vocab, SEED, "t0")).cuda()
+    cand_buf = torch.empty(R, dtype=torch.int32, device="cuda")
+    hl_buf = torch.empty(R * d, dtype=torch.float32, device="cuda")
+    stats = torch.empty((R, 4), dtype=torch.float32, device="cuda")
+    probs = torch.empty((R, 2), dtype=torch.float64, device="cuda")
+    acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    kn = torch.empty(B, dtype=torch.int32, device="cuda")
+    conf = torch.empty(B, dtype=torch.float64, device="cuda")
+    ema = torch.full((B,), EMA_START, dtype=torch.float64, device="cuda")
+    k_cur = [K_START] * B
+    stream = torch.cuda.current_stream()
+    log = {"rows": 0, "accepted": 0, "verify_ms": 0.0, "kmax": 0}
+
+    def round_(timed):
+        kmax = max(k_cur)
+        n_rows = [k + 1 for k in k_cur]
+        T = sum(n_rows)
+        cand = cand_buf[:B * (kmax + 1)].view(B, kmax + 1)
+        hL = hl_buf[:B * (kmax + 1) * d].view(B, kmax + 1, d)
+        spec.spec_draft(model, kv, t0, kmax, cand, hL)
+        if timed:
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+        spec.spec_verify(model, kv, n_rows, cand, kmax + 1, h_in=hL, h_stride=kmax + 1, stats=stats[:T], acc_len=acc,
+                         next_tok=nxt)
+        if timed:
+            ev1.record(stream)
+        spec.spec_row_probs(stats[:T], probs[:T])
+        spec.spec_schedule_k(probs[:T], n_rows, acc, ema, kn, conf, min_k=K_MIN, max_k=K_MAX)
+        spec.kv_commit(kv, acc)
+        t0.copy_(nxt)
+        k_next = kn.tolist()                    # the next round's row counts (host)
+        if timed:
+            log["rows"] += T
+            log["accepted"] += int(acc.sum().item()) + B
+            log["verify_ms"] += ev0.elapsed_time(ev1)
+            log["kmax"] = max(log["kmax"], kmax)
+        k_cur[:] = k_next
+
+    for _ in range(warm):
+        round_(False)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = Clocks(local)
+    clocks.start()
+    n_launch0 = model.launch_count()
+    torch.cuda.synchronize()
+    tw0 = time.perf_counter()
+    for _ in range(steps):
+        round_(True)
+    torch.cuda.synchronize()
+    wall_s = time.perf_counter() - tw0
+    launches = model.launch_count() - n_launch0
+    clk = clocks.stop()
+    err = model.device_error()
+    if err:
+        raise SystemExit(f"device error word {err} set during the bench")
+    rows, accepted = log["rows"], log["accepted"]
+    verify_s = log["verify_ms"] / 1e3
+    model.profile(True)
+    for _ in range(min(steps, 5)):
+        round_(False)
+    torch.cuda.synchronize()
+    model.profile(False)
+    g_ms, g_bytes, g_n = model.profile_read(0)
+    if world > 1:
+        wall_s = reduce_max(wall_s, dist, "cuda")
+        verify_s = reduce_max(verify_s, dist, "cuda")
+    hbm, peak_kind = peaks()
+    g_avg_ms = g_ms / max(g_n, 1)
+    achieved = g_bytes / max(g_n, 1) / (g_avg_ms / 1e3) / 1e9 if g_n else None
+    # verify algorithmic bytes over the timed rounds: layers 12..31 + head weights per round, KV of layers 12..31
+    F, V = shape.d_ff, shape.vocab
+    layer_w = (4 * d * d + 3 * F * d) * 2
+    n_ver = shape.n_layers - shape.exit_layer
+    mean_ctx = sum(lens) / B + (steps + warm) * 0.5 * (K_START + 1)
+    verify_bytes = steps * (n_ver * layer_w + V * d * 2) + n_ver * 2 * shape.n_kv_heads * shape.head_dim * 2 * mean_ctx * B * steps
+    line = {
+        "metric": METRIC,
+        "value": job_rate(world, rows, wall_s),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm,
+        "ms_per_step": wall_s * 1e3 / steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded random-init weights and KV contexts; no dataset)",
+        "config": {"workload": ADAPTIVE, "batch": B, "k_range": [K_MIN, K_MAX], "ctx_range": [512, 8192],
+                   "ctx_mean": sum(lens) / B, "exit_layer": shape.exit_layer, "n_layers": shape.n_layers,
+                   "l2": "inputs larger than L2 (weights and ~45 GB of KV re-streamed each round)",
+                   "parallelism": "data parallel over sequences" if world > 1 else "single GPU"},
+        "accepted_tokens_per_s": job_rate(world, accepted, wall_s),
+        "rows_per_round": rows / steps,
+        "max_k_seen": log["kmax"],
+        "verify_ms": verify_s * 1e3 / steps,
+        "verify_candidate_tokens_per_s": job_rate(world, rows, verify_s),
+        "verify_hbm_gbs": verify_bytes / verify_s / 1e9,
+        "verify_hbm_frac": verify_bytes / verify_s / 1e9 / hbm,
+        "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel (every launch of an instrumented pass of 5 rounds)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": (achieved / hbm) if achieved else None,
+                     "traffic": None, "peak_source": peak_kind, "launches": g_n, "avg_launch_us": g_avg_ms * 1e3},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": {"value": job_rate(world, rows, wall_s), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 4 * B,
+                "note": "the timed rounds already read each round's k back to the host (the next call's row counts)"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        kbar = max(1, round(rows / steps / B) - 1)
+        sec, desc, thr = oracle_round_sample(B, k=kbar, ctx=int(sum(lens) / B))
+        line["cpu_baseline"] = {"value": B * (kbar + 1) / sec, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -219,6 +392,8 @@ def main():
     __graft_entry__.build()
     from speculative_decoding_verify_04_gb300 import spec
     from synthetic import SHAPES, make_weights, make_kv_context, make_tokens
+    if args.workload == "adaptive":
+        return run_adaptive(args, spec, world, rank, local, dist)
 
     import dataclasses
     shape = SHAPES["llama7b"]
@@ -297,9 +472,8 @@ def main():
     if err:
         raise SystemExit(f"device error word {err} set during the bench")
     if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
+        ms = reduce_max(ms, dist, "cuda")
+        verify_ms = reduce_max(verify_ms, dist, "cuda")
 
     # e2e: the same rounds through the public API with the round's input (t0)
     # copied in from pinned host memory and its result read back each step
@@ -322,11 +496,13 @@ def main():
         torch.cuda.synchronize()
         t0_host.copy_(res_host[:, k + 2])
     e2e_s = (time.perf_counter() - tw0) / e_steps
-    e2e_val = world * B * (k + 1) / e2e_s
+    if world > 1:
+        e2e_s = reduce_max(e2e_s, dist, "cuda")
+    e2e_val = job_rate(world, B * (k + 1), e2e_s)
 
     hbm, peak_kind = peaks()
     cand_per_step = B * (k + 1)
-    value = world * cand_per_step * steps / (ms / 1e3)
+    value = job_rate(world, cand_per_step * steps, ms / 1e3)
     g_avg_ms = g_ms / max(g_n, 1)
     g_avg_bytes = g_bytes / max(g_n, 1)
     achieved = g_avg_bytes / (g_avg_ms / 1e3) / 1e9 if g_n else None

@@ -470,10 +470,11 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
         // SPEC_CHAIN=0 launches every GEMM on its own
         const char* ce = getenv("SPEC_CHAIN");
         m->chain = !(ce && ce[0] == '0');
-        // SPEC_ATTN_PHASE=1 runs attention as the first phase of each layer's GEMM chain
-        // (one launch per layer) instead of its own kernel
+        // attention as the first phase of each layer's GEMM chain (one launch per layer) or as
+        // its own kernel: SPEC_ATTN_PHASE=1 / 0 forces either; by default the phase runs for calls
+        // of two or more sequences (measured faster there; the separate kernel is faster for one)
         const char* ae = getenv("SPEC_ATTN_PHASE");
-        m->attn_phase = ae && ae[0] == '1';
+        m->attn_phase = (ae && ae[0] == '1') ? 1 : ((ae && ae[0] == '0') ? 0 : -1);
     }
     m->elem = m->bf16 ? 2 : 4;
     if (m->bf16) {

@@ -118,7 +118,8 @@ size_t attn_phase_part_floats(const spec_model* m) {
 
 bool attn_phase_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq) {
     const int G = m->cfg.n_heads / m->cfg.n_kv_heads;
-    return m->attn_phase && kv->tmaps && max_rows_per_seq * G <= kAttnMaxQ && batch <= kMaxPlanBatch &&
+    const bool wanted = m->attn_phase == 1 || (m->attn_phase == -1 && batch >= 2);
+    return wanted && kv->tmaps && max_rows_per_seq * G <= kAttnMaxQ && batch <= kMaxPlanBatch &&
            m->attn_part_floats >= attn_phase_part_floats(m) && m->n_attn_counters >= batch * m->cfg.n_kv_heads;
 }
 

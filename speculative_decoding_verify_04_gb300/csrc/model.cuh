@@ -108,7 +108,8 @@ struct spec_model {
 
     bool pdl = true;                 // launch forward kernels with programmatic dependent launch
     bool chain = true;               // bf16: consecutive GEMMs of a layer share one launch
-    bool attn_phase = false;         // bf16: attention as the first phase of the layer's chain (SPEC_ATTN_PHASE=1)
+    int attn_phase = -1;             // bf16: attention as the first phase of each layer's chain:
+                                     // 1 always, 0 never, -1 for calls of two or more sequences
 
     // tracing: kernel launches issued, and (when enabled) CUDA events around
     // every GEMM / attention launch with the launch's algorithmic bytes
