@@ -53,24 +53,35 @@ def parse():
     return ap.parse_args()
 
 
-def gemm_traffic_per_launch():
-    """DRAM bytes of the average GEMM launch of a round, from the committed ncu
-    summary (profiles/gemm_tc_kernel.llama7b_shapes.md).  None if the summary is
-    absent or was taken on another version of the kernel source (its
-    gemm_cu_sha256 line differs from the current gemm.cu)."""
+GEMM_SOURCES = ("gemm.cu", "attn_phase.cuh", "common.cuh", "model.cuh", "stats.cuh")
+
+
+def gemm_source_sha256():
+    """Hash of the sources the chain GEMM kernel is compiled from."""
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "speculative_decoding_verify_04_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def gemm_traffic_per_launch(avg_launch_bytes):
+    """DRAM bytes of the average GEMM-chain launch of a round: the committed ncu
+    summary (profiles/gemm_tc_kernel.llama7b_shapes.md) gives DRAM bytes over
+    algorithmic bytes for the captured launches, applied to this run's average
+    algorithmic bytes per launch (the launches move weights in proportion).
+    None if the summary is absent or was taken on other kernel sources."""
     p = os.path.join(ROOT, "profiles", "gemm_tc_kernel.llama7b_shapes.md")
-    src = os.path.join(ROOT, "speculative_decoding_verify_04_gb300", "csrc", "gemm.cu")
     if not os.path.exists(p):
         return None
     fields = {}
     for line in open(p):
-        if ":" in line and line.split(":")[0] in ("traffic_bytes_per_avg_launch", "gemm_cu_sha256"):
+        if ":" in line and line.split(":")[0] in ("traffic_over_algorithmic", "gemm_sources_sha256"):
             k, v = line.split(":", 1)
             fields[k] = v.strip()
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if fields.get("gemm_cu_sha256") != sha or "traffic_bytes_per_avg_launch" not in fields:
+    if fields.get("gemm_sources_sha256") != gemm_source_sha256() or "traffic_over_algorithmic" not in fields:
         return None
-    return float(fields["traffic_bytes_per_avg_launch"])
+    return float(fields["traffic_over_algorithmic"]) * avg_launch_bytes
 
 
 def peaks():
@@ -540,9 +551,10 @@ def main():
                                "same rounds)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": (achieved / hbm) if achieved else None,
-                     "traffic": gemm_traffic_per_launch() if args.layers is None and B == 1 else None,
-                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, "
-                                       "profiles/gemm_tc_kernel.llama7b_shapes.md",
+                     "traffic": gemm_traffic_per_launch(g_avg_bytes) if args.layers is None and B == 1 else None,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over algorithmic bytes of "
+                                       "the captured chain launches (profiles/gemm_tc_kernel.llama7b_shapes.md) "
+                                       "times this run's algorithmic bytes per launch",
                      "peak_source": peak_kind, "launches": g_n, "avg_launch_us": g_avg_ms * 1e3,
                      "avg_launch_bytes": g_avg_bytes},
         "attention": {"launches": a_n, "total_ms_per_step": a_ms / steps},

@@ -299,7 +299,7 @@ SPEC_DEV void attn_unit_simt(const uint8_t* tile, const float* qs, int nq, int k
 #pragma unroll
     for (int ps = 0; ps < NP; ++ps) {
         const int ka = key0 + 32 * ps + lane;
-#pragma unroll(NQ > 4 ? 2 : NQ)
+#pragma unroll
         for (int q = 0; q < NQ; ++q) {
             if (q >= nq) { sc[q][ps] = -INFINITY; continue; }
             // this lane's share of the 32 slots' dot products (K re-read per query: few registers)
@@ -361,7 +361,7 @@ SPEC_DEV void attn_unit_simt(const uint8_t* tile, const float* qs, int nq, int k
     // O += P V; slots past the range may hold anything, so they read slot 0 (p is 0 there)
 #pragma unroll
     for (int ps = 0; ps < NP; ++ps) {
-#pragma unroll(NQ > 4 ? 8 : 32)
+#pragma unroll
         for (int j = 0; j < 32; ++j) {
             int key = 32 * ps + j;
             key = key < nvalid ? key : 0;
@@ -654,21 +654,15 @@ SPEC_DEV bool consume_attn(const AttnPhase& A, AttnSmem& S, const AttnRing& R, i
                 if (nq == 1)
                     attn_segment_simt<HD, 1, true>(A, S, R, ring, ub, su, seg_end, seg_first, base, n_keys, row0,
                                                    g, nq, Gq, abort_flag, err, kv_bytes);
-                else if (nq == 2)
-                    attn_segment_simt<HD, 2, true>(A, S, R, ring, ub, su, seg_end, seg_first, base, n_keys, row0,
-                                                   g, nq, Gq, abort_flag, err, kv_bytes);
                 else
-                    attn_segment_simt<HD, 4, true>(A, S, R, ring, ub, su, seg_end, seg_first, base, n_keys, row0,
+                    attn_segment_simt<HD, 2, true>(A, S, R, ring, ub, su, seg_end, seg_first, base, n_keys, row0,
                                                    g, nq, Gq, abort_flag, err, kv_bytes);
             } else {
                 if (nq == 1)
                     attn_segment_simt<HD, 1, false>(A, S, R, ring, ub, su, seg_end, seg_first, base, n_keys, row0,
                                                     g, nq, Gq, abort_flag, err, kv_bytes);
-                else if (nq == 2)
-                    attn_segment_simt<HD, 2, false>(A, S, R, ring, ub, su, seg_end, seg_first, base, n_keys, row0,
-                                                    g, nq, Gq, abort_flag, err, kv_bytes);
                 else
-                    attn_segment_simt<HD, 4, false>(A, S, R, ring, ub, su, seg_end, seg_first, base, n_keys, row0,
+                    attn_segment_simt<HD, 2, false>(A, S, R, ring, ub, su, seg_end, seg_first, base, n_keys, row0,
                                                     g, nq, Gq, abort_flag, err, kv_bytes);
             }
         } else {

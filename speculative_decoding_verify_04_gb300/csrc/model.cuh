@@ -231,7 +231,7 @@ struct AttnPhase {
     int batch, kv_batch, kv_ctx, layer;
     int n_heads, n_kv_heads, head_dim;
     int tree;
-    int linear;              // every segment has <= 4 query vectors: K/V arrive by plain bulk copies
+    int linear;              // every segment has <= kAttnSimtQ query vectors: K/V arrive by plain bulk copies
                              // (rows in order) instead of swizzled tensor boxes
     const void* kc;          // cache bases (bulk copies)
     const void* vc;
@@ -243,7 +243,7 @@ struct AttnPhase {
 
 enum PhaseKind { PH_GEMM = 0, PH_ATTN = 1 };
 constexpr int kAttnMaxQ = 16;    // attention phase: query vectors per (sequence, KV head)
-constexpr int kAttnSimtQ = 4;    // up to this many: CUDA-core path, else tensor-core MMAs
+constexpr int kAttnSimtQ = 2;    // up to this many: CUDA-core path, else tensor-core MMAs
 
 // One step of a chain: a GEMM (operands, epilogue, activation buffer index)
 // or an attention phase.

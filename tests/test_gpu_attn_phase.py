@@ -127,10 +127,10 @@ def test_attention_phase_tree_gqa():
 @pytest.mark.parametrize("n_rows", [[1] * 5, [2] * 5, [3] * 5, [4] * 5, [1, 5, 3, 2, 6]],
                          ids=["q2", "q4", "q6", "q8", "ragged"])
 def test_attention_phase_small_query_groups(n_rows):
-    """2 to 8 query vectors per (sequence, KV head) take the CUDA-core path over
-    plain row copies; a ragged batch with up to 12 takes the tensor-box layout,
-    its small segments the CUDA-core path and the others the MMA path.
-    Contexts below, at and past one unit, and over several units."""
+    """2 query vectors per (sequence, KV head) take the CUDA-core path over plain
+    row copies; 4 to 8 take the tensor-box layout and the MMA path; a ragged
+    batch with up to 12 mixes both paths over the tensor-box layout.  Contexts
+    below, at and past one unit, and over several units."""
     lib()
     lens = [5, 60, 64, 200, 700]
     cap = max(lens) + 16
