@@ -35,6 +35,18 @@ Readings where the pages are silent
 * Committed length after a round is s + a + 1 (the round's first row t0
   plus a accepted draft tokens); the emitted next token is not yet in the
   cache.  The page's own ``seq_len + i`` counts from a different origin.
+* Temperature: both distributions are softmax(logits / T) with one T on both
+  sides (self-speculative decoding page, §2.4 warns that unequal
+  temperatures bias the output without any visible error), computed in
+  float64 and rounded to float32.
+* Top-p: of the page's two options (§3.4) the second is taken -- the draft
+  distribution q stays whole, only the target p is truncated to its nucleus
+  and renormalised there, so the ratio test runs against the full q.  The
+  nucleus is the shortest run of tokens, in order of decreasing probability
+  with ties to the lower token id, whose mass reaches top_p.  Mass is counted
+  in the sampler's integer weights, so the cut is exact: with S = sum w and
+  top_p = m * 2^-24, the run stops at the first cumulative weight
+  >= ceil(m * S / 2^24).  top_p >= 1 keeps the whole row.
 """
 from __future__ import annotations
 
@@ -133,6 +145,45 @@ def sample_index(w, u):
     t = sample_threshold(S, uniform_to_int(u))
     c = np.cumsum(w, dtype=np.uint64)
     return int(np.searchsorted(c, np.uint64(t), side="right"))
+
+
+def probs_at(logits, temp):
+    """softmax(logits / temp) along the last axis: float64, rounded to float32."""
+    if not (np.isfinite(temp) and temp > 0.0):
+        raise ValueError(f"temperature must be positive, got {temp!r}")
+    z = np.asarray(logits, dtype=np.float64) / float(temp)
+    e = np.exp(z - z.max(axis=-1, keepdims=True))
+    return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+
+def top_p_keep(p_row, top_p):
+    """Nucleus of one float32 probability row as a boolean mask."""
+    p = np.asarray(p_row, dtype=np.float32)
+    V = p.shape[0]
+    if top_p >= 1.0:
+        return np.ones(V, dtype=bool)
+    m = uniform_to_int(top_p)
+    if m == 0:
+        raise ValueError("top_p must be positive")
+    w = int_weights(p)
+    S = int(w.sum(dtype=np.uint64))
+    t = (m * S + TWO24 - 1) >> 24                       # ceil(m * S / 2^24)
+    order = np.lexsort((np.arange(V), -p.astype(np.float64)))   # p descending, then id
+    keep = np.zeros(V, dtype=bool)
+    mass = 0
+    for x in order:
+        keep[x] = True
+        mass += int(w[x])
+        if mass >= t:
+            break
+    return keep
+
+
+def top_p_filter(p_row, top_p):
+    """The row restricted to its nucleus and renormalised (float64, rounded to float32)."""
+    keep = top_p_keep(p_row, top_p)
+    p = np.where(keep, np.asarray(p_row, dtype=np.float32).astype(np.float64), 0.0)
+    return (p / p.sum()).astype(np.float32)
 
 
 def ratio_accept(u, qx, px):

@@ -31,10 +31,9 @@ from __future__ import annotations
 
 import numpy as np
 
-from .accept import (accept_greedy_chain, accept_greedy_tree, argmax_lowest,
-                     commit_chain, commit_tree_moves, apply_moves, int_weights,
-                     sample_index, tree_depths)
-from .decoder import softmax
+from .accept import (accept_greedy_chain, accept_greedy_tree, accept_sampling_chain,
+                     argmax_lowest, commit_chain, commit_tree_moves, apply_moves,
+                     int_weights, probs_at, sample_index, top_p_filter, tree_depths)
 
 
 def draft(dec, cache, s, t0, k, temp=0.0, u_draft=None):
@@ -59,7 +58,7 @@ def draft(dec, cache, s, t0, k, temp=0.0, u_draft=None):
         if temp == 0.0:
             cur = argmax_lowest(lg)
         else:
-            q = softmax(lg / temp).astype(np.float32)
+            q = probs_at(lg, temp)
             qs.append(q)
             cur = sample_index(int_weights(q), u_draft[j])
         toks.append(cur)
@@ -124,6 +123,25 @@ def spec_round_greedy(dec, cache, t0, k):
     a, nxt = accept_greedy_chain(d, logits)
     cache.length = commit_chain(s, a)
     return list(d[:a]) + [nxt], a, nxt, logits
+
+
+def spec_round_sampling(dec, cache, t0, k, temp, top_p, u_draft, u):
+    """One sampling chain round at temperature ``temp``.
+
+    The draft samples d_{j+1} from q_j = softmax(draft logits / temp) with
+    ``u_draft[j]``; the target rows become p_j = softmax(target logits / temp),
+    truncated to their top-p nucleus; rejection sampling with ``u[0..k]``
+    decides (self-speculative decoding page, §2.4, §3.4, §4.3).  Returns
+    ``(emitted, a, next, draft_tokens, q, p, target_logits)`` and commits.
+    """
+    s = cache.length
+    L = dec.shape.exit_layer
+    d, hL, _, q = draft(dec, cache, s, t0, k, temp=temp, u_draft=u_draft)
+    logits = verify(dec, cache, s, hL, L)
+    p = np.stack([top_p_filter(r, top_p) for r in probs_at(logits, temp)])
+    a, nxt = accept_sampling_chain(p, q, d, u)
+    cache.length = commit_chain(s, a)
+    return list(d[:a]) + [nxt], a, nxt, d, q, p, logits
 
 
 def generate_greedy_spec(dec, prompt, n_new, k, max_ctx=None, log=None):

@@ -287,3 +287,105 @@ def test_mean_emitted_matches_overlap_product():
     want = np.array([expected_tokens_positional(beta[b]) for b in range(B)])
     var = np.var(emitted)
     assert abs(emitted.mean() - want.mean()) < 4 * np.sqrt(var / B) + 1e-9
+
+
+# -- temperature and top-p ----------------------------------------------------
+def test_probs_at_two_tokens_is_logistic():
+    """Two tokens: p0 = 1 / (1 + exp((l1 - l0) / T)) (closed form)."""
+    for l0, l1, T in [(0.3, -1.2, 1.0), (2.0, 2.5, 0.7), (-4.0, 3.0, 2.5), (1.0, 1.0, 0.3)]:
+        p = A.probs_at(np.array([l0, l1]), T)
+        want = 1.0 / (1.0 + np.exp((l1 - l0) / T))
+        assert abs(float(p[0]) - want) <= 2.0 ** -24 and abs(float(p[1]) - (1 - want)) <= 2.0 ** -24
+
+
+def test_probs_at_ratios_follow_temperature():
+    """p_x / p_y = exp((l_x - l_y) / T) up to float32 rounding of both."""
+    rng = np.random.default_rng(3)
+    lg = rng.standard_normal(50) * 2.0
+    for T in (0.5, 1.0, 1.7):
+        p = A.probs_at(lg, T).astype(np.float64)
+        for x, y in [(0, 1), (7, 30), (12, 49)]:
+            assert p[x] / p[y] == pytest.approx(np.exp((lg[x] - lg[y]) / T), rel=4e-7)
+        assert abs(p.sum() - 1.0) < 50 * 2.0 ** -24
+
+
+def test_probs_at_cold_temperature_is_one_hot():
+    lg = np.array([0.1, 0.4, 0.39, -2.0])
+    p = A.probs_at(lg, 1e-5)            # the nearest gap is 1000 temperatures
+    assert list(p) == [0.0, 1.0, 0.0, 0.0]
+    with pytest.raises(ValueError):
+        A.probs_at(lg, 0.0)
+
+
+def test_top_p_hand_example():
+    """0.4 + 0.3 reaches 0.5 and 0.4 alone does not: nucleus {1, 3}, renormalised 4/7, 3/7."""
+    p = np.array([0.1, 0.4, 0.2, 0.3], dtype=np.float32)
+    assert list(A.top_p_keep(p, 0.5)) == [False, True, False, True]
+    f = A.top_p_filter(p, 0.5)
+    np.testing.assert_allclose(f, [0.0, 4 / 7, 0.0, 3 / 7], rtol=2e-7, atol=0)
+    assert list(A.top_p_keep(p, 0.75)) == [False, True, True, True]
+    assert A.top_p_keep(p, 1.0).all()
+    np.testing.assert_array_equal(A.top_p_filter(p, 1.0), p / np.float32(p.astype(np.float64).sum()))
+
+
+def test_top_p_ties_go_to_lower_ids():
+    p = np.full(4, 0.25, dtype=np.float32)
+    assert list(A.top_p_keep(p, 0.5)) == [True, True, False, False]
+    assert list(A.top_p_keep(p, 0.5 + 2.0 ** -24)) == [True, True, True, False]
+    assert list(A.top_p_keep(p, 2.0 ** -24)) == [True, False, False, False]
+
+
+def test_top_p_smallest_keeps_the_argmax():
+    rng = np.random.default_rng(5)
+    p = _rand_rows(rng, 40, 1)[0]
+    keep = A.top_p_keep(p, 2.0 ** -24)
+    assert keep.sum() == 1 and keep[int(np.argmax(p))]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_top_p_nucleus_properties(seed):
+    """The nucleus is characterised without the oracle's sort: it is closed upward
+    (any token ranked above a kept one is kept), its exact mass fraction reaches
+    top_p, and dropping its lowest-ranked token falls below top_p."""
+    rng = np.random.default_rng(seed)
+    V = 8
+    for row in _rand_rows(rng, V, 20):
+        if seed == 3:
+            row[:3] = row[3]                                  # ties
+        w = [int(x) for x in A.int_weights(row)]
+        S = sum(w)
+        for m in rng.integers(1, TWO24, size=6):
+            top_p = float(np.float32(int(m) * 2.0 ** -24))
+            keep = A.top_p_keep(row, top_p)
+            K = [x for x in range(V) if keep[x]]
+            above = lambda y, x: row[y] > row[x] or (row[y] == row[x] and y < x)
+            for x in K:
+                assert all(keep[y] for y in range(V) if above(y, x))
+            goal = Fraction(int(m), TWO24)
+            assert Fraction(sum(w[x] for x in K), S) >= goal
+            last = max(K, key=lambda x: (-float(row[x]), x))
+            assert Fraction(sum(w[x] for x in K) - w[last], S) < goal
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_top_p_rejection_law_equals_nucleus(seed):
+    """Target truncated to its nucleus, draft left whole: the emitted token's law
+    is the renormalised nucleus (k = 1, V = 5, exact over all uniforms)."""
+    rng = np.random.default_rng(10 + seed)
+    V = 5
+    p_full = _rand_rows(rng, V, 2)
+    p = np.stack([A.top_p_filter(r, 0.7) for r in p_full])
+    assert (p[0] == 0).any()
+    q = _rand_rows(rng, V, 1)
+    first = [0.0] * V
+    for x in range(V):
+        qx = float(q[0, x])
+        keep_end = _first_true(lambda m: not A.ratio_accept(_u(m), q[0, x], p[0, x]))
+        first[x] += qx * keep_end / TWO24
+        if keep_end < TWO24:
+            law = _sampler_law_of(lambda m: A.accept_sampling_chain(p, q, [x], [_u(keep_end), _u(m)])[1], V)
+            for y in range(V):
+                first[y] += qx * (1 - keep_end / TWO24) * law[y]
+    tol = 4 * 2.0 ** -24 + V * 2.0 ** -30 + V * 2.0 ** -23
+    np.testing.assert_allclose(first, p[0].astype(np.float64), rtol=0, atol=tol)
+    assert all(first[y] == 0.0 for y in range(V) if p[0, y] == 0)

@@ -164,3 +164,41 @@ def test_tree_round_commit(tiny, prompt):
     tiny.prefill(fresh, np.concatenate([prompt, [t0, ar[1], ar[2]]]))
     for l in range(tiny.n_layers):
         np.testing.assert_allclose(cache.k[l][:s + 3], fresh.k[l][:s + 3], rtol=1e-9, atol=1e-11)
+
+
+@pytest.mark.parametrize("top_p", [1.0, 0.875])
+def test_sampling_round_at_cold_temperature_is_greedy(tiny, prompt, top_p):
+    """At a temperature far below every logit gap each softmax row is one-hot
+    (other weights floor to zero), so every draw is the argmax: the sampling
+    round emits exactly what the greedy round emits."""
+    k = 4
+    rng = np.random.default_rng(21)
+    for r in range(3):
+        cg, cs = tiny.new_cache(PROMPT_LEN + 40), tiny.new_cache(PROMPT_LEN + 40)
+        t0 = argmax_lowest(tiny.prefill(cg, prompt))
+        tiny.prefill(cs, prompt)
+        for _ in range(r + 1):
+            eg, ag, ng, lg = S.spec_round_greedy(tiny, cg, t0, k)
+            u_d = (rng.integers(0, 1 << 24, k) * 2.0 ** -24).astype(np.float32)
+            u = (rng.integers(0, 1 << 24, k + 1) * 2.0 ** -24).astype(np.float32)
+            es, as_, ns, d, q, p, ls = S.spec_round_sampling(tiny, cs, t0, k, 1e-9, top_p, u_d, u)
+            gaps = np.sort(ls, axis=1)[:, -1] - np.sort(ls, axis=1)[:, -2]
+            assert gaps.min() > 1e-6
+            assert (es, as_, ns) == (eg, ag, ng) and cs.length == cg.length
+            assert ((q == 0) | (q == 1)).all() and ((p == 0) | (p == 1)).all()
+            t0 = ng
+
+
+def test_sampling_round_keeps_identical_rows(tiny, prompt):
+    """Draft and target at the same temperature: a draft token whose q and p rows
+    agree there with u * q < p is kept; the round commits s + a + 1 and emits
+    the kept tokens plus the draw."""
+    k = 3
+    cache = tiny.new_cache(PROMPT_LEN + 16)
+    t0 = argmax_lowest(tiny.prefill(cache, prompt))
+    s = cache.length
+    u_d = np.array([0.5, 0.25, 0.75], dtype=np.float32)
+    u = np.zeros(k + 1, dtype=np.float32)              # u = 0: every q(x) > 0 is kept
+    em, a, nxt, d, q, p, _ = S.spec_round_sampling(tiny, cache, t0, k, 1.0, 1.0, u_d, u)
+    assert a == k and em == list(d) + [nxt] and cache.length == s + k + 1
+    assert (q[np.arange(k), d] > 0).all()
