@@ -186,6 +186,20 @@ int spec_prefill(spec_model* m, spec_kv* kv, int32_t seq, const int32_t* tokens,
 int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0, int32_t k,
                int32_t* cand, float* h_L, float* draft_logits, void* stream);
 
+/* Sampling layer-skip draft ("self-speculative decoding" page, sections 2.4
+ * and 4.2): as spec_draft, but d_{j+1} is drawn from q_j = softmax(draft
+ * logits / temperature) with the integer inverse-CDF sampler of spec_sample
+ * driven by u_draft[b][j].
+ *   temperature  > 0, finite; the verifier's p must use the same value
+ *   u_draft  device f32 [batch][k], each m * 2^-24 with integer m in [0, 2^24)
+ *   q        device f32 [batch][k][V] out: the draft distributions (whole,
+ *            never top-p cut), the q of spec_accept
+ *   cand, h_L, draft_logits as for spec_draft (draft_logits nullable).
+ * batch <= max_batch; vocab <= 53248.  async. */
+int spec_draft_sample(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0, int32_t k,
+                      float temperature, const float* u_draft, int32_t* cand, float* h_L,
+                      float* q, float* draft_logits, void* stream);
+
 /* Verification forward of the candidate rows of sequences [0, batch).
  *   n_rows   host int32 [batch]: rows of sequence b (chain: k_b+1; tree:
  *            node count).  Sum <= max_rows, each <= 64.
@@ -216,16 +230,42 @@ int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows
 /* Rejection-sampling acceptance of a chain (no model needed).
  *   p      device f32 [batch][k+1][vocab]  target probabilities
  *   q      device f32 [batch][k][vocab]    draft probabilities
- *   draft  device int32 [batch][k]         draft tokens
+ *   draft  device int32 [batch][draft_stride]  draft tokens in columns 0..k-1
+ *          (draft_stride 0 means k; cand + 1 with stride k+1 reads the
+ *          draft tokens of spec_draft's candidate rows)
  *   u      device f32 [batch][k+1]         uniforms, each m * 2^-24, m in [0, 2^24)
  *   acc_len, next_tok  device int32 [batch] out
  * Ratio test u_j * q_j(x) < p_j(x) exactly (q_j(x) = 0 rejects); the draw
  * (residual max(0, p - q) in f32, or p when that is all zero, or the bonus
  * row p_k) is an integer inverse CDF over w = floor(r * 2^32) driven by
  * u[k].  Bit-exact and deterministic.  async. */
-int spec_accept(const float* p, const float* q, const int32_t* draft, const float* u,
-                int32_t batch, int32_t k, int32_t vocab, int32_t* acc_len,
+int spec_accept(const float* p, const float* q, const int32_t* draft, int32_t draft_stride,
+                const float* u, int32_t batch, int32_t k, int32_t vocab, int32_t* acc_len,
                 int32_t* next_tok, void* stream);
+
+/* Probability rows at a temperature, optionally cut to the top-p nucleus
+ * (self-speculative decoding page, sections 2.4 and 3.4: the target row is
+ * cut, the draft row stays whole).
+ *   logits   device f32, row r at logits + r * lg_stride (lg_stride >= vocab)
+ *   probs    device f32 out, row r at probs + r * p_stride
+ *   temperature > 0: probs = softmax(logits / temperature) in f32
+ *   top_p    >= 1: whole rows; else a multiple of 2^-24 in (0, 1): the row is
+ *            restricted to the shortest run of tokens, by decreasing
+ *            probability (ties to the lower id), whose integer weights
+ *            w = floor(p * 2^32) reach ceil(m * S / 2^24) (S = sum w,
+ *            top_p = m * 2^-24), then renormalised (zeros elsewhere).
+ * One CTA per row, the row in shared memory: vocab <= 53248.  Rows must be
+ * finite.  async. */
+int spec_probs(const float* logits, int64_t lg_stride, int32_t rows, int32_t vocab,
+               float temperature, float top_p, float* probs, int64_t p_stride, void* stream);
+
+/* One integer inverse-CDF draw per probability row: w = floor(r * 2^32),
+ * S = sum w, t = floor(m * S / 2^24) for u = m * 2^-24, token = smallest x
+ * whose inclusive prefix sum of w exceeds t (-1 for a row of zero weights).
+ *   probs device f32, row r at probs + r * p_stride; u device f32 [rows];
+ *   tokens device int32 [rows] out.  vocab <= 53248.  async. */
+int spec_sample(const float* probs, int64_t p_stride, int32_t rows, int32_t vocab,
+                const float* u, int32_t* tokens, void* stream);
 
 /* Greedy acceptance from target logits (the unfused form of spec_verify's
  * fused acceptance).  logits device f32 [batch][n_rows][vocab]; tokens device

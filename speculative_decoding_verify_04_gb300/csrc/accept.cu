@@ -36,7 +36,7 @@ SPEC_DEV float row_value(const float* p, const float* q, int x, int mode) {
 
 __global__ void __launch_bounds__(kAcceptThreads)
 accept_sample_kernel(const float* __restrict__ p, const float* __restrict__ q, const int* __restrict__ draft,
-                     const float* __restrict__ u, int k, int V, int* acc_len, int* next_tok) {
+                     int draft_stride, const float* __restrict__ u, int k, int V, int* acc_len, int* next_tok) {
     __shared__ unsigned long long step_sum[kAcceptWarps][kMaxSteps];
     __shared__ unsigned long long warp_tot[kAcceptWarps];
     __shared__ int s_a, s_mode, s_tok;
@@ -45,7 +45,7 @@ accept_sample_kernel(const float* __restrict__ p, const float* __restrict__ q, c
     if (w == 0) {
         bool rej = false;
         if (lane < k) {
-            const int x = draft[(size_t)b * k + lane];
+            const int x = draft[(size_t)b * draft_stride + lane];
             if (x < 0 || x >= V) {
                 rej = true;
             } else {
@@ -250,12 +250,15 @@ __global__ void row_probs_kernel(const spec_row_stats* __restrict__ st, int rows
 
 using namespace spec;
 
-extern "C" int spec_accept(const float* p, const float* q, const int32_t* draft, const float* u, int32_t batch,
-                           int32_t k, int32_t vocab, int32_t* acc_len, int32_t* next_tok, void* stream) {
+extern "C" int spec_accept(const float* p, const float* q, const int32_t* draft, int32_t draft_stride, const float* u,
+                           int32_t batch, int32_t k, int32_t vocab, int32_t* acc_len, int32_t* next_tok, void* stream) {
     if (!p || !q || !draft || !u || !acc_len || !next_tok) return set_error(SPEC_ERR_ARG, "spec_accept: null pointer");
     if (batch <= 0 || k < 1 || k > 32 || vocab <= 0) return set_error(SPEC_ERR_ARG, "spec_accept: bad sizes");
+    if (draft_stride == 0) draft_stride = k;
+    if (draft_stride < k) return set_error(SPEC_ERR_ARG, "spec_accept: draft_stride < k");
     if (vocab > kAcceptWarps * kMaxSteps * kStep) return set_error(SPEC_ERR_UNSUPPORTED, "spec_accept: vocab too large");
-    accept_sample_kernel<<<batch, kAcceptThreads, 0, (cudaStream_t)stream>>>(p, q, draft, u, k, vocab, acc_len, next_tok);
+    accept_sample_kernel<<<batch, kAcceptThreads, 0, (cudaStream_t)stream>>>(p, q, draft, draft_stride, u, k, vocab, acc_len,
+                                                                                 next_tok);
     return check_cuda(cudaGetLastError(), "spec_accept launch");
 }
 

@@ -586,6 +586,7 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
     const size_t w_err = take(64);
     const size_t w_pkv = take(64);
     const size_t w_plan = take((size_t)(4 * R + 3 * c.max_batch + 2 * kMaxSeqRows + 64) * 4);
+    const size_t w_dl = take((size_t)c.max_batch * V * 4);
     m->ws_bytes = off;
     if ((rc = check_cuda(cudaMalloc(&m->ws, off), "cudaMalloc(workspace)"))) return fail(rc);
     if ((rc = check_cuda(cudaMemsetAsync(m->ws, 0, off, st), "workspace clear"))) return fail(rc);
@@ -604,6 +605,7 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
     m->attn_counters = (int*)(S + w_ac);
     m->err = (int*)(S + w_err);
     m->prof_kv = (unsigned long long*)(S + w_pkv);
+    m->draft_lg = (float*)(S + w_dl);
     int* pl = (int*)(S + w_plan);
     m->plan.row_seq = pl; pl += R;
     m->plan.row_slot = pl; pl += R;
@@ -770,15 +772,17 @@ extern "C" int spec_prefill(spec_model* m, spec_kv* kv, int32_t seq, const int32
     return SPEC_OK;
 }
 
-extern "C" int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0, int32_t k, int32_t* cand,
-                          float* h_L, float* draft_logits, void* stream) {
-    if (!m || !kv || !t0 || !cand || !h_L) return set_error(SPEC_ERR_ARG, "spec_draft: null pointer");
-    if (kv->m != m) return set_error(SPEC_ERR_ARG, "spec_draft: cache of another model");
+// Draft passes; greedy (temp == 0: the LM head epilogue picks the argmax) or
+// sampling (the head writes logits, then one CTA per sequence forms
+// q = softmax(logits / temp) and draws the next token with u_draft).
+static int draft_impl(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0, int32_t k, int32_t* cand,
+                      float* h_L, float* draft_logits, float temp, const float* u_draft, float* q, cudaStream_t st) {
     const spec_model_config& c = m->cfg;
     if (c.exit_layer < 1) return set_error(SPEC_ERR_ARG, "spec_draft: exit_layer must be >= 1");
     if (batch < 1 || batch > kv->batch || batch > c.max_rows) return set_error(SPEC_ERR_ARG, "spec_draft: bad batch");
     if (k < 1 || k + 1 > kMaxSeqRows) return set_error(SPEC_ERR_ARG, "spec_draft: k must be in [1, 63]");
-    cudaStream_t st = (cudaStream_t)stream;
+    const bool sampling = temp > 0.f;
+    if (sampling && batch > c.max_batch) return set_error(SPEC_ERR_ARG, "spec_draft_sample: batch > max_batch");
     launch_k(m->pdl, set_col0_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, t0, cand, k + 1, batch);
     ++m->launches;
     SPEC_CUDA(cudaGetLastError(), "draft init");
@@ -790,11 +794,16 @@ extern "C" int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32
         SPEC_TRY(launch_plan(m, p, batch, kv->len, st));
         SPEC_TRY(launch_prologue(m, batch, nullptr, 0, cand, k + 1, j, 0, st));
         HeadSpec hs{};
-        hs.mode = HEAD_DRAFT;
+        hs.mode = sampling ? HEAD_STATS : HEAD_DRAFT;
         hs.T = batch;
         hs.r0 = 0;
-        hs.logits = draft_logits ? draft_logits + (size_t)j * c.vocab : nullptr;
-        hs.logits_stride = k * c.vocab;
+        if (draft_logits) {
+            hs.logits = draft_logits + (size_t)j * c.vocab;
+            hs.logits_stride = k * c.vocab;
+        } else if (sampling) {
+            hs.logits = m->draft_lg;
+            hs.logits_stride = c.vocab;
+        }
         hs.logits_row0 = 0;
         hs.cand = cand;
         hs.cand_stride = k + 1;
@@ -802,11 +811,45 @@ extern "C" int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32
         hs.batch = batch;
         // the LM head leaves the residual stream alone, so the layer-L state is copied after it
         SPEC_TRY(run_layers(m, kv, batch, batch, 1, 0, c.exit_layer, 0, j < k, j < k ? &hs : nullptr, st));
+        if (sampling && j < k) {
+            SampleArgs a{};
+            a.in = hs.logits;
+            a.in_stride = hs.logits_stride;
+            a.out = q + (size_t)j * c.vocab;
+            a.out_stride = (long long)k * c.vocab;
+            a.u = u_draft + j;
+            a.u_stride = k;
+            a.tok = cand + j + 1;
+            a.tok_stride = k + 1;
+            a.rows = batch;
+            a.V = c.vocab;
+            a.temp = temp;
+            a.err = m->err;
+            SPEC_TRY(launch_sample_rows(a, m->pdl, st));
+            ++m->launches;
+        }
         launch_k(m->pdl, copy_rows_kernel, dim3(batch), dim3(256), 0, st, (const float*)m->h, h_L, batch, c.d_model, k + 1, j);
         ++m->launches;
         SPEC_CUDA(cudaGetLastError(), "draft state copy");
     }
     return SPEC_OK;
+}
+
+extern "C" int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0, int32_t k, int32_t* cand,
+                          float* h_L, float* draft_logits, void* stream) {
+    if (!m || !kv || !t0 || !cand || !h_L) return set_error(SPEC_ERR_ARG, "spec_draft: null pointer");
+    if (kv->m != m) return set_error(SPEC_ERR_ARG, "spec_draft: cache of another model");
+    return draft_impl(m, kv, batch, t0, k, cand, h_L, draft_logits, 0.f, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+extern "C" int spec_draft_sample(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0, int32_t k,
+                                 float temperature, const float* u_draft, int32_t* cand, float* h_L, float* q,
+                                 float* draft_logits, void* stream) {
+    if (!m || !kv || !t0 || !cand || !h_L || !u_draft || !q) return set_error(SPEC_ERR_ARG, "spec_draft_sample: null pointer");
+    if (kv->m != m) return set_error(SPEC_ERR_ARG, "spec_draft_sample: cache of another model");
+    if (!(temperature > 0.f) || !(temperature <= 3.402823466e38f))
+        return set_error(SPEC_ERR_ARG, "spec_draft_sample: temperature must be positive and finite");
+    return draft_impl(m, kv, batch, t0, k, cand, h_L, draft_logits, temperature, u_draft, q, (cudaStream_t)stream);
 }
 
 extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows, const float* h_in,

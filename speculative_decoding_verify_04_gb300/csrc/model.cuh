@@ -58,6 +58,23 @@ struct GemmShape {
     int K;           // input features
 };
 
+
+// One CTA per row: softmax at a temperature (or rows given as probabilities),
+// optional top-p nucleus, optional integer inverse-CDF draw (sample.cu).
+constexpr int kSampMaxVocab = 53248;        // the row lives in shared memory (208 KB)
+struct SampleArgs {
+    const float* in; long long in_stride;   // logits (softmax) or probabilities (draw only)
+    float* out; long long out_stride;       // nullable: the row's probabilities
+    const float* u; int u_stride;           // nullable: uniform of row r at u[r * u_stride]
+    int* tok; int tok_stride;               // drawn token of row r at tok[r * tok_stride]
+    int rows, V;
+    float temp;                             // softmax at this temperature; <= 0: rows are probabilities
+    unsigned top_p_m;                       // 0: whole row; else the nucleus of top_p = m * 2^-24
+    int* err;                               // nullable device error word
+};
+
+int launch_sample_rows(const SampleArgs& a, bool pdl, cudaStream_t st);
+
 }  // namespace spec
 
 struct spec_model {
@@ -90,6 +107,7 @@ struct spec_model {
     float* ss_part = nullptr;        // [d/128][max_rows] per-tile sums of squares of h
     spec_row_stats* stat_part = nullptr;  // [ceil(V/128)][max_rows]
     spec_row_stats* row_stats = nullptr;  // [max_rows]
+    float* draft_lg = nullptr;       // [max_batch][V] draft logits of a sampling pass
     float* gemm_part = nullptr;      // split-K partial tiles
     size_t gemm_part_floats = 0;
     int* counters = nullptr;         // tile arrival counters, then chain barrier, chain exits, head tiles

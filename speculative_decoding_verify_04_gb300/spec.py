@@ -26,7 +26,7 @@ EXPORTS = [
     "spec_kv_create", "spec_kv_destroy", "spec_kv_set_lengths", "spec_kv_get_lengths", "spec_kv_import",
     "spec_kv_export", "spec_prefill", "spec_draft", "spec_verify", "spec_accept", "spec_accept_greedy",
     "kv_commit", "spec_row_probs", "spec_schedule_k", "spec_profile", "spec_profile_read", "spec_launch_count",
-    "spec_verify_noalloc",
+    "spec_verify_noalloc", "spec_draft_sample", "spec_probs", "spec_sample",
 ]
 
 
@@ -71,7 +71,10 @@ def load(path: str = LIB_PATH):
         "spec_prefill": ([P, P, I, P, I, P, P, P], I),
         "spec_draft": ([P, P, I, P, I, P, P, P, P], I),
         "spec_verify": ([P, P, I, POINTER(I), P, I, P, I, POINTER(I), P, P, P, P, P, P], I),
-        "spec_accept": ([P, P, P, P, I, I, I, P, P, P], I),
+        "spec_accept": ([P, P, P, I, P, I, I, I, P, P, P], I),
+        "spec_draft_sample": ([P, P, I, P, I, c_float, P, P, P, P, P, P], I),
+        "spec_probs": ([P, ctypes.c_int64, I, I, c_float, c_float, P, ctypes.c_int64, P], I),
+        "spec_sample": ([P, ctypes.c_int64, I, I, P, P, P], I),
         "spec_accept_greedy": ([P, P, POINTER(I), I, I, I, P, P, P, P], I),
         "kv_commit": ([P, I, P, P, I, P], I),
         "spec_row_probs": ([P, I, P, P], I),
@@ -242,6 +245,46 @@ def spec_draft(model, kv, t0, k, cand, h_L, draft_logits=None, stream=None):
                              _stream(stream)))
 
 
+def spec_draft_sample(model, kv, t0, k, temperature, u_draft, cand, h_L, q, draft_logits=None, stream=None):
+    """Sampling draft: d_{j+1} drawn from q_j = softmax(draft logits / temperature)
+    with ``u_draft[b, j]``; ``q`` [B, k, V] receives the draft distributions."""
+    B = t0.numel()
+    V = model.cfg.vocab
+    _need(t0, torch.int32, "t0")
+    _need(u_draft, torch.float32, "u_draft", B * k)
+    _need(cand, torch.int32, "cand", B * (k + 1))
+    _need(h_L, torch.float32, "h_L", B * (k + 1) * model.cfg.d_model)
+    _need(q, torch.float32, "q", B * k * V)
+    _need(draft_logits, torch.float32, "draft_logits", B * k * V)
+    _check(load().spec_draft_sample(model.handle, kv.handle, B, _ptr(t0), k, float(temperature), _ptr(u_draft),
+                                    _ptr(cand), _ptr(h_L), _ptr(q), _ptr(draft_logits), _stream(stream)))
+
+
+def _rows2d(t, name):
+    """A 2-D float32 CUDA view with unit inner stride: (pointer, rows, cols, row stride)."""
+    if t is None or not t.is_cuda or t.dtype != torch.float32 or t.dim() != 2 or t.stride(1) != 1:
+        raise SpecError(f"{name}: need a 2-D CUDA float32 tensor with contiguous rows")
+    return c_void_p(t.data_ptr()), t.shape[0], t.shape[1], t.stride(0)
+
+
+def spec_probs(logits, probs, temperature, top_p=1.0, stream=None):
+    """Rows of ``probs`` = softmax(logits / temperature), cut to the top-p nucleus
+    when ``top_p`` < 1 (a multiple of 2^-24).  Both are 2-D [rows, V] views."""
+    lp, rows, V, ls = _rows2d(logits, "logits")
+    pp, prow, pV, ps = _rows2d(probs, "probs")
+    if prow < rows or pV != V:
+        raise SpecError("probs: shape does not match logits")
+    _check(load().spec_probs(lp, ls, rows, V, float(temperature), float(top_p), pp, ps, _stream(stream)))
+
+
+def spec_sample(probs, u, tokens, stream=None):
+    """One integer inverse-CDF draw per row of ``probs`` [rows, V] with ``u`` [rows]."""
+    pp, rows, V, ps = _rows2d(probs, "probs")
+    _need(u, torch.float32, "u", rows)
+    _need(tokens, torch.int32, "tokens", rows)
+    _check(load().spec_sample(pp, ps, rows, V, _ptr(u), _ptr(tokens), _stream(stream)))
+
+
 def spec_verify(model, kv, n_rows, tokens, tok_stride, h_in=None, h_stride=0, tree_parent=None, logits=None,
                 stats=None, acc_len=None, next_tok=None, path=None, stream=None, _entry="spec_verify"):
     B = len(n_rows)
@@ -266,16 +309,20 @@ def spec_verify_noalloc(model, kv, n_rows, tokens, tok_stride, **kw):
 
 
 def spec_accept(p, q, draft, u, acc_len, next_tok, stream=None):
+    """Rejection-sampling acceptance.  ``draft`` is [B, k] with contiguous rows;
+    a column slice such as ``cand[:, 1:]`` of the draft's candidates works."""
     B, k1, V = p.shape
     k = k1 - 1
     _need(p, torch.float32, "p")
     _need(q, torch.float32, "q", B * k * V)
-    _need(draft, torch.int32, "draft", B * k)
+    if (not draft.is_cuda or draft.dtype != torch.int32 or draft.dim() != 2 or draft.shape[0] < B
+            or draft.shape[1] < k or draft.stride(1) != 1):
+        raise SpecError("draft: need a [B, k] CUDA int32 tensor with contiguous rows")
     _need(u, torch.float32, "u", B * (k + 1))
     _need(acc_len, torch.int32, "acc_len", B)
     _need(next_tok, torch.int32, "next_tok", B)
-    _check(load().spec_accept(_ptr(p), _ptr(q), _ptr(draft), _ptr(u), B, k, V, _ptr(acc_len), _ptr(next_tok),
-                              _stream(stream)))
+    _check(load().spec_accept(_ptr(p), _ptr(q), _ptr(draft), draft.stride(0), _ptr(u), B, k, V, _ptr(acc_len),
+                              _ptr(next_tok), _stream(stream)))
 
 
 def spec_accept_greedy(logits, tokens, acc_len, next_tok, tree_parent=None, path=None, stream=None):
