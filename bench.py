@@ -15,7 +15,12 @@ whole round time) -- with accepted tokens/s, the verify-step-only rate and the
 HBM roofline fraction of the dominant kernel (the tcgen05 GEMM) alongside.
 Weights and KV (> L2) are re-streamed every round, so no L2 flush is needed.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--impl reference]
+--mode sample runs sampling rounds instead: draft tokens drawn from
+softmax(draft logits / 0.8) with seeded uniforms (spec_draft_sample), target
+rows at the same temperature cut to their top-p 0.9 nucleus (spec_probs),
+rejection sampling (spec_accept) and kv_commit.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--mode greedy|sample] [--impl reference]
 """
 from __future__ import annotations
 
@@ -34,6 +39,7 @@ sys.path.insert(0, ROOT)
 METRIC = "verified candidate tokens/s and accepted tokens/s @1 GB300; % HBM roofline"
 WORKLOAD = "llama7b-shape layer-skip self-spec (draft 12/32 layers), chain k=4, ctx 4096, greedy"
 K_DRAFT, CTX, SEED = 4, 4096, 4
+TEMP, TOP_P = 0.8, 15099494 * 2.0 ** -24        # top-p 0.9 rounded down to a multiple of 2^-24
 
 
 def parse():
@@ -47,6 +53,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers of the same shape (small case for profiler captures)")
     ap.add_argument("--exit-layer", type=int, default=None)
+    ap.add_argument("--mode", default="greedy", choices=["greedy", "sample"],
+                    help="chain workload: greedy acceptance, or sampling at temperature 0.8 with top-p 0.9")
     ap.add_argument("--workload", default="chain", choices=["chain", "adaptive"],
                     help="chain: k=4, ctx 4096, batch 1 (or --batch); adaptive: batch 32, contexts 512..8192, "
                          "per-sequence k in [2,16] from the confidence schedule")
@@ -402,7 +410,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     from speculative_decoding_verify_04_gb300 import spec
-    from synthetic import SHAPES, make_weights, make_kv_context, make_tokens
+    from synthetic import SHAPES, make_weights, make_kv_context, make_tokens, make_uniforms
     if args.workload == "adaptive":
         return run_adaptive(args, spec, world, rank, local, dist)
 
@@ -436,12 +444,40 @@ def main():
     ev_v0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ev_v1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     acc_log = torch.zeros((steps, B), dtype=torch.int32, device="cuda")
+    sampling = args.mode == "sample"
+    V = shape.vocab
+    if sampling:
+        # every round's uniforms, resident before the timed region
+        n_rounds = warm + 2 * steps + 1
+        u_draft = torch.from_numpy(make_uniforms((n_rounds, B, k), SEED + rank, "u_draft")).cuda()
+        u_acc = torch.from_numpy(make_uniforms((n_rounds, B, k + 1), SEED + rank, "u_accept")).cuda()
+        q = torch.empty((B, k, V), dtype=torch.float32, device="cuda")
+        logits = torch.empty((B * (k + 1), V), dtype=torch.float32, device="cuda")
+        p = torch.empty_like(logits)
+    rnd = [0]
+
+    def draft(ud=None):
+        if sampling:
+            spec.spec_draft_sample(model, kv, t0, k, TEMP, ud, cand, hL, q)
+        else:
+            spec.spec_draft(model, kv, t0, k, cand, hL)
+
+    def verify(ua=None):
+        if sampling:
+            spec.spec_verify(model, kv, [k + 1] * B, cand, k + 1, h_in=hL, h_stride=k + 1, logits=logits)
+            spec.spec_probs(logits, p, TEMP, TOP_P)
+            spec.spec_accept(p.view(B, k + 1, V), q, cand[:, 1:], ua, acc, nxt)
+        else:
+            spec.spec_verify(model, kv, [k + 1] * B, cand, k + 1, h_in=hL, h_stride=k + 1, acc_len=acc,
+                             next_tok=nxt)
 
     def step(i=None):
-        spec.spec_draft(model, kv, t0, k, cand, hL)
+        j = rnd[0]
+        rnd[0] += 1
+        draft(u_draft[j] if sampling else None)
         if i is not None:
             ev_v0[i].record(stream)
-        spec.spec_verify(model, kv, [k + 1] * B, cand, k + 1, h_in=hL, h_stride=k + 1, acc_len=acc, next_tok=nxt)
+        verify(u_acc[j] if sampling else None)
         if i is not None:
             ev_v1[i].record(stream)
             acc_log[i].copy_(acc)
@@ -486,19 +522,30 @@ def main():
         ms = reduce_max(ms, dist, "cuda")
         verify_ms = reduce_max(verify_ms, dist, "cuda")
 
-    # e2e: the same rounds through the public API with the round's input (t0)
-    # copied in from pinned host memory and its result read back each step
+    # e2e: the same rounds through the public API with the round's inputs (t0,
+    # and in sampling mode its uniforms) copied in from pinned host memory and
+    # its result read back each step
     t0_host = torch.empty(B, dtype=torch.int32).pin_memory()
     res_host = torch.empty((B, k + 3), dtype=torch.int32).pin_memory()
     t0_host.copy_(t0.cpu())
     res_dev = torch.empty((B, k + 3), dtype=torch.int32, device="cuda")
     e_steps = max(3, steps // 2)
+    h2d = 4 * B
+    if sampling:
+        ud_host = make_uniforms((e_steps, B, k), SEED + rank, "u_draft_e2e")
+        ua_host = make_uniforms((e_steps, B, k + 1), SEED + rank, "u_accept_e2e")
+        ud_host, ua_host = torch.from_numpy(ud_host).pin_memory(), torch.from_numpy(ua_host).pin_memory()
+        ud_dev, ua_dev = torch.empty_like(u_draft[0]), torch.empty_like(u_acc[0])
+        h2d += 4 * B * k + 4 * B * (k + 1)
     torch.cuda.synchronize()
     tw0 = time.perf_counter()
-    for _ in range(e_steps):
+    for e in range(e_steps):
         t0.copy_(t0_host, non_blocking=True)
-        spec.spec_draft(model, kv, t0, k, cand, hL)
-        spec.spec_verify(model, kv, [k + 1] * B, cand, k + 1, h_in=hL, h_stride=k + 1, acc_len=acc, next_tok=nxt)
+        if sampling:
+            ud_dev.copy_(ud_host[e], non_blocking=True)
+            ua_dev.copy_(ua_host[e], non_blocking=True)
+        draft(ud_dev if sampling else None)
+        verify(ua_dev if sampling else None)
         spec.kv_commit(kv, acc)
         res_dev[:, :k + 1].copy_(cand)
         res_dev[:, k + 1].copy_(acc)
@@ -523,6 +570,8 @@ def main():
     n_ver = shape.n_layers - shape.exit_layer
     kv_bytes = n_ver * 2 * shape.n_kv_heads * shape.head_dim * 2 * (CTX + k + 1) * B
     verify_bytes = n_ver * layer_w + V * d * 2 + kv_bytes
+    workload = WORKLOAD if not sampling else WORKLOAD.replace(
+        "greedy", f"sampling (T {TEMP}, top-p {TOP_P:.7g}, rejection sampling)")
     line = {
         "metric": METRIC,
         "value": value,
@@ -536,7 +585,8 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded random-init weights and KV context; no dataset)",
-        "config": {"workload": WORKLOAD if args.layers is None else WORKLOAD + f" (reduced: {shape.n_layers} layers)",
+        "config": {"workload": workload if args.layers is None else workload + f" (reduced: {shape.n_layers} layers)",
+                   "mode": args.mode,
                    "batch": B, "k": k, "ctx": CTX, "exit_layer": shape.exit_layer, "n_layers": shape.n_layers,
                    "l2": "inputs larger than L2 (13.5 GB weights re-streamed each round)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -561,7 +611,7 @@ def main():
         "pdl": os.environ.get("SPEC_PDL", "1") != "0",
         "gpu_launches": launches,
         "clocks": clk,
-        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": 4 * B * (k + 3)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

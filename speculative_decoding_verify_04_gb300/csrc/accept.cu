@@ -1,138 +1,12 @@
-// Acceptance, KV commit and draft-length scheduling kernels.
-//
-// Rejection sampling ("self-speculative decoding" page, m.lqnn.cn/news/278124,
-// section 2.4 and the acceptance routine of section 4.3): draft token x at
-// position j is kept with probability min(1, p_j(x)/q_j(x)) -- zero when
-// q_j(x) = 0 -- tested as u_j * q_j(x) < p_j(x), exact in float64 because the
-// product of two float32 values has at most 48 significant bits.  At the first
-// rejection the correction is drawn from max(0, p_j - q_j) (clipped, section
-// 5.2), or from p_j when that residual is all zero; when all k are kept a bonus
-// token is drawn from p_k.  "Draw" is an integer inverse CDF so the result is
-// bit-exact on any machine: w_x = floor(r_x * 2^32) (an exact power-of-two
-// scaling of a float32), S = sum w (exact in 64 bits), t = floor(m * S / 2^24)
-// for the uniform u = m * 2^-24, and the token is the smallest x whose inclusive
-// prefix sum of w exceeds t.
+// Greedy acceptance (unfused form), KV commit and draft-length scheduling
+// kernels.  Rejection-sampling acceptance shares the row machinery of the
+// sampling kernels and lives beside them.
 #include <algorithm>
 
 #include "model.cuh"
 #include "stats.cuh"
 
 namespace spec {
-
-constexpr int kAcceptThreads = 256;
-constexpr int kAcceptWarps = kAcceptThreads / 32;
-constexpr int kStep = 128;                 // elements per warp step (32 lanes x 4)
-constexpr int kMaxSteps = 64;              // steps per warp segment (V <= 8*64*128 = 65536)
-
-SPEC_DEV unsigned long long weight_of(float r) {
-    return __float2ull_rz(r * 4294967296.0f);     // r in [0,1]: exact scaling, then floor
-}
-
-SPEC_DEV float row_value(const float* p, const float* q, int x, int mode) {
-    // mode 0: residual max(0, p - q); 1: p
-    if (mode == 0) return fmaxf(__fsub_rn(p[x], q[x]), 0.f);
-    return p[x];
-}
-
-__global__ void __launch_bounds__(kAcceptThreads)
-accept_sample_kernel(const float* __restrict__ p, const float* __restrict__ q, const int* __restrict__ draft,
-                     int draft_stride, const float* __restrict__ u, int k, int V, int* acc_len, int* next_tok) {
-    __shared__ unsigned long long step_sum[kAcceptWarps][kMaxSteps];
-    __shared__ unsigned long long warp_tot[kAcceptWarps];
-    __shared__ int s_a, s_mode, s_tok;
-    const int b = blockIdx.x, t = threadIdx.x, w = t >> 5, lane = t & 31;
-
-    if (w == 0) {
-        bool rej = false;
-        if (lane < k) {
-            const int x = draft[(size_t)b * draft_stride + lane];
-            if (x < 0 || x >= V) {
-                rej = true;
-            } else {
-                const float qx = q[((size_t)b * k + lane) * V + x];
-                const float px = p[((size_t)b * (k + 1) + lane) * V + x];
-                const float uj = u[(size_t)b * (k + 1) + lane];
-                rej = !(qx > 0.f && (double)uj * (double)qx < (double)px);
-            }
-        }
-        const unsigned mask = __ballot_sync(0xffffffffu, rej);
-        if (lane == 0) {
-            s_a = mask ? (__ffs(mask) - 1) : k;
-            s_mode = (s_a < k) ? 0 : 1;
-        }
-    }
-    __syncthreads();
-    const int a = s_a;
-    const float* pr = p + ((size_t)b * (k + 1) + a) * V;
-    const float* qr = (a < k) ? q + ((size_t)b * k + a) * V : nullptr;
-    const int seg = (V + kAcceptWarps - 1) / kAcceptWarps;
-    const int s0 = w * seg, s1 = min(V, s0 + seg);
-
-    unsigned long long S = 0;
-    for (int pass = 0; pass < 2; ++pass) {
-        const int mode = s_mode;
-        unsigned long long tot = 0;
-        for (int st = 0, base = s0; base < s1; base += kStep, ++st) {
-            unsigned long long ws = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int x = base + i * 32 + lane;
-                if (x < s1) ws += weight_of(row_value(pr, qr, x, mode));
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-            if (lane == 0) step_sum[w][st] = ws;
-            tot += ws;
-        }
-        if (lane == 0) warp_tot[w] = tot;
-        __syncthreads();
-        S = 0;
-        for (int i = 0; i < kAcceptWarps; ++i) S += warp_tot[i];
-        if (S != 0 || mode == 1) break;
-        __syncthreads();
-        if (t == 0) s_mode = 1;           // residual all zero: draw from p
-        __syncthreads();
-    }
-    const int mode = s_mode;
-    const unsigned long long m = (unsigned long long)(u[(size_t)b * (k + 1) + k] * 16777216.0f);
-    const unsigned long long thr = m * (S >> 24) + ((m * (S & 0xFFFFFFull)) >> 24);
-    // the warp whose segment holds the threshold
-    unsigned long long before = 0;
-    int ww = 0;
-    for (; ww < kAcceptWarps - 1; ++ww) {
-        if (before + warp_tot[ww] > thr) break;
-        before += warp_tot[ww];
-    }
-    if (w == ww) {
-        const int ws0 = ww * seg, ws1 = min(V, ws0 + seg);
-        int st = 0;
-        for (int base = ws0; base < ws1; base += kStep, ++st) {
-            if (before + step_sum[ww][st] > thr) break;
-            before += step_sum[ww][st];
-        }
-        const int base = ws0 + st * kStep;
-        int found = -1;
-        for (int i = 0; i < 4 && found < 0; ++i) {
-            const int x = base + i * 32 + lane;
-            unsigned long long wv = (x < ws1) ? weight_of(row_value(pr, qr, x, mode)) : 0ull;
-            unsigned long long inc = wv;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long nb = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += nb;
-            }
-            const unsigned hit = __ballot_sync(0xffffffffu, before + inc > thr);
-            if (hit) found = base + i * 32 + (__ffs(hit) - 1);
-            before += __shfl_sync(0xffffffffu, inc, 31);
-        }
-        if (lane == 0) s_tok = found;
-    }
-    __syncthreads();
-    if (t == 0) {
-        acc_len[b] = a;
-        next_tok[b] = s_tok;
-    }
-}
 
 // Unfused greedy acceptance: per sequence, row summaries from the logits then
 // the chain or tree rule.  The tree (parent and depth of each node) travels in
@@ -249,18 +123,6 @@ __global__ void row_probs_kernel(const spec_row_stats* __restrict__ st, int rows
 }  // namespace spec
 
 using namespace spec;
-
-extern "C" int spec_accept(const float* p, const float* q, const int32_t* draft, int32_t draft_stride, const float* u,
-                           int32_t batch, int32_t k, int32_t vocab, int32_t* acc_len, int32_t* next_tok, void* stream) {
-    if (!p || !q || !draft || !u || !acc_len || !next_tok) return set_error(SPEC_ERR_ARG, "spec_accept: null pointer");
-    if (batch <= 0 || k < 1 || k > 32 || vocab <= 0) return set_error(SPEC_ERR_ARG, "spec_accept: bad sizes");
-    if (draft_stride == 0) draft_stride = k;
-    if (draft_stride < k) return set_error(SPEC_ERR_ARG, "spec_accept: draft_stride < k");
-    if (vocab > kAcceptWarps * kMaxSteps * kStep) return set_error(SPEC_ERR_UNSUPPORTED, "spec_accept: vocab too large");
-    accept_sample_kernel<<<batch, kAcceptThreads, 0, (cudaStream_t)stream>>>(p, q, draft, draft_stride, u, k, vocab, acc_len,
-                                                                                 next_tok);
-    return check_cuda(cudaGetLastError(), "spec_accept launch");
-}
 
 extern "C" int spec_accept_greedy(const float* logits, const int32_t* tokens, const int32_t* tree_parent,
                                   int32_t batch, int32_t n_rows, int32_t vocab, int32_t* acc_len,
