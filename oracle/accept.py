@@ -18,7 +18,13 @@ Test infrastructure only.  Sources:
 * Commit / rollback: the cache keeps the accepted prefix only and its write
   pointer equals the committed length (self-speculative decoding page, §3.3).
 * Draft-length schedule: DSpark page §2.2 (confidence score) and §2.3 (linear
-  map with thresholds, clamped).
+  map with thresholds, clamped); optionally its §2.3 refinement: after a round
+  whose first draft token was rejected, k drops to its minimum at once.
+* Alternative schedules: the additive increase / decrease of the
+  self-speculative decoding page (§3.2: window of the last 64 rounds, k + 1
+  above 0.85 acceptance, k - 1 below 0.7, k in [2, 8]) and the linearly
+  shrinking K_t of the speculative decoding principles and practice page
+  (intelliparadigm.com/article/weixin_33702545/2059090, §3.3).
 
 Readings where the pages are silent
 -----------------------------------
@@ -32,6 +38,11 @@ Readings where the pages are silent
 * The residual max(0, p - q) is formed with one float32 subtraction.
 * u[k] (the last uniform of a sequence) drives whichever of the residual or
   bonus draw happens; u[0..k-1] drive the ratio tests.
+* Additive schedule: the window's acceptance is kept / drafted over the last
+  64 rounds (fewer at the start); crossing a threshold is read as being
+  beyond it after the round (every round while beyond, as congestion control
+  adds every round), strictly: exactly 0.85 or 0.7 leaves k unchanged.
+  The comparison is exact (integers against the thresholds as fractions).
 * Committed length after a round is s + a + 1 (the round's first row t0
   plus a accepted draft tokens); the emitted next token is not yet in the
   cache.  The page's own ``seq_len + i`` counts from a different origin.
@@ -51,6 +62,7 @@ Readings where the pages are silent
 from __future__ import annotations
 
 from dataclasses import dataclass
+from fractions import Fraction
 
 import numpy as np
 
@@ -255,6 +267,7 @@ class KSchedule:
     decay: float = 0.9
     k0: int = 2
     ema0: float = 0.5
+    first_reject_min: bool = False   # a round whose first draft token is rejected resets k to min_k
 
 
 def top12_probs(logits_row):
@@ -295,4 +308,47 @@ def schedule_update(ema, a, k, top1, top2, sch: KSchedule = KSchedule()):
         s1 = s1 + float(top1[i])
         sg = sg + (float(top1[i]) - float(top2[i]))
     c = confidence(s1 / n, sg / n, ema)
-    return next_k(c, sch), ema, c
+    k_next = next_k(c, sch)
+    if sch.first_reject_min and a == 0:
+        k_next = sch.min_k
+    return k_next, ema, c
+
+
+# -- alternative draft-length schedules ---------------------------------------
+@dataclass
+class AIMDSchedule:
+    """Additive increase / decrease of k from a sliding acceptance window
+    (self-speculative decoding page, §3.2, last paragraph)."""
+    window: int = 64
+    up: float = 0.85          # alpha above this: k + 1
+    down: float = 0.7         # alpha below this: k - 1
+    min_k: int = 2
+    max_k: int = 8
+
+
+def aimd_update(history, a, k, sch: AIMDSchedule = AIMDSchedule()):
+    """One round of the additive schedule for one sequence.
+
+    ``history`` is the list of ``(a_i, k_i)`` of earlier rounds (oldest
+    first); this round's ``(a, k)`` is appended and only the last
+    ``sch.window`` rounds are kept.  alpha = kept / drafted over the window.
+    Returns ``(k_next, history)``.
+    """
+    history = (list(history) + [(int(a), int(k))])[-sch.window:]
+    kept = sum(x for x, _ in history)
+    drafted = sum(y for _, y in history)
+    alpha = Fraction(kept, drafted)
+    k_next = k
+    if alpha > Fraction(sch.up).limit_denominator(1000):
+        k_next = k + 1
+    elif alpha < Fraction(sch.down).limit_denominator(1000):
+        k_next = k - 1
+    return max(sch.min_k, min(sch.max_k, k_next)), history
+
+
+def decay_k(t, T, k_max):
+    """K_t = max(1, round(K_max * (1 - t / T))) (speculative decoding principles
+    and practice page, intelliparadigm.com/article/weixin_33702545/2059090, §3.3): the
+    draft length shrinks as the generated count t nears the predicted total T.
+    float64 arithmetic; round is to the nearest integer, ties to even."""
+    return max(1, int(round(float(k_max) * (1.0 - float(t) / float(T)))))

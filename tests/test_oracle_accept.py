@@ -389,3 +389,60 @@ def test_top_p_rejection_law_equals_nucleus(seed):
     tol = 4 * 2.0 ** -24 + V * 2.0 ** -30 + V * 2.0 ** -23
     np.testing.assert_allclose(first, p[0].astype(np.float64), rtol=0, atol=tol)
     assert all(first[y] == 0.0 for y in range(V) if p[0, y] == 0)
+
+
+# -- alternative draft-length schedules ----------------------------------------
+def test_first_reject_resets_to_min():
+    """DSpark refinement: a round whose first draft token is rejected drops k to
+    min_k whatever the confidence; otherwise the linear map decides."""
+    sch = A.KSchedule(first_reject_min=True)
+    top1, top2 = [0.99] * 5, [0.001] * 5          # confidence high enough for max_k
+    k0, _, c0 = A.schedule_update(0.9, 0, 4, top1, top2, A.KSchedule())
+    k1, _, c1 = A.schedule_update(0.9, 0, 4, top1, top2, sch)
+    assert c0 == c1 and k0 > sch.min_k and k1 == sch.min_k
+    k2, _, _ = A.schedule_update(0.9, 1, 4, top1, top2, sch)
+    assert k2 == A.schedule_update(0.9, 1, 4, top1, top2, A.KSchedule())[0] > sch.min_k
+
+
+def test_aimd_hand_sequence():
+    """All kept: +1 a round up to 8; all rejected: the window's acceptance falls
+    below 0.7 after enough rounds, then -1 a round down to 2."""
+    h, k, ks = [], 2, []
+    for _ in range(8):
+        k, h = A.aimd_update(h, k, k)
+        ks.append(k)
+    assert ks == [3, 4, 5, 6, 7, 8, 8, 8]
+    # 8 rounds of 8/8 then rejections of k: window acceptance = kept / drafted
+    ks = []
+    for _ in range(6):
+        k, h = A.aimd_update(h, 0, k)
+        ks.append(k)
+    kept = sum(a for a, _ in h)
+    assert kept == 2 + 3 + 4 + 5 + 6 + 7 + 8 + 8
+    # acceptance after each rejection round: 43/(43+8), 43/(43+16), 43/(43+23), ...
+    # 43/51 = 0.843 (keep), 43/59 = 0.729 (keep), 43/66 = 0.652 (-1) ...
+    assert ks[:3] == [8, 8, 7]
+    assert ks[-1] < 7
+
+
+def test_aimd_thresholds_are_strict_and_window_slides():
+    sch = A.AIMDSchedule(window=4)
+    # 17 of 20 kept is exactly 0.85: no change; 7 of 10 exactly 0.7: no change
+    k, h = A.aimd_update([(5, 5), (5, 5), (5, 5)], 2, 5, sch)
+    assert k == 5 and len(h) == 4
+    k, h = A.aimd_update([(5, 10), (2, 0)], 0, 0, A.AIMDSchedule(window=4, min_k=0))
+    assert k == 0          # 7/10 exactly: unchanged
+    # the window forgets: after 4 perfect rounds the early failures are gone
+    h = [(0, 8)] * 4
+    for _ in range(4):
+        k, h = A.aimd_update(h, 8, 8, A.AIMDSchedule(window=4))
+    assert h == [(8, 8)] * 4 and k == 8
+
+
+def test_decay_k_table():
+    """K_t = max(1, round(6 (1 - t/100))): halves round to even."""
+    want = {0: 6, 10: 5, 25: 4, 50: 3, 75: 2, 90: 1, 99: 1, 100: 1, 150: 1}
+    for t, k in want.items():
+        assert A.decay_k(t, 100, 6) == k, (t, A.decay_k(t, 100, 6))
+    assert A.decay_k(1, 8, 4) == 4          # 3.5 -> 4 (even)
+    assert A.decay_k(3, 8, 4) == 2          # 2.5 -> 2 (even)
