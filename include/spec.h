@@ -124,7 +124,21 @@ typedef struct spec_k_schedule {
     int32_t min_k, max_k;  /* clamp range of k                                   */
     double  low, high;     /* confidence thresholds mapped to min_k and max_k    */
     double  decay;         /* EMA decay of the acceptance rate                   */
+    int32_t first_reject_min;  /* nonzero: a round whose first draft token was
+                              rejected (acc_len 0) sets k to min_k (DSpark 2.3) */
 } spec_k_schedule;
+
+/* Additive increase / decrease of k over a sliding window ("self-speculative
+ * decoding" page, m.lqnn.cn/news/278124, section 3.2): alpha = kept / drafted
+ * draft tokens over the last `window` rounds; alpha > up -> k + 1, alpha <
+ * down -> k - 1 (strict, every round), clamped to [min_k, max_k].  The
+ * thresholds are exact fractions. */
+typedef struct spec_aimd_schedule {
+    int32_t window;              /* rounds in the window, 1..256                  */
+    int32_t min_k, max_k;
+    int32_t up_num, up_den;      /* e.g. 85 / 100                                 */
+    int32_t down_num, down_den;  /* e.g. 7 / 10                                   */
+} spec_aimd_schedule;
 
 /* Last error message of the calling thread ("" if none).  The string stays
  * valid until the next failing call on the same thread. */
@@ -303,6 +317,27 @@ int spec_row_probs(const spec_row_stats* stats, int32_t rows, double* out, void*
 int spec_schedule_k(const double* top_probs, const int32_t* n_rows, const int32_t* acc_len,
                     double* ema, int32_t batch, const spec_k_schedule* sch, int32_t* k_next,
                     double* conf, void* stream);
+
+/* One round of the additive schedule, sequences [0, batch):
+ *   acc_len  device int32 [batch]: draft tokens kept this round
+ *   k_cur    device int32 [batch]: draft length of this round
+ *   state    device int32 [batch][2 * window + 2]: each sequence's window
+ *            (count, next slot, kept[window], drafted[window]); zero it
+ *            before the first round
+ *   k_next   device int32 [batch] out.  async. */
+int spec_schedule_aimd(const int32_t* acc_len, const int32_t* k_cur, int32_t* state, int32_t batch,
+                       const spec_aimd_schedule* sch, int32_t* k_next, void* stream);
+
+/* Draft length shrinking with the generated count (speculative decoding
+ * principles and practice page, intelliparadigm.com/article/weixin_33702545/
+ * 2059090, section 3.3): k_next = max(1, round(k_max * (1 - t / T))) in
+ * float64, rounded to nearest with ties to even.
+ *   generated device int32 [batch]: t, tokens generated so far
+ *   total     device int32 [batch]: T, the predicted total (>= 1; smaller
+ *             values give 1)
+ *   k_next    device int32 [batch] out.  async. */
+int spec_schedule_decay(const int32_t* generated, const int32_t* total, int32_t batch, int32_t k_max,
+                        int32_t* k_next, void* stream);
 
 /* spec_verify without any device memory of its own per call: same arguments,
  * results and stream semantics as spec_verify.  This entry point has no

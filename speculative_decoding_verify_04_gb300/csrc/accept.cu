@@ -83,6 +83,7 @@ struct SchedParams {
     int n_rows[kMaxPlanBatch];
     int min_k, max_k;
     double low, high, decay;
+    int first_reject_min;
 };
 
 __global__ void schedule_kernel(const double* __restrict__ probs, const int* __restrict__ acc_len, double* ema,
@@ -106,9 +107,48 @@ __global__ void schedule_kernel(const double* __restrict__ probs, const int* __r
                                            __dsub_rn(sp.high, sp.low)));
     long long kk = (long long)lin;            // truncation toward zero
     kk = kk < sp.min_k ? sp.min_k : (kk > sp.max_k ? sp.max_k : kk);
+    if (sp.first_reject_min && acc_len[b] == 0) kk = sp.min_k;
     ema[b] = e;
     k_next[b] = (int)kk;
     if (conf_out) conf_out[b] = c;
+}
+
+// Additive schedule: one thread per sequence; its window lives in `state` as
+// [count, next slot, kept[W], drafted[W]].
+__global__ void aimd_kernel(const int* __restrict__ acc_len, const int* __restrict__ k_cur, int* state, int batch,
+                            spec_aimd_schedule sch, int* k_next) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= batch) return;
+    const int W = sch.window;
+    int* st = state + (size_t)b * (2 * W + 2);
+    int count = st[0], slot = st[1];
+    const int k = k_cur[b];
+    st[2 + slot] = acc_len[b];
+    st[2 + W + slot] = k;
+    slot = slot + 1 == W ? 0 : slot + 1;
+    count = count < W ? count + 1 : W;
+    st[0] = count;
+    st[1] = slot;
+    long long kept = 0, drafted = 0;
+    for (int i = 0; i < count; ++i) {
+        kept += st[2 + i];
+        drafted += st[2 + W + i];
+    }
+    int kn = k;
+    if (kept * sch.up_den > (long long)sch.up_num * drafted) kn = k + 1;
+    else if (kept * sch.down_den < (long long)sch.down_num * drafted) kn = k - 1;
+    k_next[b] = kn < sch.min_k ? sch.min_k : (kn > sch.max_k ? sch.max_k : kn);
+}
+
+__global__ void decay_kernel(const int* __restrict__ generated, const int* __restrict__ total, int batch, int k_max,
+                             int* k_next) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= batch) return;
+    const int T = total[b];
+    if (T < 1) { k_next[b] = 1; return; }
+    const double x = __dmul_rn((double)k_max, __dsub_rn(1.0, __ddiv_rn((double)generated[b], (double)T)));
+    const double r = rint(x);                       // nearest, ties to even
+    k_next[b] = r < 1.0 ? 1 : (int)r;
 }
 
 __global__ void row_probs_kernel(const spec_row_stats* __restrict__ st, int rows, double* out) {
@@ -198,6 +238,26 @@ extern "C" int spec_schedule_k(const double* top_probs, const int32_t* n_rows, c
     }
     sp.min_k = sch->min_k; sp.max_k = sch->max_k;
     sp.low = sch->low; sp.high = sch->high; sp.decay = sch->decay;
+    sp.first_reject_min = sch->first_reject_min;
     schedule_kernel<<<(batch + 127) / 128, 128, 0, (cudaStream_t)stream>>>(top_probs, acc_len, ema, sp, k_next, conf);
     return check_cuda(cudaGetLastError(), "spec_schedule_k launch");
+}
+
+extern "C" int spec_schedule_aimd(const int32_t* acc_len, const int32_t* k_cur, int32_t* state, int32_t batch,
+                                  const spec_aimd_schedule* sch, int32_t* k_next, void* stream) {
+    if (!acc_len || !k_cur || !state || !sch || !k_next) return set_error(SPEC_ERR_ARG, "spec_schedule_aimd: null pointer");
+    if (batch <= 0) return set_error(SPEC_ERR_ARG, "spec_schedule_aimd: bad batch");
+    if (sch->window < 1 || sch->window > 256 || sch->min_k < 1 || sch->max_k < sch->min_k || sch->up_den <= 0 ||
+        sch->down_den <= 0)
+        return set_error(SPEC_ERR_ARG, "spec_schedule_aimd: bad schedule");
+    aimd_kernel<<<(batch + 127) / 128, 128, 0, (cudaStream_t)stream>>>(acc_len, k_cur, state, batch, *sch, k_next);
+    return check_cuda(cudaGetLastError(), "spec_schedule_aimd launch");
+}
+
+extern "C" int spec_schedule_decay(const int32_t* generated, const int32_t* total, int32_t batch, int32_t k_max,
+                                   int32_t* k_next, void* stream) {
+    if (!generated || !total || !k_next) return set_error(SPEC_ERR_ARG, "spec_schedule_decay: null pointer");
+    if (batch <= 0 || k_max < 1) return set_error(SPEC_ERR_ARG, "spec_schedule_decay: bad sizes");
+    decay_kernel<<<(batch + 127) / 128, 128, 0, (cudaStream_t)stream>>>(generated, total, batch, k_max, k_next);
+    return check_cuda(cudaGetLastError(), "spec_schedule_decay launch");
 }

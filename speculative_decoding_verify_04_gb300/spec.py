@@ -26,7 +26,8 @@ EXPORTS = [
     "spec_kv_create", "spec_kv_destroy", "spec_kv_set_lengths", "spec_kv_get_lengths", "spec_kv_import",
     "spec_kv_export", "spec_prefill", "spec_draft", "spec_verify", "spec_accept", "spec_accept_greedy",
     "kv_commit", "spec_row_probs", "spec_schedule_k", "spec_profile", "spec_profile_read", "spec_launch_count",
-    "spec_verify_noalloc", "spec_draft_sample", "spec_probs", "spec_sample",
+    "spec_verify_noalloc", "spec_draft_sample", "spec_probs", "spec_sample", "spec_schedule_aimd",
+    "spec_schedule_decay",
 ]
 
 
@@ -41,7 +42,13 @@ class ModelConfig(ctypes.Structure):
 
 
 class KSchedule(ctypes.Structure):
-    _fields_ = [("min_k", c_int32), ("max_k", c_int32), ("low", c_double), ("high", c_double), ("decay", c_double)]
+    _fields_ = [("min_k", c_int32), ("max_k", c_int32), ("low", c_double), ("high", c_double), ("decay", c_double),
+                ("first_reject_min", c_int32)]
+
+
+class AIMDSchedule(ctypes.Structure):
+    _fields_ = [("window", c_int32), ("min_k", c_int32), ("max_k", c_int32), ("up_num", c_int32),
+                ("up_den", c_int32), ("down_num", c_int32), ("down_den", c_int32)]
 
 
 _lib = None
@@ -75,6 +82,8 @@ def load(path: str = LIB_PATH):
         "spec_draft_sample": ([P, P, I, P, I, c_float, P, P, P, P, P, P], I),
         "spec_probs": ([P, ctypes.c_int64, I, I, c_float, c_float, P, ctypes.c_int64, P], I),
         "spec_sample": ([P, ctypes.c_int64, I, I, P, P, P], I),
+        "spec_schedule_aimd": ([P, P, P, I, POINTER(AIMDSchedule), P, P], I),
+        "spec_schedule_decay": ([P, P, I, I, P, P], I),
         "spec_accept_greedy": ([P, P, POINTER(I), I, I, I, P, P, P, P], I),
         "kv_commit": ([P, I, P, P, I, P], I),
         "spec_row_probs": ([P, I, P, P], I),
@@ -350,16 +359,43 @@ def spec_row_probs(stats, out, rows=None, stream=None):
 
 
 def spec_schedule_k(top_probs, n_rows, acc_len, ema, k_next, conf=None, min_k=2, max_k=16, low=0.3, high=0.8,
-                    decay=0.9, stream=None):
+                    decay=0.9, first_reject_min=False, stream=None):
     B = len(n_rows)
     _need(top_probs, torch.float64, "top_probs", 2 * sum(n_rows))
     _need(acc_len, torch.int32, "acc_len", B)
     _need(ema, torch.float64, "ema", B)
     _need(k_next, torch.int32, "k_next", B)
     _need(conf, torch.float64, "conf", B)
-    sch = KSchedule(min_k, max_k, low, high, decay)
+    sch = KSchedule(min_k, max_k, low, high, decay, 1 if first_reject_min else 0)
     _check(load().spec_schedule_k(_ptr(top_probs), _i32_array(n_rows), _ptr(acc_len), _ptr(ema), B,
                                   ctypes.byref(sch), _ptr(k_next), _ptr(conf), _stream(stream)))
+
+
+def aimd_state(batch, window=64, device="cuda"):
+    """Zeroed per-sequence window state for spec_schedule_aimd."""
+    return torch.zeros((batch, 2 * window + 2), dtype=torch.int32, device=device)
+
+
+def spec_schedule_aimd(acc_len, k_cur, state, k_next, window=64, min_k=2, max_k=8, up=(85, 100), down=(7, 10),
+                       stream=None):
+    """Additive increase / decrease of k over the last ``window`` rounds."""
+    B = acc_len.numel()
+    _need(acc_len, torch.int32, "acc_len", B)
+    _need(k_cur, torch.int32, "k_cur", B)
+    _need(state, torch.int32, "state", B * (2 * window + 2))
+    _need(k_next, torch.int32, "k_next", B)
+    sch = AIMDSchedule(window, min_k, max_k, up[0], up[1], down[0], down[1])
+    _check(load().spec_schedule_aimd(_ptr(acc_len), _ptr(k_cur), _ptr(state), B, ctypes.byref(sch), _ptr(k_next),
+                                     _stream(stream)))
+
+
+def spec_schedule_decay(generated, total, k_max, k_next, stream=None):
+    """k_next = max(1, round(k_max * (1 - generated / total))), ties to even."""
+    B = generated.numel()
+    _need(generated, torch.int32, "generated", B)
+    _need(total, torch.int32, "total", B)
+    _need(k_next, torch.int32, "k_next", B)
+    _check(load().spec_schedule_decay(_ptr(generated), _ptr(total), B, int(k_max), _ptr(k_next), _stream(stream)))
 
 
 def stats_argmax(stats):
