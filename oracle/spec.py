@@ -66,6 +66,85 @@ def draft(dec, cache, s, t0, k, temp=0.0, u_draft=None):
     return toks, np.stack(hs), lgs, (np.stack(qs) if qs else None)
 
 
+def top_children(row, c):
+    """The ``c`` highest-logit token ids of a row, best first, ties to the lower id."""
+    z = np.asarray(row, dtype=np.float64)
+    order = np.lexsort((np.arange(z.shape[0]), -z))
+    return [int(x) for x in order[:c]]
+
+
+def draft_tree(dec, cache, s, t0, parents):
+    """Layer-skip draft of a level-order token tree at committed length ``s``.
+
+    The root is ``t0``; level by level, the nodes of the current level run
+    layers [0, L) (node i in slot s + i at position s + depth(i), seeing the
+    committed context, its ancestors and itself) and the shared LM head, and
+    the children of node i take the best draft tokens of i's row in order:
+    the k-th child (by node index) gets the k-th highest logit (FlashSpec page,
+    lnrk.cn/news/47842, §2.2 and §6.2: a tree of candidates from the draft's
+    top choices; self-speculative decoding page §2.1: the first L layers and
+    the LM head are the draft).  A last pass runs layers [0, L) on the deepest
+    level without the head so that every node has its layer-L state.
+    Returns ``(tokens[n], h_L[n, d], draft_logits[n, V] (rows of the nodes
+    that have children, else zero))``.
+    """
+    L = dec.shape.exit_layer
+    n = len(parents)
+    depth = tree_depths(parents)
+    vis_all = tree_visibility(s, parents)
+    tokens = [0] * n
+    tokens[0] = int(t0)
+    hs = np.zeros((n, dec.shape.d_model))
+    lgs = np.zeros((n, dec.shape.vocab))
+    for lev in range(int(depth.max()) + 1):
+        nodes = [i for i in range(n) if depth[i] == lev]
+        h = dec.embed([tokens[i] for i in nodes])
+        h = dec.run_layers(h, 0, L, [s + lev] * len(nodes), [s + i for i in nodes], [vis_all[i] for i in nodes],
+                           cache)
+        for r, i in enumerate(nodes):
+            hs[i] = h[r]
+        kids = {i: [c for c in range(n) if parents[c] == i] for i in nodes}
+        if not any(kids.values()):
+            break
+        lg = dec.logits(h)
+        for r, i in enumerate(nodes):
+            if kids[i]:
+                lgs[i] = lg[r]
+                for c, tok in zip(kids[i], top_children(lg[r], len(kids[i]))):
+                    tokens[c] = tok
+    return tokens, hs, lgs
+
+
+def tree_round_layerskip(dec, cache, t0, parents):
+    """One greedy round of the layer-skip tree: draft_tree, layers [L, N) over
+    every node (tree mask), greedy tree acceptance, commit of the path.
+    Returns ``(emitted, depth, path, next, tokens, target_logits)``."""
+    s = cache.length
+    L = dec.shape.exit_layer
+    tokens, hL, _ = draft_tree(dec, cache, s, t0, parents)
+    logits = verify(dec, cache, s, hL, L, parents=parents)
+    depth, node, path, nxt = accept_greedy_tree(tokens, parents, logits)
+    moves, new_len = commit_tree_moves(s, path)
+    apply_moves(cache, moves)
+    cache.length = new_len
+    return [tokens[i] for i in path[1:]] + [nxt], depth, path, nxt, tokens, logits
+
+
+def generate_greedy_tree_spec(dec, prompt, n_new, parents, max_ctx=None, log=None):
+    """Greedy decoding by layer-skip tree rounds; equals :func:`generate_greedy_ar`."""
+    n = len(parents)
+    cache = dec.new_cache(max_ctx or (len(prompt) + n_new + n + 2))
+    t0 = argmax_lowest(dec.prefill(cache, prompt))
+    out = [t0]
+    while len(out) < n_new:
+        s = cache.length
+        emitted, depth, _, t0, _, _ = tree_round_layerskip(dec, cache, t0, parents)
+        out += emitted
+        if log is not None:
+            log.append((s, depth))
+    return out[:n_new]
+
+
 def chain_visibility(s, T):
     return [np.arange(0, s + t + 1) for t in range(T)]
 

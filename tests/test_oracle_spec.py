@@ -202,3 +202,54 @@ def test_sampling_round_keeps_identical_rows(tiny, prompt):
     em, a, nxt, d, q, p, _ = S.spec_round_sampling(tiny, cache, t0, k, 1.0, 1.0, u_d, u)
     assert a == k and em == list(d) + [nxt] and cache.length == s + k + 1
     assert (q[np.arange(k), d] > 0).all()
+
+
+# -- layer-skip token trees ----------------------------------------------------
+def test_top_children_order_and_ties():
+    row = np.array([0.5, 2.0, -1.0, 2.0, 0.7, 2.0])
+    assert S.top_children(row, 1) == [1]
+    assert S.top_children(row, 4) == [1, 3, 5, 4]
+
+
+@pytest.fixture(scope="module")
+def deep():
+    shape = ModelShape(4, 64, 4, 2, 16, 128, 96, 2, "f32", init_std=0.2)
+    return Decoder(shape, weights_to_numpy(make_weights(shape, seed=8)))
+
+
+def test_unit_branching_tree_draft_is_chain_draft(deep):
+    pr = make_tokens(10, deep.shape.vocab, seed=8)
+    k = 4
+    c1, c2 = deep.new_cache(32), deep.new_cache(32)
+    t0 = argmax_lowest(deep.prefill(c1, pr))
+    deep.prefill(c2, pr)
+    d, hL, lg, _ = S.draft(deep, c1, c1.length, t0, k)
+    toks, hs, lgs = S.draft_tree(deep, c2, c2.length, t0, tree_parents([1] * k))
+    assert toks == [t0] + list(d)
+    np.testing.assert_array_equal(hs, hL)
+    np.testing.assert_array_equal(lgs[:k], lg)
+    for l in range(deep.shape.exit_layer):
+        np.testing.assert_array_equal(c1.k[l][:c1.length + k + 1], c2.k[l][:c2.length + k + 1])
+
+
+def test_tree_draft_children_are_the_parents_best_tokens(deep):
+    pr = make_tokens(10, deep.shape.vocab, seed=9)
+    par = tree_parents([3, 2, 2])
+    c = deep.new_cache(64)
+    t0 = argmax_lowest(deep.prefill(c, pr))
+    toks, hs, lgs = S.draft_tree(deep, c, c.length, t0, par)
+    for i in range(len(par)):
+        kids = [j for j in range(len(par)) if par[j] == i]
+        if kids:
+            got = [toks[j] for j in kids]
+            assert len(set(got)) == len(got) and got[0] == argmax_lowest(lgs[i])
+            assert all(lgs[i][got[m]] >= lgs[i][got[m + 1]] for m in range(len(got) - 1))
+
+
+@pytest.mark.parametrize("branching", [[3, 2], [4, 2, 2], [2, 2, 2, 2]])
+def test_greedy_tree_spec_equals_greedy_ar(deep, branching):
+    pr = make_tokens(10, deep.shape.vocab, seed=8)
+    ar = S.generate_greedy_ar(deep, pr, 40)
+    log = []
+    assert S.generate_greedy_tree_spec(deep, pr, 40, tree_parents(branching), log=log) == ar
+    assert any(d > 0 for _, d in log)
