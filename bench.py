@@ -15,6 +15,11 @@ whole round time) -- with accepted tokens/s, the verify-step-only rate and the
 HBM roofline fraction of the dominant kernel (the tcgen05 GEMM) alongside.
 Weights and KV (> L2) are re-streamed every round, so no L2 flush is needed.
 
+--tree 4,2,2 runs greedy layer-skip tree rounds instead of chains: the draft
+grows a 29-node token tree level by level (spec_draft_tree), verify runs
+layers 12..31 over all nodes with the tree mask and fused greedy tree
+acceptance, kv_commit compacts the accepted path.
+
 --mode sample runs sampling rounds instead: draft tokens drawn from
 softmax(draft logits / 0.8) with seeded uniforms (spec_draft_sample), target
 rows at the same temperature cut to their top-p 0.9 nucleus (spec_probs),
@@ -27,6 +32,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -55,6 +61,8 @@ def parse():
     ap.add_argument("--exit-layer", type=int, default=None)
     ap.add_argument("--mode", default="greedy", choices=["greedy", "sample"],
                     help="chain workload: greedy acceptance, or sampling at temperature 0.8 with top-p 0.9")
+    ap.add_argument("--tree", default=None,
+                    help="greedy layer-skip token tree instead of the chain, e.g. 4,2,2 (children per node by level)")
     ap.add_argument("--workload", default="chain", choices=["chain", "adaptive"],
                     help="chain: k=4, ctx 4096, batch 1 (or --batch); adaptive: batch 32, contexts 512..8192, "
                          "per-sequence k in [2,16] from the confidence schedule")
@@ -421,9 +429,13 @@ def main():
                                     exit_layer=args.exit_layer if args.exit_layer is not None else args.layers // 2)
     B, k = args.batch, K_DRAFT
     steps, warm = args.steps, args.warmup
-    grow = (steps + warm + 2) * (k + 1) + 8
+    tree_arg = [int(x) for x in args.tree.split(",")] if args.tree else None
+    n_cand = 1 + sum(math.prod(tree_arg[:i + 1]) for i in range(len(tree_arg))) if tree_arg else k + 1
+    per_round = len(tree_arg) + 1 if tree_arg else k + 1         # most tokens a round commits
+    rounds_total = warm + 2 * steps + max(3, steps // 2) + 1
+    grow = rounds_total * per_round + n_cand + 8
     w = make_weights(shape, SEED + rank, device="cuda")
-    model = spec.Model(shape, w, max_rows=max(64, B * (k + 1)), max_batch=B, max_position=CTX + grow + 64)
+    model = spec.Model(shape, w, max_rows=max(64, B * n_cand), max_batch=B, max_position=CTX + grow + 64)
     del w
     torch.cuda.empty_cache()
     kv = spec.KVCache(model, B, CTX + grow)
@@ -444,6 +456,18 @@ def main():
     ev_v0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ev_v1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     acc_log = torch.zeros((steps, B), dtype=torch.int32, device="cuda")
+    tree = None
+    if args.tree:
+        from synthetic import tree_parents
+        tree = [int(x) for x in tree_parents([int(x) for x in args.tree.split(",")])]
+        if args.mode != "greedy":
+            raise SystemExit("--tree takes greedy acceptance")
+    assert n_cand == (len(tree) if tree else k + 1)
+    if tree:
+        tokens_t = torch.empty((B, n_cand), dtype=torch.int32, device="cuda")
+        hL = torch.empty((B, n_cand, shape.d_model), dtype=torch.float32, device="cuda")
+        tree_scratch = torch.empty((B * n_cand, shape.vocab), dtype=torch.float32, device="cuda")
+        path = torch.empty((B, 64), dtype=torch.int32, device="cuda")
     sampling = args.mode == "sample"
     V = shape.vocab
     if sampling:
@@ -457,13 +481,18 @@ def main():
     rnd = [0]
 
     def draft(ud=None):
-        if sampling:
+        if tree:
+            spec.spec_draft_tree(model, kv, t0, tree, tokens_t, hL, tree_scratch)
+        elif sampling:
             spec.spec_draft_sample(model, kv, t0, k, TEMP, ud, cand, hL, q)
         else:
             spec.spec_draft(model, kv, t0, k, cand, hL)
 
     def verify(ua=None):
-        if sampling:
+        if tree:
+            spec.spec_verify(model, kv, [n_cand] * B, tokens_t, n_cand, h_in=hL, h_stride=n_cand, tree_parent=tree,
+                             acc_len=acc, next_tok=nxt, path=path)
+        elif sampling:
             spec.spec_verify(model, kv, [k + 1] * B, cand, k + 1, h_in=hL, h_stride=k + 1, logits=logits)
             spec.spec_probs(logits, p, TEMP, TOP_P)
             spec.spec_accept(p.view(B, k + 1, V), q, cand[:, 1:], ua, acc, nxt)
@@ -481,7 +510,7 @@ def main():
         if i is not None:
             ev_v1[i].record(stream)
             acc_log[i].copy_(acc)
-        spec.kv_commit(kv, acc)
+        spec.kv_commit(kv, acc, path if tree else None)
         t0.copy_(nxt)
 
     for _ in range(warm):
@@ -526,9 +555,9 @@ def main():
     # and in sampling mode its uniforms) copied in from pinned host memory and
     # its result read back each step
     t0_host = torch.empty(B, dtype=torch.int32).pin_memory()
-    res_host = torch.empty((B, k + 3), dtype=torch.int32).pin_memory()
+    res_host = torch.empty((B, n_cand + 2), dtype=torch.int32).pin_memory()
     t0_host.copy_(t0.cpu())
-    res_dev = torch.empty((B, k + 3), dtype=torch.int32, device="cuda")
+    res_dev = torch.empty((B, n_cand + 2), dtype=torch.int32, device="cuda")
     e_steps = max(3, steps // 2)
     h2d = 4 * B
     if sampling:
@@ -546,20 +575,20 @@ def main():
             ua_dev.copy_(ua_host[e], non_blocking=True)
         draft(ud_dev if sampling else None)
         verify(ua_dev if sampling else None)
-        spec.kv_commit(kv, acc)
-        res_dev[:, :k + 1].copy_(cand)
-        res_dev[:, k + 1].copy_(acc)
-        res_dev[:, k + 2].copy_(nxt)
+        spec.kv_commit(kv, acc, path if tree else None)
+        res_dev[:, :n_cand].copy_(tokens_t if tree else cand)
+        res_dev[:, n_cand].copy_(acc)
+        res_dev[:, n_cand + 1].copy_(nxt)
         res_host.copy_(res_dev, non_blocking=True)
         torch.cuda.synchronize()
-        t0_host.copy_(res_host[:, k + 2])
+        t0_host.copy_(res_host[:, n_cand + 1])
     e2e_s = (time.perf_counter() - tw0) / e_steps
     if world > 1:
         e2e_s = reduce_max(e2e_s, dist, "cuda")
-    e2e_val = job_rate(world, B * (k + 1), e2e_s)
+    e2e_val = job_rate(world, B * n_cand, e2e_s)
 
     hbm, peak_kind = peaks()
-    cand_per_step = B * (k + 1)
+    cand_per_step = B * n_cand
     value = job_rate(world, cand_per_step * steps, ms / 1e3)
     g_avg_ms = g_ms / max(g_n, 1)
     g_avg_bytes = g_bytes / max(g_n, 1)
@@ -572,6 +601,8 @@ def main():
     verify_bytes = n_ver * layer_w + V * d * 2 + kv_bytes
     workload = WORKLOAD if not sampling else WORKLOAD.replace(
         "greedy", f"sampling (T {TEMP}, top-p {TOP_P:.7g}, rejection sampling)")
+    if tree:
+        workload = WORKLOAD.replace("chain k=4", f"token tree {args.tree} ({n_cand} nodes, layer-skip draft)")
     line = {
         "metric": METRIC,
         "value": value,
@@ -587,11 +618,11 @@ def main():
         "data": "synthetic (seeded random-init weights and KV context; no dataset)",
         "config": {"workload": workload if args.layers is None else workload + f" (reduced: {shape.n_layers} layers)",
                    "mode": args.mode,
-                   "batch": B, "k": k, "ctx": CTX, "exit_layer": shape.exit_layer, "n_layers": shape.n_layers,
+                   "batch": B, "k": k if not tree else None, "tree": args.tree, "ctx": CTX, "exit_layer": shape.exit_layer, "n_layers": shape.n_layers,
                    "l2": "inputs larger than L2 (13.5 GB weights re-streamed each round)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "accepted_tokens_per_s": world * (accepted + B * steps) / (ms / 1e3),
-        "acceptance_rate": accepted / (B * steps * k),
+        "acceptance_rate": accepted / (B * steps * (per_round - 1)),
         "verify_ms": verify_ms,
         "verify_candidate_tokens_per_s": world * cand_per_step / (verify_ms / 1e3),
         "verify_hbm_gbs": verify_bytes / (verify_ms / 1e3) / 1e9,
@@ -612,7 +643,7 @@ def main():
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": 4 * B * (k + 3)},
+                "d2h_bytes_per_step": 4 * B * (n_cand + 2)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sec, desc, thr = oracle_round_sample(B)

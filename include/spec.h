@@ -214,6 +214,27 @@ int spec_draft_sample(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* 
                       float temperature, const float* u_draft, int32_t* cand, float* h_L,
                       float* q, float* draft_logits, void* stream);
 
+/* Layer-skip draft of a level-order token tree per sequence (FlashSpec page,
+ * lnrk.cn/news/47842, sections 2.2 and 6.2, with the self-speculative
+ * decoding page's first-L-layer draft): level by level, layers [0, L) run on
+ * the tree's nodes (node i in slot s_b + i at position s_b + depth(i), seeing
+ * the committed context, its ancestors and itself) and the shared LM head
+ * gives each node of the level its children: the k-th child (by node index)
+ * takes the k-th highest draft logit, ties to the lower token id.  A last
+ * pass gives every node its layer-L state.  Writes KV layers [0, L) at slots
+ * s_b .. s_b + n_nodes - 1; lengths unchanged.
+ *   t0           device int32 [batch]: each tree's root token
+ *   tree_parent  host int32 [n_nodes]: parent[0] = -1, parent[i] in [0, i),
+ *                depths non-decreasing (level order), at most 16 children a node
+ *   tokens       device int32 [batch][n_nodes] out (tokens[b][0] = t0[b])
+ *   h_L          device f32 [batch][n_nodes][d] out: layer-L state of every node
+ *   logits       device f32 [batch * n_nodes][V]: scratch for the draft rows
+ * Follow with spec_verify(h_in = h_L, tree_parent, tokens) and kv_commit with
+ * the accepted path.  batch * n_nodes <= max_rows; 2 <= n_nodes <= 64.  async. */
+int spec_draft_tree(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0,
+                    const int32_t* tree_parent, int32_t n_nodes, int32_t* tokens,
+                    float* h_L, float* logits, void* stream);
+
 /* Verification forward of the candidate rows of sequences [0, batch).
  *   n_rows   host int32 [batch]: rows of sequence b (chain: k_b+1; tree:
  *            node count).  Sum <= max_rows, each <= 64.

@@ -8,6 +8,7 @@
 // which the verifier continues from.  Position ids are the committed length
 // plus the row's offset (chain) or depth (tree).
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -172,6 +173,56 @@ __global__ void set_col0_kernel(const int* __restrict__ t0, int* cand, int strid
     pdl_trigger();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < batch) cand[(size_t)b * stride] = t0[b];
+}
+
+// Children of the nodes of one tree level take their parent's best draft
+// tokens: the k-th child (by node index) the k-th highest logit, ties to the
+// lower token id.  One CTA per (sequence, parent node); rounds of block-wide
+// argmax that skip the ids already taken.
+struct TreeKids {
+    int start[kMaxSeqRows + 1];   // children of node i: kid[start[i] .. start[i+1])
+    int kid[kMaxSeqRows];
+};
+constexpr int kMaxTreeKids = 16;
+
+__global__ void __launch_bounds__(256)
+tree_expand_kernel(const float* __restrict__ logits, int V, int rows_per_seq, int node0, TreeKids tk, int* tokens,
+                   int n_nodes) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float s_v[8];
+    __shared__ int s_i[8];
+    __shared__ int taken[kMaxTreeKids];
+    const int b = blockIdx.x, i = node0 + blockIdx.y, t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int c0 = tk.start[i], nc = min(tk.start[i + 1] - c0, kMaxTreeKids);
+    const float* row = logits + ((size_t)b * rows_per_seq + i) * V;
+    for (int k = 0; k < nc; ++k) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int x = t; x < V; x += 256) {
+            bool skip = false;
+            for (int q = 0; q < k; ++q) skip |= taken[q] == x;
+            const float v = row[x];
+            if (!skip && (v > bv || (v == bv && x < bi))) { bv = v; bi = x; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0) { s_v[w] = bv; s_i[w] = bi; }
+        __syncthreads();
+        if (t == 0) {
+            float v = s_v[0];
+            int id = s_i[0];
+            for (int q = 1; q < 8; ++q)
+                if (s_v[q] > v || (s_v[q] == v && s_i[q] < id)) { v = s_v[q]; id = s_i[q]; }
+            taken[k] = id;
+            tokens[(size_t)b * n_nodes + tk.kid[c0 + k]] = id;
+        }
+        __syncthreads();
+    }
 }
 
 __global__ void add_len_kernel(int* len, int seq, int n, int cap, int* err) {
@@ -850,6 +901,80 @@ extern "C" int spec_draft_sample(spec_model* m, spec_kv* kv, int32_t batch, cons
     if (!(temperature > 0.f) || !(temperature <= 3.402823466e38f))
         return set_error(SPEC_ERR_ARG, "spec_draft_sample: temperature must be positive and finite");
     return draft_impl(m, kv, batch, t0, k, cand, h_L, draft_logits, temperature, u_draft, q, (cudaStream_t)stream);
+}
+
+extern "C" int spec_draft_tree(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0, const int32_t* tree_parent,
+                               int32_t n_nodes, int32_t* tokens, float* h_L, float* logits, void* stream) {
+    if (!m || !kv || !t0 || !tree_parent || !tokens || !h_L || !logits)
+        return set_error(SPEC_ERR_ARG, "spec_draft_tree: null pointer");
+    if (kv->m != m) return set_error(SPEC_ERR_ARG, "spec_draft_tree: cache of another model");
+    const spec_model_config& c = m->cfg;
+    if (c.exit_layer < 1) return set_error(SPEC_ERR_ARG, "spec_draft_tree: exit_layer must be >= 1");
+    if (batch < 1 || batch > kv->batch) return set_error(SPEC_ERR_ARG, "spec_draft_tree: bad batch");
+    if (n_nodes < 2 || n_nodes > kMaxSeqRows) return set_error(SPEC_ERR_ARG, "spec_draft_tree: n_nodes must be in [2, 64]");
+    if ((long long)batch * n_nodes > c.max_rows) return set_error(SPEC_ERR_CAPACITY, "spec_draft_tree: batch * n_nodes > max_rows");
+    if (tree_parent[0] != -1) return set_error(SPEC_ERR_ARG, "tree_parent[0] must be -1");
+    PlanParams p{};
+    p.batch = batch;
+    p.mode = 1;
+    p.parent[0] = -1;
+    p.depth[0] = 0;
+    for (int i = 1; i < n_nodes; ++i) {
+        if (tree_parent[i] < 0 || tree_parent[i] >= i) return set_error(SPEC_ERR_ARG, "tree_parent[i] must be in [0, i)");
+        p.parent[i] = tree_parent[i];
+        p.depth[i] = p.depth[tree_parent[i]] + 1;
+        if (p.depth[i] < p.depth[i - 1]) return set_error(SPEC_ERR_ARG, "spec_draft_tree: nodes must be in level order");
+    }
+    TreeKids tk{};
+    {
+        int at = 0;
+        for (int i = 0; i < n_nodes; ++i) {
+            tk.start[i] = at;
+            int nk = 0;
+            for (int j = i + 1; j < n_nodes; ++j)
+                if (tree_parent[j] == i) { tk.kid[at++] = j; ++nk; }
+            if (nk > kMaxTreeKids) return set_error(SPEC_ERR_ARG, "spec_draft_tree: at most 16 children a node");
+        }
+        tk.start[n_nodes] = at;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    launch_k(m->pdl, set_col0_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, t0, tokens, n_nodes, batch);
+    ++m->launches;
+    SPEC_CUDA(cudaGetLastError(), "tree draft init");
+    const int D = p.depth[n_nodes - 1];
+    int l0 = 0;
+    for (int lev = 0; lev <= D; ++lev) {
+        int l1 = l0;
+        while (l1 < n_nodes && p.depth[l1] == lev) ++l1;
+        // layers [0, L) over every node up to this level (earlier levels again: the
+        // cost is the weight stream, the same for these few rows)
+        for (int b = 0; b < batch; ++b) p.n_rows[b] = l1;
+        const int T = batch * l1;
+        SPEC_TRY(launch_plan(m, p, T, kv->len, st));
+        SPEC_TRY(launch_prologue(m, T, nullptr, 0, tokens, n_nodes, 0, 0, st));
+        const bool expand = lev < D;
+        HeadSpec hs{};
+        hs.mode = HEAD_STATS;
+        hs.T = T;
+        hs.r0 = 0;
+        hs.logits = logits;
+        hs.logits_stride = c.vocab;
+        hs.logits_row0 = 0;
+        hs.batch = batch;
+        SPEC_TRY(run_layers(m, kv, T, batch, l1, 0, c.exit_layer, 1, expand, expand ? &hs : nullptr, st));
+        if (expand) {
+            launch_k(m->pdl, tree_expand_kernel, dim3(batch, l1 - l0), dim3(256), 0, st, (const float*)logits,
+                     c.vocab, l1, l0, tk, tokens, n_nodes);
+            ++m->launches;
+            SPEC_CUDA(cudaGetLastError(), "tree expansion");
+        } else {
+            launch_k(m->pdl, copy_rows_kernel, dim3(T), dim3(256), 0, st, (const float*)m->h, h_L, T, c.d_model, 1, 0);
+            ++m->launches;
+            SPEC_CUDA(cudaGetLastError(), "tree draft state copy");
+        }
+        l0 = l1;
+    }
+    return SPEC_OK;
 }
 
 extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows, const float* h_in,

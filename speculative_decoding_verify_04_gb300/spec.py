@@ -27,7 +27,7 @@ EXPORTS = [
     "spec_kv_export", "spec_prefill", "spec_draft", "spec_verify", "spec_accept", "spec_accept_greedy",
     "kv_commit", "spec_row_probs", "spec_schedule_k", "spec_profile", "spec_profile_read", "spec_launch_count",
     "spec_verify_noalloc", "spec_draft_sample", "spec_probs", "spec_sample", "spec_schedule_aimd",
-    "spec_schedule_decay",
+    "spec_schedule_decay", "spec_draft_tree",
 ]
 
 
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH):
         "spec_sample": ([P, ctypes.c_int64, I, I, P, P, P], I),
         "spec_schedule_aimd": ([P, P, P, I, POINTER(AIMDSchedule), P, P], I),
         "spec_schedule_decay": ([P, P, I, I, P, P], I),
+        "spec_draft_tree": ([P, P, I, P, POINTER(I), I, P, P, P, P], I),
         "spec_accept_greedy": ([P, P, POINTER(I), I, I, I, P, P, P, P], I),
         "kv_commit": ([P, I, P, P, I, P], I),
         "spec_row_probs": ([P, I, P, P], I),
@@ -267,6 +268,19 @@ def spec_draft_sample(model, kv, t0, k, temperature, u_draft, cand, h_L, q, draf
     _need(draft_logits, torch.float32, "draft_logits", B * k * V)
     _check(load().spec_draft_sample(model.handle, kv.handle, B, _ptr(t0), k, float(temperature), _ptr(u_draft),
                                     _ptr(cand), _ptr(h_L), _ptr(q), _ptr(draft_logits), _stream(stream)))
+
+
+def spec_draft_tree(model, kv, t0, tree_parent, tokens, h_L, logits, stream=None):
+    """Layer-skip draft of a level-order token tree (children take their parent's
+    best draft tokens).  tokens [B, n], h_L [B, n, d], logits [B * n, V] scratch."""
+    B = t0.numel()
+    n = len(tree_parent)
+    _need(t0, torch.int32, "t0")
+    _need(tokens, torch.int32, "tokens", B * n)
+    _need(h_L, torch.float32, "h_L", B * n * model.cfg.d_model)
+    _need(logits, torch.float32, "logits", B * n * model.cfg.vocab)
+    _check(load().spec_draft_tree(model.handle, kv.handle, B, _ptr(t0), _i32_array(tree_parent), n, _ptr(tokens),
+                                  _ptr(h_L), _ptr(logits), _stream(stream)))
 
 
 def _rows2d(t, name):
