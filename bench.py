@@ -20,6 +20,9 @@ grows a 29-node token tree level by level (spec_draft_tree), verify runs
 layers 12..31 over all nodes with the tree mask and fused greedy tree
 acceptance, kv_commit compacts the accepted path.
 
+--page 64 keeps the KV cache in 64-slot pages (page tables, pages taken before
+each write and returned past the committed length at every commit).
+
 --mode sample runs sampling rounds instead: draft tokens drawn from
 softmax(draft logits / 0.8) with seeded uniforms (spec_draft_sample), target
 rows at the same temperature cut to their top-p 0.9 nucleus (spec_probs),
@@ -61,6 +64,8 @@ def parse():
     ap.add_argument("--exit-layer", type=int, default=None)
     ap.add_argument("--mode", default="greedy", choices=["greedy", "sample"],
                     help="chain workload: greedy acceptance, or sampling at temperature 0.8 with top-p 0.9")
+    ap.add_argument("--page", type=int, default=0,
+                    help="paged KV cache with pages of this many slots (a power of two, at least 64); 0: contiguous")
     ap.add_argument("--tree", default=None,
                     help="greedy layer-skip token tree instead of the chain, e.g. 4,2,2 (children per node by level)")
     ap.add_argument("--workload", default="chain", choices=["chain", "adaptive"],
@@ -438,7 +443,7 @@ def main():
     model = spec.Model(shape, w, max_rows=max(64, B * n_cand), max_batch=B, max_position=CTX + grow + 64)
     del w
     torch.cuda.empty_cache()
-    kv = spec.KVCache(model, B, CTX + grow)
+    kv = spec.KVCache(model, B, CTX + grow, page=args.page or None)
     for b in range(B):
         kc, vc = make_kv_context(shape, 1, CTX, SEED * 1000 + rank * 100 + b, device="cuda")
         kv.import_rows(b, 0, kc[:, 0].contiguous(), vc[:, 0].contiguous())
@@ -618,7 +623,8 @@ def main():
         "data": "synthetic (seeded random-init weights and KV context; no dataset)",
         "config": {"workload": workload if args.layers is None else workload + f" (reduced: {shape.n_layers} layers)",
                    "mode": args.mode,
-                   "batch": B, "k": k if not tree else None, "tree": args.tree, "ctx": CTX, "exit_layer": shape.exit_layer, "n_layers": shape.n_layers,
+                   "batch": B, "k": k if not tree else None, "tree": args.tree, "ctx": CTX,
+                   "kv": f"paged, {args.page}-slot pages" if args.page else "contiguous", "exit_layer": shape.exit_layer, "n_layers": shape.n_layers,
                    "l2": "inputs larger than L2 (13.5 GB weights re-streamed each round)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "accepted_tokens_per_s": world * (accepted + B * steps) / (ms / 1e3),

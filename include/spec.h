@@ -166,6 +166,26 @@ int spec_device_error(spec_model* m, int32_t* host_bits);
  * K and V, in the model dtype: layout [layer][seq][kv_head][slot][hd]
  * (one allocation, never grown).  Lengths start at 0.  sync. */
 int spec_kv_create(spec_model* m, int32_t batch, int32_t max_ctx, spec_kv** out);
+
+/* Paged KV cache ("self-speculative decoding" page, m.lqnn.cn/news/278124,
+ * sections 3.3 and 4.5: rollback by page, compaction): a pool of n_pages
+ * pages of `page` slots (a power of two, at least 64) per layer, shared by the batch
+ * sequences, each addressing up to max_ctx slots through its page table.
+ * Calls that write slots take the pages they need from the pool first (in
+ * sequence order, deterministic); kv_commit and spec_kv_set_lengths return
+ * the pages past the committed lengths (page-granular rollback); a tree
+ * commit compacts the accepted path through the table.  An empty pool sets
+ * SPEC_DEVERR_CAPACITY.  Every other call behaves as with spec_kv_create and
+ * gives the same results bit for bit.  sync. */
+int spec_kv_create_paged(spec_model* m, int32_t batch, int32_t max_ctx, int32_t page, int32_t n_pages,
+                         spec_kv** out);
+
+/* Pages left in the pool of a paged cache (0 for a contiguous one).  sync. */
+int spec_kv_free_pages(spec_kv* kv, int32_t* host_free, void* stream);
+
+/* Page table, host int32 [batch][ceil(max_ctx / page)] (-1: no page; a
+ * contiguous cache reports page b for sequence b).  sync. */
+int spec_kv_page_table(spec_kv* kv, int32_t* host_table, void* stream);
 void spec_kv_destroy(spec_kv* kv);
 
 /* Committed lengths: set from / copy to host int32 [batch].  sync. */

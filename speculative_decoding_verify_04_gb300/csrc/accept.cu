@@ -45,24 +45,71 @@ accept_greedy_kernel(const float* __restrict__ logits, const int* __restrict__ t
 // per (layer, kv head, sequence); lengths are updated by a second launch.
 template <typename KT>
 __global__ void commit_tree_kernel(KT* kc, KT* vc, const int* len, const int* acc_len, const int* path,
-                                   int path_stride, int n_layers, int n_kv_heads, int kv_batch, int kv_ctx,
-                                   int hd, int* err) {
+                                   int path_stride, int n_kv_heads, KVPages kvp, int kv_ctx, int hd, int* err) {
     pdl_wait();
     pdl_trigger();
     const int lh = blockIdx.x, b = blockIdx.y;
     const int layer = lh / n_kv_heads, kvh = lh % n_kv_heads;
     const int s = len[b], a = acc_len[b];
-    const size_t head = (((size_t)layer * kv_batch + b) * n_kv_heads + kvh) * kv_ctx;
     for (int d = 1; d <= a; ++d) {
         const int src = s + path[(size_t)b * path_stride + d], dst = s + d;
         if (src >= kv_ctx || dst >= kv_ctx) { if (threadIdx.x == 0) dev_error(err, SPEC_DEVERR_CAPACITY); return; }
+        const long long rs = kv_row(kvp, n_kv_heads, layer, b, kvh, src), rd = kv_row(kvp, n_kv_heads, layer, b, kvh, dst);
+        if (rs < 0 || rd < 0) { if (threadIdx.x == 0) dev_error(err, SPEC_DEVERR_CAPACITY); return; }
         KT kv0 = KT(), vv0 = KT();
         const int i = threadIdx.x;
-        if (i < hd) { kv0 = kc[(head + src) * hd + i]; vv0 = vc[(head + src) * hd + i]; }
+        if (i < hd) { kv0 = kc[(size_t)rs * hd + i]; vv0 = vc[(size_t)rs * hd + i]; }
         __syncthreads();
-        if (i < hd) { kc[(head + dst) * hd + i] = kv0; vc[(head + dst) * hd + i] = vv0; }
+        if (i < hd) { kc[(size_t)rd * hd + i] = kv0; vc[(size_t)rd * hd + i] = vv0; }
         __syncthreads();
     }
+}
+
+// Paged caches.  One thread walks every sequence in order, so which page a
+// block of slots gets is deterministic.
+//   ensure: before a call writes slots, every block of slots below end[b]
+//   (len[b] + n[b] when relative, else n[b]) holds a page, popped from the free
+//   stack; an empty stack sets the capacity error.
+//   release (page-granular rollback, "self-speculative decoding" page section
+//   3.3): the blocks past the committed length give their pages back.
+struct PageNeed { int batch; int relative; int n[kMaxPlanBatch]; };
+
+__global__ void ensure_pages_kernel(const int* __restrict__ len, PageNeed need, int* table, int page, int max_pages,
+                                    const int* free_pages, int* free_top, int* err) {
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int top = *free_top;
+    for (int b = 0; b < need.batch; ++b) {
+        const int end = need.relative ? len[b] + need.n[b] : need.n[b];
+        const int blocks = min(max_pages, (end + page - 1) / page);
+        if ((end + page - 1) / page > max_pages) dev_error(err, SPEC_DEVERR_CAPACITY);
+        for (int p = 0; p < blocks; ++p) {
+            int* e = table + (size_t)b * max_pages + p;
+            if (*e >= 0) continue;
+            if (top == 0) { dev_error(err, SPEC_DEVERR_CAPACITY); break; }
+            *e = free_pages[--top];
+        }
+    }
+    *free_top = top;
+}
+
+__global__ void release_pages_kernel(const int* __restrict__ len, int batch, int* table, int page, int max_pages,
+                                     int* free_pages, int* free_top, int n_pages) {
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int top = *free_top;
+    for (int b = 0; b < batch; ++b) {
+        const int keep = (len[b] + page - 1) / page;
+        for (int p = max_pages - 1; p >= keep; --p) {
+            int* e = table + (size_t)b * max_pages + p;
+            if (*e < 0) continue;
+            if (top < n_pages) free_pages[top++] = *e;
+            *e = -1;
+        }
+    }
+    *free_top = top;
 }
 
 __global__ void commit_len_kernel(int* len, const int* acc_len, int batch, int kv_ctx, int* err) {
@@ -160,6 +207,29 @@ __global__ void row_probs_kernel(const spec_row_stats* __restrict__ st, int rows
     out[2 * (size_t)r + 1] = __ddiv_rn(exp((double)s.top2 - (double)s.top1), S);
 }
 
+int kv_ensure_pages(spec_kv* kv, int batch, const int* n, bool relative, cudaStream_t st) {
+    if (!kv->paged) return SPEC_OK;
+    if (batch > kMaxPlanBatch) return set_error(SPEC_ERR_CAPACITY, "paged cache: too many sequences in one call");
+    PageNeed need{};
+    need.batch = batch;
+    need.relative = relative ? 1 : 0;
+    for (int b = 0; b < batch; ++b) need.n[b] = n[b];
+    spec_model* m = kv->m;
+    launch_k(m->pdl, ensure_pages_kernel, dim3(1), dim3(32), 0, st, (const int*)kv->len, need, kv->table, kv->page,
+             kv->max_pages, (const int*)kv->free_pages, kv->free_top, m->err);
+    ++m->launches;
+    return check_cuda(cudaGetLastError(), "page allocation launch");
+}
+
+int kv_release_pages(spec_kv* kv, int batch, cudaStream_t st) {
+    if (!kv->paged) return SPEC_OK;
+    spec_model* m = kv->m;
+    launch_k(m->pdl, release_pages_kernel, dim3(1), dim3(32), 0, st, (const int*)kv->len, batch, kv->table, kv->page,
+             kv->max_pages, kv->free_pages, kv->free_top, kv->n_pages);
+    ++m->launches;
+    return check_cuda(cudaGetLastError(), "page release launch");
+}
+
 }  // namespace spec
 
 using namespace spec;
@@ -198,19 +268,21 @@ extern "C" int kv_commit(spec_kv* kv, int32_t batch, const int32_t* acc_len, con
         const int threads = m->cfg.head_dim;
         if (m->bf16)
             launch_k(m->pdl, commit_tree_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st,
-                (__nv_bfloat16*)kv->k, (__nv_bfloat16*)kv->v, kv->len, acc_len, path, path_stride, m->cfg.n_layers,
-                m->cfg.n_kv_heads, kv->batch, kv->max_ctx, m->cfg.head_dim, m->err);
+                (__nv_bfloat16*)kv->k, (__nv_bfloat16*)kv->v, kv->len, acc_len, path, path_stride,
+                m->cfg.n_kv_heads, kv->pages(), kv->max_ctx, m->cfg.head_dim, m->err);
         else
-            launch_k(m->pdl, commit_tree_kernel<float>, grid, dim3(threads), 0, st, (float*)kv->k, (float*)kv->v, kv->len, acc_len, path,
-                                                                path_stride, m->cfg.n_layers, m->cfg.n_kv_heads,
-                                                                kv->batch, kv->max_ctx, m->cfg.head_dim, m->err);
+            launch_k(m->pdl, commit_tree_kernel<float>, grid, dim3(threads), 0, st, (float*)kv->k, (float*)kv->v,
+                     kv->len, acc_len, path, path_stride, m->cfg.n_kv_heads, kv->pages(), kv->max_ctx,
+                     m->cfg.head_dim, m->err);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return check_cuda(e, "kv_commit tree launch");
     }
     launch_k(m->pdl, commit_len_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, kv->len, acc_len, batch, kv->max_ctx,
              m->err);
     m->launches += path ? 2 : 1;
-    return check_cuda(cudaGetLastError(), "kv_commit launch");
+    const int rc = check_cuda(cudaGetLastError(), "kv_commit launch");
+    if (rc) return rc;
+    return kv->paged ? kv_release_pages(kv, batch, st) : SPEC_OK;
 }
 
 extern "C" int spec_row_probs(const spec_row_stats* stats, int32_t rows, double* out, void* stream) {

@@ -156,10 +156,6 @@ attention_kernel(AttnParams a, int n_rb) {
         sL[t] = 0.f;
     }
 
-    const size_t head_off = (((size_t)a.layer * a.kv_batch + b) * a.n_kv_heads + g) * a.kv_ctx;
-    const KT* Kg = static_cast<const KT*>(a.kc) + head_off * HD;
-    const KT* Vg = static_cast<const KT*>(a.vc) + head_off * HD;
-
     const int d_own = t % HD;
     const int i_own = (t / HD) * QPT;
     float acc[QPT];
@@ -168,14 +164,18 @@ attention_kernel(AttnParams a, int n_rb) {
 
     for (int kt = k_begin; kt < k_end; kt += kKeyTile) {
         const int nk = min(kKeyTile, k_end - kt);
+        long long row = kv_row(a.kvp, a.n_kv_heads, a.layer, b, g, kt);      // a tile never crosses a page
+        if (row < 0) { if (t == 0) dev_error(a.err, SPEC_DEVERR_CAPACITY); row = 0; }
+        const KT* Kt = static_cast<const KT*>(a.kc) + (size_t)row * HD;
+        const KT* Vt = static_cast<const KT*>(a.vc) + (size_t)row * HD;
         __syncthreads();
         // K, V tile -> shared (f32)
         constexpr int VEC = 16 / sizeof(KT);
         for (int i = t; i < kKeyTile * HD / VEC; i += kAttnThreads) {
             const int kk = (i * VEC) / HD, d0 = (i * VEC) % HD;
             if (kk < nk) {
-                const uint4 kr = *reinterpret_cast<const uint4*>(Kg + (size_t)(kt + kk) * HD + d0);
-                const uint4 vr = *reinterpret_cast<const uint4*>(Vg + (size_t)(kt + kk) * HD + d0);
+                const uint4 kr = *reinterpret_cast<const uint4*>(Kt + (size_t)kk * HD + d0);
+                const uint4 vr = *reinterpret_cast<const uint4*>(Vt + (size_t)kk * HD + d0);
                 const KT* kp = reinterpret_cast<const KT*>(&kr);
                 const KT* vp = reinterpret_cast<const KT*>(&vr);
 #pragma unroll
@@ -334,19 +334,20 @@ attention_decode_kernel(AttnParams a) {
         for (int e = 0; e < EPL; ++e) acc[r][e] = 0.f;
     }
 
-    const size_t head_off = (((size_t)a.layer * a.kv_batch + b) * a.n_kv_heads + g) * a.kv_ctx;
-    const KT* Kg = static_cast<const KT*>(a.kc) + head_off * HD + lk * EPL;
-    const KT* Vg = static_cast<const KT*>(a.vc) + head_off * HD + lk * EPL;
+    const KT* Kc = static_cast<const KT*>(a.kc) + lk * EPL;
+    const KT* Vc = static_cast<const KT*>(a.vc) + lk * EPL;
 
     for (int kb = w_begin; kb < w_end; kb += KPW * U) {
         uint4 kr[U], vr[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int key = kb + u * KPW + grp;
-            if (key < w_end) {
-                kr[u] = __ldg(reinterpret_cast<const uint4*>(Kg + (size_t)key * HD));
-                vr[u] = __ldg(reinterpret_cast<const uint4*>(Vg + (size_t)key * HD));
+            const long long row = key < w_end ? kv_row(a.kvp, a.n_kv_heads, a.layer, b, g, key) : -1;
+            if (row >= 0) {
+                kr[u] = __ldg(reinterpret_cast<const uint4*>(Kc + (size_t)row * HD));
+                vr[u] = __ldg(reinterpret_cast<const uint4*>(Vc + (size_t)row * HD));
             } else {
+                if (key < w_end) dev_error(a.err, SPEC_DEVERR_CAPACITY);
                 kr[u] = make_uint4(0, 0, 0, 0);
                 vr[u] = make_uint4(0, 0, 0, 0);
             }
@@ -548,9 +549,6 @@ attention_mma_kernel(AttnParams a, int n_qb) {
     }
     __syncthreads();
 
-    const size_t head_off = (((size_t)a.layer * a.kv_batch + b) * a.n_kv_heads + g) * a.kv_ctx;
-    const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(a.kc) + head_off * HD;
-    const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(a.vc) + head_off * HD;
     const unsigned long long mk0 = sMask[gq], mk1 = sMask[gq + 8];
 
     float o[VD][4];
@@ -559,18 +557,24 @@ attention_mma_kernel(AttnParams a, int n_qb) {
     float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
 
     for (int kt = k_begin + 16 * warp; kt < k_end; kt += 64) {
+        // the tile's rows: a 16-key tile never crosses a page (keys past the
+        // capacity read the last slot's row and are masked)
+        long long trow = kv_row(a.kvp, a.n_kv_heads, a.layer, b, g, kt);
+        if (trow < 0) { dev_error(a.err, SPEC_DEVERR_CAPACITY); trow = 0; }
+        const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(a.kc) + (size_t)trow * HD;
+        const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(a.vc) + (size_t)trow * HD;
         uint4 kr[2][KP], vr[4][VP];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int key = min(kt + 4 * (gq >> 1) + 2 * h + (gq & 1), a.kv_ctx - 1);
-            const uint4* row = reinterpret_cast<const uint4*>(Kg + (size_t)key * HD);
+            const uint4* row = reinterpret_cast<const uint4*>(Kg + (size_t)(key - kt) * HD);
 #pragma unroll
             for (int p = 0; p < KP; ++p) kr[h][p] = __ldg(row + 4 * p + cq);
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int key = kt + 4 * cq + r;
-            const uint4* row = reinterpret_cast<const uint4*>(Vg + (size_t)min(key, a.kv_ctx - 1) * HD);
+            const uint4* row = reinterpret_cast<const uint4*>(Vg + (size_t)(min(key, a.kv_ctx - 1) - kt) * HD);
 #pragma unroll
             for (int p = 0; p < VP; ++p) vr[r][p] = __ldg(row + VP * gq + p);
         }

@@ -14,6 +14,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include "model.cuh"
 #include "stats.cuh"
@@ -237,7 +238,9 @@ __global__ void add_len_kernel(int* len, int seq, int n, int cap, int* err) {
 
 template <typename T>
 __global__ void kv_copy_kernel(T* cache, T* buf, int to_cache, int seq, int layer0, int n_layers, int slot0,
-                               int n_slots, int kv_batch, int Hkv, int ctx, int hd) {
+                               int n_slots, KVPages kvp, int Hkv, int hd, int* err) {
+    pdl_wait();
+    pdl_trigger();
     const size_t total = (size_t)n_layers * n_slots * Hkv * hd;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
         const int e = (int)(i % hd);
@@ -245,7 +248,9 @@ __global__ void kv_copy_kernel(T* cache, T* buf, int to_cache, int seq, int laye
         const int h = (int)(rest % Hkv); rest /= Hkv;
         const int s = (int)(rest % n_slots);
         const int l = (int)(rest / n_slots);
-        const size_t c = ((((size_t)(layer0 + l) * kv_batch + seq) * Hkv + h) * ctx + slot0 + s) * hd + e;
+        const long long row = kv_row(kvp, Hkv, layer0 + l, seq, h, slot0 + s);
+        if (row < 0) { dev_error(err, SPEC_DEVERR_CAPACITY); continue; }
+        const size_t c = (size_t)row * hd + e;
         if (to_cache) cache[c] = buf[i]; else buf[i] = cache[c];
     }
 }
@@ -278,8 +283,8 @@ static EpiParams base_epi(spec_model* m, spec_kv* kv, int T) {
     e.q = m->q;
     e.kc = kv->k;
     e.vc = kv->v;
-    e.kv_batch = kv->batch;
     e.kv_ctx = kv->max_ctx;
+    e.kvp = kv->pages();
     e.n_heads = c.n_heads;
     e.n_kv_heads = c.n_kv_heads;
     e.head_dim = c.head_dim;
@@ -360,7 +365,6 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             at.at.out_lo = (size_t)m->max_rows_pad * qdim;
             at.at.plan = m->plan;
             at.at.batch = batch;
-            at.at.kv_batch = kv->batch;
             at.at.kv_ctx = kv->max_ctx;
             at.at.layer = l;
             at.at.n_heads = c.n_heads;
@@ -370,6 +374,7 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             at.at.linear = max_rows_per_seq * (c.n_heads / c.n_kv_heads) <= kAttnSimtQ;
             at.at.kc = kv->k;
             at.at.vc = kv->v;
+            at.at.kvp = kv->pages();
             pend[np++] = at;
         } else {   // attention
             AttnParams a{};
@@ -380,13 +385,13 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             a.out_lo = (size_t)m->max_rows_pad * qdim;
             a.plan = m->plan;
             a.batch = batch;
-            a.kv_batch = kv->batch;
             a.kv_ctx = kv->max_ctx;
             a.layer = l;
             a.n_heads = c.n_heads;
             a.n_kv_heads = c.n_kv_heads;
             a.head_dim = c.head_dim;
             a.tree = tree;
+            a.kvp = kv->pages();
             a.err = m->err;
             SPEC_TRY(launch_attention(m, a, max_rows_per_seq, st));
         }
@@ -700,8 +705,8 @@ extern "C" int spec_device_error(spec_model* m, int32_t* host_bits) {
     return SPEC_OK;
 }
 
-extern "C" int spec_kv_create(spec_model* m, int32_t batch, int32_t max_ctx, spec_kv** out) {
-    if (!m || !out) return set_error(SPEC_ERR_ARG, "spec_kv_create: null pointer");
+// page = 0: contiguous cache (one page of max_ctx slots per sequence)
+static int kv_create(spec_model* m, int32_t batch, int32_t max_ctx, int32_t page, int32_t n_pages, spec_kv** out) {
     *out = nullptr;
     if (batch < 1 || max_ctx < 1) return set_error(SPEC_ERR_ARG, "spec_kv_create: bad sizes");
     if (batch > m->cfg.max_batch) return set_error(SPEC_ERR_CAPACITY, "spec_kv_create: batch > max_batch");
@@ -709,20 +714,72 @@ extern "C" int spec_kv_create(spec_model* m, int32_t batch, int32_t max_ctx, spe
     kv->m = m;
     kv->batch = batch;
     kv->max_ctx = max_ctx;
-    const size_t bytes = (size_t)m->cfg.n_layers * batch * m->cfg.n_kv_heads * max_ctx * m->cfg.head_dim * m->elem;
+    kv->paged = page > 0;
+    kv->page = kv->paged ? page : max_ctx;
+    kv->max_pages = kv->paged ? (max_ctx + page - 1) / page : 1;
+    kv->n_pages = kv->paged ? n_pages : batch;
+    const size_t bytes = (size_t)m->cfg.n_layers * kv->n_pages * m->cfg.n_kv_heads * kv->page * m->cfg.head_dim * m->elem;
+    const size_t tab = (size_t)batch * kv->max_pages;
     int rc = check_cuda(cudaMalloc(&kv->k, bytes), "cudaMalloc(K cache)");
     if (!rc) rc = check_cuda(cudaMalloc(&kv->v, bytes), "cudaMalloc(V cache)");
     if (!rc) rc = check_cuda(cudaMalloc(&kv->len, (size_t)batch * 4), "cudaMalloc(lengths)");
+    if (!rc) rc = check_cuda(cudaMalloc(&kv->table, tab * 4), "cudaMalloc(page table)");
     if (!rc) rc = check_cuda(cudaMemset(kv->k, 0, bytes), "clear K");
     if (!rc) rc = check_cuda(cudaMemset(kv->v, 0, bytes), "clear V");
     if (!rc) rc = check_cuda(cudaMemset(kv->len, 0, (size_t)batch * 4), "clear lengths");
+    if (!rc) {
+        // contiguous: sequence b is page b; paged: no page held, every page free
+        std::vector<int> t(tab, -1);
+        if (!kv->paged) for (int b = 0; b < batch; ++b) t[b] = b;
+        rc = check_cuda(cudaMemcpy(kv->table, t.data(), tab * 4, cudaMemcpyHostToDevice), "page table");
+    }
+    if (!rc && kv->paged) {
+        rc = check_cuda(cudaMalloc(&kv->free_pages, (size_t)(n_pages + 1) * 4), "cudaMalloc(free pages)");
+        if (!rc) {
+            std::vector<int> f(n_pages + 1);
+            for (int i = 0; i < n_pages; ++i) f[i] = n_pages - 1 - i;      // popped from the top: page 0 first
+            f[n_pages] = n_pages;
+            rc = check_cuda(cudaMemcpy(kv->free_pages, f.data(), f.size() * 4, cudaMemcpyHostToDevice), "free pages");
+            kv->free_top = kv->free_pages + n_pages;
+        }
+    }
     if (!rc && !make_kv_tmaps(kv)) rc = set_error(SPEC_ERR_CUDA, "spec_kv_create: K/V tensor maps");
     if (rc) {
-        cudaFree(kv->k); cudaFree(kv->v); cudaFree(kv->len);
-        delete kv;
+        spec_kv_destroy(kv);
         return rc;
     }
     *out = kv;
+    return SPEC_OK;
+}
+
+extern "C" int spec_kv_create(spec_model* m, int32_t batch, int32_t max_ctx, spec_kv** out) {
+    if (!m || !out) return set_error(SPEC_ERR_ARG, "spec_kv_create: null pointer");
+    return kv_create(m, batch, max_ctx, 0, 0, out);
+}
+
+extern "C" int spec_kv_create_paged(spec_model* m, int32_t batch, int32_t max_ctx, int32_t page, int32_t n_pages,
+                                    spec_kv** out) {
+    if (!m || !out) return set_error(SPEC_ERR_ARG, "spec_kv_create_paged: null pointer");
+    *out = nullptr;
+    if (page < 64 || (page & (page - 1)) != 0)
+        return set_error(SPEC_ERR_ARG, "spec_kv_create_paged: page must be a power of two, at least 64");
+    if (n_pages < 1) return set_error(SPEC_ERR_ARG, "spec_kv_create_paged: n_pages must be positive");
+    return kv_create(m, batch, max_ctx, page, n_pages, out);
+}
+
+extern "C" int spec_kv_free_pages(spec_kv* kv, int32_t* host_free, void* stream) {
+    if (!kv || !host_free) return set_error(SPEC_ERR_ARG, "spec_kv_free_pages: null pointer");
+    if (!kv->paged) { *host_free = 0; return SPEC_OK; }
+    SPEC_CUDA(cudaMemcpyAsync(host_free, kv->free_top, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream), "free pages");
+    SPEC_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "free pages sync");
+    return SPEC_OK;
+}
+
+extern "C" int spec_kv_page_table(spec_kv* kv, int32_t* host_table, void* stream) {
+    if (!kv || !host_table) return set_error(SPEC_ERR_ARG, "spec_kv_page_table: null pointer");
+    SPEC_CUDA(cudaMemcpyAsync(host_table, kv->table, (size_t)kv->batch * kv->max_pages * 4, cudaMemcpyDeviceToHost,
+                              (cudaStream_t)stream), "page table");
+    SPEC_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "page table sync");
     return SPEC_OK;
 }
 
@@ -731,6 +788,8 @@ extern "C" void spec_kv_destroy(spec_kv* kv) {
     cudaFree(kv->k);
     cudaFree(kv->v);
     cudaFree(kv->len);
+    cudaFree(kv->table);
+    cudaFree(kv->free_pages);
     delete kv;
 }
 
@@ -740,6 +799,10 @@ extern "C" int spec_kv_set_lengths(spec_kv* kv, const int32_t* host_len, void* s
         if (host_len[b] < 0 || host_len[b] > kv->max_ctx) return set_error(SPEC_ERR_CAPACITY, "length beyond max_ctx");
     SPEC_CUDA(cudaMemcpyAsync(kv->len, host_len, (size_t)kv->batch * 4, cudaMemcpyHostToDevice, (cudaStream_t)stream),
               "set lengths");
+    if (kv->paged) {          // pages for the slots below the new lengths, the rest back
+        SPEC_TRY(kv_release_pages(kv, kv->batch, (cudaStream_t)stream));
+        SPEC_TRY(kv_ensure_pages(kv, kv->batch, host_len, false, (cudaStream_t)stream));
+    }
     SPEC_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "set lengths sync");
     return SPEC_OK;
 }
@@ -761,17 +824,21 @@ static int kv_copy(spec_kv* kv, int32_t seq, int32_t layer0, int32_t n_layers, i
         n_slots < 1 || slot0 + n_slots > kv->max_ctx)
         return set_error(SPEC_ERR_ARG, "spec_kv_import/export: range outside the cache");
     cudaStream_t st = (cudaStream_t)stream;
+    if (kv->paged && to_cache) {          // pages for the imported slots
+        int need[kMaxPlanBatch] = {0};
+        need[seq] = slot0 + n_slots;
+        SPEC_TRY(kv_ensure_pages(kv, seq + 1, need, false, st));
+    }
     for (int which = 0; which < 2; ++which) {
         void* cache = which ? kv->v : kv->k;
         void* buf = which ? v : k;
         if (m->bf16)
             kv_copy_kernel<__nv_bfloat16><<<1024, 256, 0, st>>>((__nv_bfloat16*)cache, (__nv_bfloat16*)buf, to_cache,
-                                                               seq, layer0, n_layers, slot0, n_slots, kv->batch,
-                                                               c.n_kv_heads, kv->max_ctx, c.head_dim);
+                                                               seq, layer0, n_layers, slot0, n_slots, kv->pages(),
+                                                               c.n_kv_heads, c.head_dim, m->err);
         else
             kv_copy_kernel<float><<<1024, 256, 0, st>>>((float*)cache, (float*)buf, to_cache, seq, layer0, n_layers,
-                                                       slot0, n_slots, kv->batch, c.n_kv_heads, kv->max_ctx,
-                                                       c.head_dim);
+                                                       slot0, n_slots, kv->pages(), c.n_kv_heads, c.head_dim, m->err);
     }
     return check_cuda(cudaGetLastError(), "kv copy launch");
 }
@@ -800,6 +867,7 @@ extern "C" int spec_prefill(spec_model* m, spec_kv* kv, int32_t seq, const int32
         p.batch = seq + 1;
         p.mode = 0;
         p.n_rows[seq] = T;
+        SPEC_TRY(kv_ensure_pages(kv, seq + 1, p.n_rows, true, st));
         SPEC_TRY(launch_plan(m, p, T, kv->len, st));
         SPEC_TRY(launch_prologue(m, T, nullptr, 0, tokens + done, 0, 0, 0, st));
         const bool last = done + T >= n;
@@ -834,6 +902,11 @@ static int draft_impl(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* 
     if (k < 1 || k + 1 > kMaxSeqRows) return set_error(SPEC_ERR_ARG, "spec_draft: k must be in [1, 63]");
     const bool sampling = temp > 0.f;
     if (sampling && batch > c.max_batch) return set_error(SPEC_ERR_ARG, "spec_draft_sample: batch > max_batch");
+    if (kv->paged) {
+        int need[kMaxPlanBatch];
+        for (int b = 0; b < batch; ++b) need[b] = k + 1;
+        SPEC_TRY(kv_ensure_pages(kv, batch, need, true, st));
+    }
     launch_k(m->pdl, set_col0_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, t0, cand, k + 1, batch);
     ++m->launches;
     SPEC_CUDA(cudaGetLastError(), "draft init");
@@ -938,6 +1011,11 @@ extern "C" int spec_draft_tree(spec_model* m, spec_kv* kv, int32_t batch, const 
         tk.start[n_nodes] = at;
     }
     cudaStream_t st = (cudaStream_t)stream;
+    if (kv->paged) {
+        int need[kMaxPlanBatch];
+        for (int b = 0; b < batch; ++b) need[b] = n_nodes;
+        SPEC_TRY(kv_ensure_pages(kv, batch, need, true, st));
+    }
     launch_k(m->pdl, set_col0_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, t0, tokens, n_nodes, batch);
     ++m->launches;
     SPEC_CUDA(cudaGetLastError(), "tree draft init");
@@ -1016,6 +1094,7 @@ extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int3
     }
     cudaStream_t st = (cudaStream_t)stream;
     const int lo = h_in ? c.exit_layer : 0;
+    SPEC_TRY(kv_ensure_pages(kv, batch, p.n_rows, true, st));
     SPEC_TRY(launch_plan(m, p, T, kv->len, st));
     SPEC_TRY(launch_prologue(m, T, h_in, h_stride, tokens, tok_stride, 0, lo, st));
     HeadSpec hs{};

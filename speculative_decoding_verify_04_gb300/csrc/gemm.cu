@@ -95,7 +95,7 @@ bool make_kv_tmaps(spec_kv* kv) {
     const spec_model_config& c = m->cfg;
     kv->tmaps = false;
     if (!m->bf16 || (c.head_dim != 64 && c.head_dim != 128)) return true;
-    const uint64_t rows = (uint64_t)kv->batch * c.n_kv_heads * kv->max_ctx;
+    const uint64_t rows = (uint64_t)kv->n_pages * c.n_kv_heads * kv->page;
     if (rows >= (1ull << 31)) return true;            // slot coordinates are 32-bit
     if (!load_encoder()) return false;
     for (int w = 0; w < 2; ++w) {
@@ -203,16 +203,18 @@ SPEC_DEV void apply_qkv(const EpiParams& e, int tile, int j0, int nr, EpiSmem& s
                 const int kvh = (n - qd) / hd;
                 const int seq = e.plan.row_seq[r], slot = e.plan.row_slot[r];
                 if (slot < 0 || slot >= e.kv_ctx) { dev_error(e.err, SPEC_DEVERR_CAPACITY); continue; }
-                const size_t off = ((((size_t)e.layer * e.kv_batch + seq) * e.n_kv_heads + kvh) * e.kv_ctx + slot) * hd + i;
-                static_cast<KT*>(e.kc)[off] = from_f32<KT>(o);
+                const long long row = kv_row(e.kvp, e.n_kv_heads, e.layer, seq, kvh, slot);
+                if (row < 0) { dev_error(e.err, SPEC_DEVERR_CAPACITY); continue; }
+                static_cast<KT*>(e.kc)[(size_t)row * hd + i] = from_f32<KT>(o);
             }
         } else {
             const int i = n & (hd - 1);
             const int kvh = (n - qd - kvd) / hd;
             const int seq = e.plan.row_seq[r], slot = e.plan.row_slot[r];
             if (slot < 0 || slot >= e.kv_ctx) { dev_error(e.err, SPEC_DEVERR_CAPACITY); continue; }
-            const size_t off = ((((size_t)e.layer * e.kv_batch + seq) * e.n_kv_heads + kvh) * e.kv_ctx + slot) * hd + i;
-            static_cast<KT*>(e.vc)[off] = from_f32<KT>(v);
+            const long long row = kv_row(e.kvp, e.n_kv_heads, e.layer, seq, kvh, slot);
+            if (row < 0) { dev_error(e.err, SPEC_DEVERR_CAPACITY); continue; }
+            static_cast<KT*>(e.vc)[(size_t)row * hd + i] = from_f32<KT>(v);
         }
     }
 }
@@ -532,7 +534,7 @@ SPEC_DEV bool grid_wait(const int* bar, int target, volatile int* abort_flag, in
 
 // ATTN: the chain may hold an attention phase (instantiated only then, so the
 // plain GEMM chains carry none of its code or registers).
-template <bool ATTN>
+template <bool ATTN, bool PAGED = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
     extern __shared__ uint8_t smem_raw[];
@@ -635,6 +637,12 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                     AttnUnit au = n_units > 0 ? attn_locate(as, A.batch, A.n_kv_heads, ub) : AttnUnit{0, 0, 0, 1};
                     int seq_base = as.base[au.b];
                     int seq_keys = min(seq_base + as.nrows[au.b], A.kv_ctx);
+                    // a unit's first row: (page * Hkv + head) * page size + slot in page; a
+                    // contiguous cache has page = sequence (the paged variant keeps the last
+                    // page-table entry it read)
+                    const size_t layer_bytes =
+                        (size_t)A.layer * A.kvp.n_pages * A.n_kv_heads * A.kvp.page * A.head_dim * 2;
+                    [[maybe_unused]] int pg_b = -1, pg_blk = -1, pg_page = -1;
                     for (int i = 0; i < n_units; ++i) {
                         if (i > 0 && ++au.tile == au.tiles) {
                             au.tile = 0;
@@ -655,18 +663,32 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                         if (!mbar_wait(R.empty + a_slot, a_phase ^ 1u, abort_flag, err)) { ok = false; break; }
                         uint8_t* dst = R.slot(a_slot);
                         uint64_t* fb = R.full + a_slot;
+                        // the unit's first cache row (a unit never crosses a page; the last page
+                        // looked up is kept); a page not held reads row 0 and flags the error
+                        int krow;
+                        if constexpr (PAGED) {
+                            const int blk = key0 >> A.kvp.shift;
+                            if (au.b != pg_b || blk != pg_blk) {
+                                pg_b = au.b;
+                                pg_blk = blk;
+                                pg_page = A.kvp.table[(size_t)au.b * A.kvp.max_pages + blk];
+                            }
+                            krow = pg_page < 0 ? -1
+                                               : (pg_page * A.n_kv_heads + au.g) * A.kvp.page + (key0 & (A.kvp.page - 1));
+                        } else {
+                            krow = (au.b * A.n_kv_heads + au.g) * A.kv_ctx + key0;
+                        }
+                        if (krow < 0) { dev_error(err, SPEC_DEVERR_CAPACITY); krow = 0; }
                         if (A.linear) {
                             // the unit's valid K rows and V rows: two contiguous copies
                             const uint32_t bytes = (uint32_t)min(ku, seq_keys - key0) * A.head_dim * 2;
-                            const size_t off =
-                                ((((size_t)A.layer * A.kv_batch + au.b) * A.n_kv_heads + au.g) * A.kv_ctx + key0) *
-                                A.head_dim * 2;
+                            const size_t off = layer_bytes + (size_t)krow * A.head_dim * 2;
                             mbar_arrive_expect_tx(fb, 2 * bytes);
                             bulk_load(dst, static_cast<const char*>(A.kc) + off, bytes, fb, pw);
                             bulk_load(dst + kAttnUnitBytes / 2, static_cast<const char*>(A.vc) + off, bytes, fb, pw);
                         } else {
                             mbar_arrive_expect_tx(fb, kAttnUnitBytes);
-                            const int row = (au.b * A.n_kv_heads + au.g) * A.kv_ctx + key0;
+                            const int row = krow;
                             for (int db = 0; db < nbox; ++db) {
                                 tma_load_3d(dst + db * box, &P->tmW, 64 * db, row, A.layer, fb, pw);
                                 tma_load_3d(dst + (nbox + db) * box, &P->tmX, 64 * db, row, A.layer, fb, pw);
@@ -1044,10 +1066,13 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
     if (!attr_set) {
         cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncSetAttribute(gemm_tc_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         attr_set = true;
     }
     const int slot = prof_start(m, st);
-    if (ch.attn >= 0)
+    if (ch.attn >= 0 && ch.ph[ch.attn].at.kvp.shift >= 0)
+        launch_k(m->pdl, gemm_tc_kernel<true, true>, dim3(G), dim3(kTcThreads), smem, st, ch, L);
+    else if (ch.attn >= 0)
         launch_k(m->pdl, gemm_tc_kernel<true>, dim3(G), dim3(kTcThreads), smem, st, ch, L);
     else
         launch_k(m->pdl, gemm_tc_kernel<false>, dim3(G), dim3(kTcThreads), smem, st, ch, L);

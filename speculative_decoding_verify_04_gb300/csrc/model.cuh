@@ -34,6 +34,35 @@ struct RowPlan {
 };
 
 // Parameters of the plan kernel, passed by value.
+// Where slot s of sequence b lives in the cache: page table[b * max_pages +
+// s / page], row s % page of that page; a page holds `page` slots of every KV
+// head of one layer ([layer][page][kv head][slot in page][hd]).  A contiguous
+// cache is the special case of one page per sequence (page = capacity,
+// table = 0, 1, ..., batch - 1).
+struct KVPages {
+    const int* table;     // [kv batch][max_pages], -1 where no page is held
+    int page;             // slots a page (a power of two for paged caches)
+    int max_pages;        // pages a sequence can address
+    int n_pages;          // pages a layer holds
+    int shift;            // log2(page) for paged caches; -1: contiguous (sequence b is page b)
+};
+
+// Row of slot `slot` (sequence seq, KV head kvh) counted inside one layer's
+// block of the cache; -1 when the slot's page is not held.  A contiguous
+// cache needs no table read.
+SPEC_DEV long long kv_row_in_layer(const KVPages& p, int n_kv_heads, int seq, int kvh, int slot) {
+    if (p.shift < 0) return ((long long)seq * n_kv_heads + kvh) * p.page + slot;
+    const int blk = slot >> p.shift;
+    const int pg = p.table[(size_t)seq * p.max_pages + blk];
+    if (pg < 0) return -1;
+    return ((long long)pg * n_kv_heads + kvh) * p.page + (slot & (p.page - 1));
+}
+// The same row counted from the start of the cache (layer blocks of n_pages pages).
+SPEC_DEV long long kv_row(const KVPages& p, int n_kv_heads, int layer, int seq, int kvh, int slot) {
+    const long long r = kv_row_in_layer(p, n_kv_heads, seq, kvh, slot);
+    return r < 0 ? -1 : (long long)layer * p.n_pages * n_kv_heads * p.page + r;
+}
+
 struct PlanParams {
     int batch;
     int mode;                        // 0 chain, 1 tree, 2 one-row-per-sequence draft pass
@@ -147,6 +176,18 @@ struct spec_kv {
     void* k = nullptr;               // [layer][seq][kvh][slot][hd]
     void* v = nullptr;
     int* len = nullptr;              // [batch] committed lengths (device)
+    // pages: a contiguous cache is one page per sequence; a paged cache shares a
+    // pool of n_pages pages of `page` slots between its sequences
+    bool paged = false;
+    int page = 0, max_pages = 0, n_pages = 0;
+    int* table = nullptr;            // [batch][max_pages] page of each block of slots, -1 if none
+    int* free_pages = nullptr;       // paged: stack of free pages [n_pages], top at free_top[0]
+    int* free_top = nullptr;
+    spec::KVPages pages() const {
+        int sh = -1;
+        if (paged) { sh = 0; while ((1 << sh) < page) ++sh; }
+        return spec::KVPages{table, page, max_pages, n_pages, sh};
+    }
     // bf16 caches: 3-D TMA maps {head dim, seq * kvh * slot, layer} with boxes
     // of 64 dims x (8 KB / 128 B) slots, 128-byte swizzle (attention phase of the
     // GEMM chain); tmaps is false where the cache is too large to address
@@ -194,7 +235,8 @@ struct EpiParams {
     // QKV
     float* q;
     void* kc; void* vc;     // cache bases
-    int kv_batch, kv_ctx;   // cache geometry
+    int kv_ctx;             // slots a sequence can address
+    KVPages kvp;
     int n_heads, n_kv_heads, head_dim;
     const float* rope_cos; const float* rope_sin;
     int max_position;
@@ -246,13 +288,14 @@ struct AttnPhase {
     void* out;               // [rows][H hd] bf16 hi rows, then lo rows at out_lo
     size_t out_lo;
     RowPlan plan;
-    int batch, kv_batch, kv_ctx, layer;
+    int batch, kv_ctx, layer;
     int n_heads, n_kv_heads, head_dim;
     int tree;
     int linear;              // every segment has <= kAttnSimtQ query vectors: K/V arrive by plain bulk copies
                              // (rows in order) instead of swizzled tensor boxes
     const void* kc;          // cache bases (bulk copies)
     const void* vc;
+    KVPages kvp;
     float* part;             // [CTAs][2][16][hd + 2] partial softmax states
     int* counters;           // [batch * n_kv_heads] arrivals (zero between launches)
     int* err;
@@ -290,15 +333,20 @@ struct AttnParams {
     void* out;              // [rows][H hd] model dtype (O-projection input)
     size_t out_lo;          // element offset of the lo half (bf16 models)
     RowPlan plan;
-    int batch, kv_batch, kv_ctx, layer;
+    int batch, kv_ctx, layer;
     int n_heads, n_kv_heads, head_dim;
     int tree;               // 0 chain, 1 tree
+    KVPages kvp;
     int splits;
     float* part;
     int* counters;
     int* err;
 };
 int launch_attention(spec_model* m, const AttnParams& a, int max_rows_per_seq, cudaStream_t st);
+// paged caches (no-ops for contiguous ones): pages for slots below len[b] + n[b]
+// (relative) or n[b] (absolute) of sequences [0, batch); pages past the lengths back
+int kv_ensure_pages(spec_kv* kv, int batch, const int* n, bool relative, cudaStream_t st);
+int kv_release_pages(spec_kv* kv, int batch, cudaStream_t st);
 int attn_splits(const spec_model* m, int blocks, int kv_ctx);
 size_t attn_scratch_floats(const spec_model* m, int batch, int max_rows_per_seq, int kv_ctx, int* n_counters);
 size_t attn_partial_floats_needed(const spec_model* m, int batch, int max_rows_per_seq);

@@ -27,7 +27,7 @@ EXPORTS = [
     "spec_kv_export", "spec_prefill", "spec_draft", "spec_verify", "spec_accept", "spec_accept_greedy",
     "kv_commit", "spec_row_probs", "spec_schedule_k", "spec_profile", "spec_profile_read", "spec_launch_count",
     "spec_verify_noalloc", "spec_draft_sample", "spec_probs", "spec_sample", "spec_schedule_aimd",
-    "spec_schedule_decay", "spec_draft_tree",
+    "spec_schedule_decay", "spec_draft_tree", "spec_kv_create_paged", "spec_kv_free_pages", "spec_kv_page_table",
 ]
 
 
@@ -85,6 +85,9 @@ def load(path: str = LIB_PATH):
         "spec_schedule_aimd": ([P, P, P, I, POINTER(AIMDSchedule), P, P], I),
         "spec_schedule_decay": ([P, P, I, I, P, P], I),
         "spec_draft_tree": ([P, P, I, P, POINTER(I), I, P, P, P, P], I),
+        "spec_kv_create_paged": ([P, I, I, I, I, POINTER(P)], I),
+        "spec_kv_free_pages": ([P, POINTER(I), P], I),
+        "spec_kv_page_table": ([P, POINTER(I), P], I),
         "spec_accept_greedy": ([P, P, POINTER(I), I, I, I, P, P, P, P], I),
         "kv_commit": ([P, I, P, P, I, P], I),
         "spec_row_probs": ([P, I, P, P], I),
@@ -192,15 +195,36 @@ class Model:
 
 
 class KVCache:
-    """KV cache of ``batch`` sequences x ``max_ctx`` slots (owns the library handle)."""
+    """KV cache of ``batch`` sequences x ``max_ctx`` slots (owns the library handle).
 
-    def __init__(self, model: Model, batch, max_ctx):
+    With ``page`` (a multiple of 64) the cache is paged: a pool of ``n_pages``
+    pages of ``page`` slots shared by the sequences through their page tables.
+    """
+
+    def __init__(self, model: Model, batch, max_ctx, page=None, n_pages=None):
         self.model = model
         self.batch = batch
         self.max_ctx = max_ctx
+        self.page = page
         h = c_void_p()
-        _check(load().spec_kv_create(model.handle, batch, max_ctx, ctypes.byref(h)))
+        if page:
+            if n_pages is None:
+                n_pages = batch * ((max_ctx + page - 1) // page)
+            _check(load().spec_kv_create_paged(model.handle, batch, max_ctx, page, n_pages, ctypes.byref(h)))
+        else:
+            _check(load().spec_kv_create(model.handle, batch, max_ctx, ctypes.byref(h)))
         self.handle = h
+
+    def free_pages(self, stream=None):
+        n = c_int32()
+        _check(load().spec_kv_free_pages(self.handle, ctypes.byref(n), _stream(stream)))
+        return n.value
+
+    def page_table(self, stream=None):
+        cols = (self.max_ctx + self.page - 1) // self.page if self.page else 1
+        arr = (c_int32 * (self.batch * cols))()
+        _check(load().spec_kv_page_table(self.handle, arr, _stream(stream)))
+        return [list(arr[b * cols:(b + 1) * cols]) for b in range(self.batch)]
 
     def set_lengths(self, lens, stream=None):
         _check(load().spec_kv_set_lengths(self.handle, _i32_array(lens), _stream(stream)))
