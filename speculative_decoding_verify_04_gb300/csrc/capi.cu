@@ -374,7 +374,6 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             at.at.linear = max_rows_per_seq * (c.n_heads / c.n_kv_heads) <= kAttnSimtQ;
             at.at.kc = kv->k;
             at.at.vc = kv->v;
-            at.at.kvp = kv->pages();
             pend[np++] = at;
         } else {   // attention
             AttnParams a{};

@@ -640,8 +640,9 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                     // a unit's first row: (page * Hkv + head) * page size + slot in page; a
                     // contiguous cache has page = sequence (the paged variant keeps the last
                     // page-table entry it read)
+                    const KVPages& kvp = P->e.kvp;
                     const size_t layer_bytes =
-                        (size_t)A.layer * A.kvp.n_pages * A.n_kv_heads * A.kvp.page * A.head_dim * 2;
+                        (size_t)A.layer * kvp.n_pages * A.n_kv_heads * kvp.page * A.head_dim * 2;
                     [[maybe_unused]] int pg_b = -1, pg_blk = -1, pg_page = -1;
                     for (int i = 0; i < n_units; ++i) {
                         if (i > 0 && ++au.tile == au.tiles) {
@@ -667,14 +668,14 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                         // looked up is kept); a page not held reads row 0 and flags the error
                         int krow;
                         if constexpr (PAGED) {
-                            const int blk = key0 >> A.kvp.shift;
+                            const int blk = key0 >> kvp.shift;
                             if (au.b != pg_b || blk != pg_blk) {
                                 pg_b = au.b;
                                 pg_blk = blk;
-                                pg_page = A.kvp.table[(size_t)au.b * A.kvp.max_pages + blk];
+                                pg_page = kvp.table[(size_t)au.b * kvp.max_pages + blk];
                             }
                             krow = pg_page < 0 ? -1
-                                               : (pg_page * A.n_kv_heads + au.g) * A.kvp.page + (key0 & (A.kvp.page - 1));
+                                               : (pg_page * A.n_kv_heads + au.g) * kvp.page + (key0 & (kvp.page - 1));
                         } else {
                             krow = (au.b * A.n_kv_heads + au.g) * A.kv_ctx + key0;
                         }
@@ -1070,7 +1071,7 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
         attr_set = true;
     }
     const int slot = prof_start(m, st);
-    if (ch.attn >= 0 && ch.ph[ch.attn].at.kvp.shift >= 0)
+    if (ch.attn >= 0 && ch.ph[ch.attn].e.kvp.shift >= 0)
         launch_k(m->pdl, gemm_tc_kernel<true, true>, dim3(G), dim3(kTcThreads), smem, st, ch, L);
     else if (ch.attn >= 0)
         launch_k(m->pdl, gemm_tc_kernel<true>, dim3(G), dim3(kTcThreads), smem, st, ch, L);

@@ -235,9 +235,9 @@ struct EpiParams {
     // QKV
     float* q;
     void* kc; void* vc;     // cache bases
-    int kv_ctx;             // slots a sequence can address
     KVPages kvp;
     int n_heads, n_kv_heads, head_dim;
+    int kv_ctx;             // slots a sequence can address
     const float* rope_cos; const float* rope_sin;
     int max_position;
     float q_scale;
@@ -247,11 +247,10 @@ struct EpiParams {
     void* x_next;
     size_t x_next_lo;       // element offset of the lo half (bf16 models)
     float* ss_out;
-    int d_model;
     // SwiGLU
     void* act;
     size_t act_lo;
-    int d_ff;
+    int d_model, d_ff;
     // LM head
     float* logits;          // nullable; row r goes to logits[(r - logits_row0) * logits_stride]
     int logits_stride, logits_row0;
@@ -263,8 +262,9 @@ struct EpiParams {
     int* done_counter;
     // draft / acceptance outputs
     int* cand; int cand_stride; int cand_col;   // draft: cand[seq*stride + col] = argmax
-    const int* tokens; int tok_stride;           // acceptance: row tokens
+    const int* tokens;                           // acceptance: row tokens (tok_stride a sequence)
     int* acc_len; int* next_tok; int* path;
+    int tok_stride;
     int batch;
 };
 
@@ -293,9 +293,8 @@ struct AttnPhase {
     int tree;
     int linear;              // every segment has <= kAttnSimtQ query vectors: K/V arrive by plain bulk copies
                              // (rows in order) instead of swizzled tensor boxes
-    const void* kc;          // cache bases (bulk copies)
+    const void* kc;          // cache bases (bulk copies); the page table is the phase's EpiParams kvp
     const void* vc;
-    KVPages kvp;
     float* part;             // [CTAs][2][16][hd + 2] partial softmax states
     int* counters;           // [batch * n_kv_heads] arrivals (zero between launches)
     int* err;
