@@ -68,7 +68,7 @@ def parse():
                     help="paged KV cache with pages of this many slots (a power of two, at least 64); 0: contiguous")
     ap.add_argument("--tree", default=None,
                     help="greedy layer-skip token tree instead of the chain, e.g. 4,2,2 (children per node by level)")
-    ap.add_argument("--workload", default="chain", choices=["chain", "adaptive"],
+    ap.add_argument("--workload", default="chain", choices=["chain", "adaptive", "tiny", "accept", "tree8"],
                     help="chain: k=4, ctx 4096, batch 1 (or --batch); adaptive: batch 32, contexts 512..8192, "
                          "per-sequence k in [2,16] from the confidence schedule")
     return ap.parse_args()
@@ -255,6 +255,280 @@ ADAPTIVE = ("llama7b-shape layer-skip self-spec (draft 12/32 layers), batch 32, 
 B_ADAPT, K_MIN, K_MAX, K_START, EMA_START = 32, 2, 16, 2, 0.5
 
 
+def _timed(step, steps, warm, world, dist, local):
+    """Warm-up, then ``steps`` calls of ``step`` between CUDA events on the
+    current stream with SM clocks sampled; returns (seconds, clocks)."""
+    import torch
+    for _ in range(warm):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = Clocks(local)
+    clocks.start()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    sec = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        sec = reduce_max(sec, dist, "cuda")
+    return sec, clk
+
+
+def _line(args, world, steps, warm, sec, value_units, dtype, config, extra):
+    line = {"metric": METRIC, "value": job_rate(world, value_units, sec), "unit": "tokens/s", "n_gpus": world,
+            "steps": steps, "warmup": warm, "ms_per_step": sec * 1e3 / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic (seeded random-init weights and inputs; no dataset)", "config": config}
+    line.update(extra)
+    return line
+
+
+def run_tiny(args, spec, world, rank, local, dist):
+    """The tiny fp32 decoder (2 layers, d 256, 4 heads x 64, FFN 1024, vocab
+    1024, draft = layer 0 + the LM head): one step = prefill a 32-token prompt,
+    then greedy chain rounds of k = 4 until 64 tokens are out.  The host reads
+    each round's accepted length (the stopping test): part of the step."""
+    import torch
+    from synthetic import SHAPES, make_weights, make_tokens
+    shape = SHAPES["tiny"]
+    k, n_prompt, n_new = 4, 32, 64
+    w = make_weights(shape, 1 + rank, device="cuda")
+    model = spec.Model(shape, w, max_rows=64, max_batch=1, max_position=256)
+    del w
+    prompt = torch.from_numpy(make_tokens(n_prompt, shape.vocab, 1 + rank)).cuda()
+    cand = torch.empty((1, k + 1), dtype=torch.int32, device="cuda")
+    hL = torch.empty((1, k + 1, shape.d_model), dtype=torch.float32, device="cuda")
+    acc = torch.empty(1, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+    t0 = torch.empty(1, dtype=torch.int32, device="cuda")
+    acc_host = torch.empty(1, dtype=torch.int32).pin_memory()
+    log = {"rounds": 0}
+    kv = spec.KVCache(model, 1, n_prompt + n_new + k + 8)
+
+    def generate():
+        kv.set_lengths([0])
+        spec.spec_prefill(model, kv, 0, prompt, None, t0)
+        out = 1
+        while out < n_new:
+            spec.spec_draft(model, kv, t0, k, cand, hL)
+            spec.spec_verify(model, kv, [k + 1], cand, k + 1, h_in=hL, h_stride=k + 1, acc_len=acc, next_tok=nxt)
+            spec.kv_commit(kv, acc)
+            t0.copy_(nxt)
+            acc_host.copy_(acc)
+            torch.cuda.current_stream().synchronize()
+            out += int(acc_host.item()) + 1
+            log["rounds"] += 1
+
+    steps, warm = args.steps, args.warmup
+    n0 = model.launch_count()
+    sec, clk = _timed(generate, steps, warm, world, dist, local)
+    rounds = log["rounds"] * steps // (steps + warm)
+    launches = (model.launch_count() - n0) * steps // (steps + warm)
+    if model.device_error():
+        raise SystemExit("device error word set during the bench")
+    hbm, peak_kind = peaks()
+    d, F, V = shape.d_model, shape.d_ff, shape.vocab
+    w_bytes = (shape.n_layers * (4 * d * d + 3 * F * d) + 2 * V * d) * 4
+    achieved = rounds * w_bytes / sec / 1e9
+    extra = {
+        "accepted_tokens_per_s": job_rate(world, n_new * steps, sec),
+        "rounds_per_step": rounds / steps,
+        "roofline": {"bound": "hbm", "kernel": "whole generation (launch-bound: 10.5 MB of weights a round)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": peak_kind},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": {"value": job_rate(world, n_new * steps, sec), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 4 * rounds // max(steps, 1),
+                "note": "the step already reads every round's accepted length back to the host"},
+    }
+    line = _line(args, world, steps, warm, sec, rounds * (k + 1), "f32",
+                 {"workload": "tiny fp32 decoder (2 layers, d 256, vocab 1024), prompt 32, 64 tokens, chain k=4 greedy",
+                  "l2": "fits in L2 (launch-bound correctness workload)"}, extra)
+    line["value_note"] = "verified candidate tokens/s over the whole generation; accepted_tokens_per_s = 64 per step"
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import spec as OS
+        from oracle.decoder import Decoder
+        from synthetic import weights_to_numpy
+        dec = Decoder(shape, weights_to_numpy(make_weights(shape, 1, device="cpu")))
+        tw = time.perf_counter()
+        OS.generate_greedy_spec(dec, make_tokens(n_prompt, shape.vocab, 1), n_new, k)
+        t = time.perf_counter() - tw
+        line["cpu_baseline"] = {"value": n_new / t, "unit": "tokens/s (accepted)", "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": "one whole 64-token generation"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_accept(args, spec, world, rank, local, dist):
+    """The acceptance call alone: 256 sequences, k = 5, vocab 32000, p and q
+    the softmax of N(0, 9) target logits and of those plus N(0, 1) noise, draft
+    tokens drawn from q, one uniform a position plus one for the draw.  One
+    step = one spec_accept over resident inputs (360 MB, larger than L2).
+    Algorithmic bytes per sequence: the row(s) the draw reads (p_a and q_a
+    after a rejection, p_k after k acceptances) plus one 32-byte sector of p
+    and of q per ratio test."""
+    import numpy as np
+    import torch
+    from synthetic import make_accept_inputs
+    B, k, V = 256, 5, 32000
+    p, q, x, u = make_accept_inputs(B, k, V, seed=2 + rank)
+    pg, qg = torch.from_numpy(p).cuda(), torch.from_numpy(q).cuda()
+    xg, ug = torch.from_numpy(x.astype(np.int32)).cuda(), torch.from_numpy(u).cuda()
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    steps, warm = max(args.steps, 100), args.warmup
+    sec, clk = _timed(lambda: spec.spec_accept(pg, qg, xg, ug, acc, nxt), steps, warm, world, dist, local)
+    a = acc.cpu().numpy()
+    alg = sum((2 if a[b] < k else 1) * V * 4 + 2 * min(int(a[b]) + 1, k) * 32 for b in range(B))
+    hbm, peak_kind = peaks()
+    achieved = alg / (sec / steps) / 1e9
+    # e2e: the inputs copied in from pinned host memory every call, the decisions read back
+    ph, qh = torch.from_numpy(p).pin_memory(), torch.from_numpy(q).pin_memory()
+    xh, uh = torch.from_numpy(x.astype(np.int32)).pin_memory(), torch.from_numpy(u).pin_memory()
+    oh = torch.empty((2, B), dtype=torch.int32).pin_memory()
+    e_steps = 10
+    torch.cuda.synchronize()
+    tw = time.perf_counter()
+    for _ in range(e_steps):
+        pg.copy_(ph, non_blocking=True)
+        qg.copy_(qh, non_blocking=True)
+        xg.copy_(xh, non_blocking=True)
+        ug.copy_(uh, non_blocking=True)
+        spec.spec_accept(pg, qg, xg, ug, acc, nxt)
+        oh[0].copy_(acc, non_blocking=True)
+        oh[1].copy_(nxt, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - tw) / e_steps
+    if world > 1:
+        e2e_s = reduce_max(e2e_s, dist, "cuda")
+    extra = {
+        "sequences_per_s": job_rate(world, B * steps, sec),
+        "mean_accepted": float(a.mean()),
+        "roofline": {"bound": "hbm", "kernel": "accept_rows_kernel (one CTA of 768 threads a sequence)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg,
+                     "dense_bytes_per_launch": B * (2 * k + 1) * V * 4},
+        "gpu_launches": steps,
+        "clocks": clk,
+        "e2e": {"value": job_rate(world, B * k, e2e_s), "unit": "tokens/s",
+                "h2d_bytes_per_step": p.nbytes + q.nbytes + x.size * 4 + u.nbytes, "d2h_bytes_per_step": 8 * B},
+    }
+    line = _line(args, world, steps, warm, sec, B * k * steps, "f32",
+                 {"workload": "acceptance alone: batch 256, k=5, vocab 32000, logits N(0,3^2), draft = target + N(0,1)",
+                  "l2": "inputs larger than L2 (360 MB of p and q)"}, extra)
+    line["value_note"] = "draft tokens decided per second"
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import accept as A
+        n = 16
+        tw = time.perf_counter()
+        for b in range(n):
+            A.accept_sampling_chain(p[b], q[b], x[b], u[b])
+        t = (time.perf_counter() - tw) / n
+        line["cpu_baseline"] = {"value": k / t, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} of the 256 sequences, one at a time"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_tree8(args, spec, world, rank, local, dist):
+    """Tree verification: 8-layer bf16 decoder (d 1024, 16 query / 4 KV heads
+    x 64, FFN 2816, vocab 32000), a 2048-token random prompt prefilled, a
+    29-node token tree [4, 2, 2] in level order, batch 1.  One step = one
+    spec_verify over the tree from the embeddings (ancestor-only mask, depth
+    positions, fused greedy longest-path acceptance) + kv_commit of the path."""
+    import torch
+    from synthetic import SHAPES, make_weights, make_tokens, tree_parents
+    shape = SHAPES["tree8"]
+    ctx = 2048
+    par = [int(v) for v in tree_parents([4, 2, 2])]
+    n = len(par)
+    steps, warm = args.steps, args.warmup
+    cap = ctx + (steps + warm + 4) * 4 + 2 * n
+    w = make_weights(shape, 3 + rank, device="cuda")
+    model = spec.Model(shape, w, max_rows=64, max_batch=1, max_position=cap + 8)
+    del w
+    kv = spec.KVCache(model, 1, cap)
+    spec.spec_prefill(model, kv, 0, torch.from_numpy(make_tokens(ctx, shape.vocab, 3 + rank)).cuda())
+    toks = torch.from_numpy(make_tokens(n, shape.vocab, 30 + rank, "tree")).cuda().view(1, n)
+    acc = torch.empty(1, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+    path = torch.empty((1, 64), dtype=torch.int32, device="cuda")
+
+    def step():
+        spec.spec_verify(model, kv, [n], toks, n, tree_parent=par, acc_len=acc, next_tok=nxt, path=path)
+        spec.kv_commit(kv, acc, path)
+
+    n0 = model.launch_count()
+    sec, clk = _timed(step, steps, warm, world, dist, local)
+    launches = (model.launch_count() - n0) * steps // (steps + warm)
+    if model.device_error():
+        raise SystemExit("device error word set during the bench")
+    d, F, V = shape.d_model, shape.d_ff, shape.vocab
+    qkv = (shape.n_heads + 2 * shape.n_kv_heads) * shape.head_dim
+    w_bytes = shape.n_layers * (qkv * d + d * shape.n_heads * shape.head_dim + 3 * F * d) * 2 + V * d * 2
+    kv_bytes = shape.n_layers * 2 * shape.n_kv_heads * shape.head_dim * 2 * (ctx + n)
+    hbm, peak_kind = peaks()
+    achieved = (w_bytes + kv_bytes) / (sec / steps) / 1e9
+    # e2e: the tree's tokens from pinned host memory, the decision read back
+    th = toks.cpu().pin_memory()
+    oh = torch.empty((1, 66), dtype=torch.int32).pin_memory()
+    e_steps = max(3, steps // 2)
+    torch.cuda.synchronize()
+    tw = time.perf_counter()
+    for _ in range(e_steps):
+        toks.copy_(th, non_blocking=True)
+        step()
+        oh[0, :64].copy_(path[0], non_blocking=True)
+        oh[0, 64:65].copy_(acc, non_blocking=True)
+        oh[0, 65:66].copy_(nxt, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - tw) / e_steps
+    if world > 1:
+        e2e_s = reduce_max(e2e_s, dist, "cuda")
+    extra = {
+        "roofline": {"bound": "hbm", "kernel": "whole verification step (GEMM chains + tree attention)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": peak_kind, "algorithmic_bytes_per_step": w_bytes + kv_bytes},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": {"value": job_rate(world, n, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": 4 * n,
+                "d2h_bytes_per_step": 4 * 66},
+    }
+    line = _line(args, world, steps, warm, sec, n * steps, "bf16",
+                 {"workload": "tree verification: 8-layer bf16 d1024 GQA 16/4, vocab 32000, ctx 2048, tree [4,2,2]",
+                  "l2": "weights 246 MB re-streamed each step (larger than L2)"}, extra)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import spec as OS
+        from oracle.decoder import Decoder
+        from synthetic import weights_to_numpy
+        from synthetic import make_kv_context
+        dec = Decoder(shape, weights_to_numpy(make_weights(shape, 3, device="cpu")))
+        cache = dec.new_cache(ctx + n + 4)
+        kc, vc = make_kv_context(shape, 1, ctx, 3, device="cpu")
+        cache.load(kc[:, 0].float().numpy(), vc[:, 0].float().numpy())
+        tw = time.perf_counter()
+        OS.verify(dec, cache, ctx, dec.embed(toks[0].cpu().numpy()), 0, parents=par)
+        t = time.perf_counter() - tw
+        line["cpu_baseline"] = {"value": n / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": "one tree verification over a 2048-slot synthetic context"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def run_adaptive(args, spec, world, rank, local, dist):
     """Adaptive-k rounds: every sequence verifies its own k_b + 1 rows; after
     the fused acceptance, the per-row top-1 / top-2 probabilities feed the
@@ -424,6 +698,9 @@ def main():
     __graft_entry__.build()
     from speculative_decoding_verify_04_gb300 import spec
     from synthetic import SHAPES, make_weights, make_kv_context, make_tokens, make_uniforms
+    if args.workload in ("tiny", "accept", "tree8"):
+        return {"tiny": run_tiny, "accept": run_accept, "tree8": run_tree8}[args.workload](
+            args, spec, world, rank, local, dist)
     if args.workload == "adaptive":
         return run_adaptive(args, spec, world, rank, local, dist)
 
