@@ -12,7 +12,8 @@ context whose units spread over many CTAs (partial states merged across CTAs).
 * tree verification of a root with three children (ancestor-only mask).
 
 Both paths must match the oracle's logits within 2e-2 and each other within
-2e-3; the chained path must use one launch fewer per layer.
+2e-3; the chained path must use fewer launches (the attention joins the
+layer's GEMM launch; GEMMs this small otherwise launch one by one).
 """
 import os
 
@@ -88,7 +89,7 @@ def test_attention_phase_chain_gqa(lens):
         lg, launches = _run_verify(model, kv, [T_b] * len(lens), tk)
         out.append((lg, launches))
     (lf, nf), (lp, n_p) = out
-    assert n_p - nf == N_LAYERS, (nf, n_p)
+    assert nf + N_LAYERS <= n_p, (nf, n_p)
     worst = 0.0
     for b, s in enumerate(lens):
         ref = OS.verify(dec, caches[b], s, dec.embed(toks[b]), 0)
@@ -115,7 +116,7 @@ def test_attention_phase_tree_gqa():
         kv, caches = _contexts(model, dec, shape, lens, cap, seed=73)
         out.append(_run_verify(model, kv, [4] * len(lens), tk, parents))
     (lf, nf), (lp, n_p) = out
-    assert n_p - nf == N_LAYERS, (nf, n_p)
+    assert nf + N_LAYERS <= n_p, (nf, n_p)
     for b, s in enumerate(lens):
         ref = OS.verify(dec, caches[b], s, dec.embed(toks[b]), 0, parents=parents)
         rows = slice(b * 4, (b + 1) * 4)
@@ -143,7 +144,7 @@ def test_attention_phase_small_query_groups(n_rows):
         kv, caches = _contexts(model, dec, shape, lens, cap, seed=83)
         out.append(_run_verify(model, kv, n_rows, tk, vocab=shape.vocab))
     (lf, nf), (lp, n_p) = out
-    assert n_p - nf == N_LAYERS, (nf, n_p)
+    assert nf + N_LAYERS <= n_p, (nf, n_p)
     r0 = 0
     for b, s in enumerate(lens):
         n = n_rows[b]
