@@ -311,11 +311,26 @@ struct AcceptArgs {
     int* acc_len; int* next_tok;
 };
 
-__global__ void __launch_bounds__(kSampThreads, 1)
+// The acceptance streams its one or two rows from memory once: 16 warps each
+// own a contiguous segment, walked in steps of 256 tokens (8 loads a lane in
+// flight); every step's integer weight sum is kept, so the draw finds its
+// segment and step from the sums and re-reads only that step.
+constexpr int kAccThreads = 512;
+constexpr int kAccWarps = kAccThreads / 32;
+constexpr int kAccStep = 256;
+constexpr int kAccMaxSteps = 16;            // vocab <= 16 warps x 16 steps x 256 = 65536
+constexpr int kAccMaxVocab = kAccWarps * kAccMaxSteps * kAccStep;
+
+struct AccSmem {
+    unsigned long long step[kAccWarps][kAccMaxSteps];
+    unsigned long long tot[kAccWarps];
+    unsigned long long before;
+    int a, wf, sf, tok;
+};
+
+__global__ void __launch_bounds__(kAccThreads)
 accept_rows_kernel(AcceptArgs a) {
-    extern __shared__ float row[];
-    __shared__ SampSmem sm;
-    __shared__ int s_a;
+    __shared__ AccSmem sm;
     pdl_wait();
     pdl_trigger();
     const int b = blockIdx.x, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -334,29 +349,92 @@ accept_rows_kernel(AcceptArgs a) {
             }
         }
         const unsigned mask = __ballot_sync(0xffffffffu, rej);
-        if (lane == 0) s_a = mask ? (__ffs(mask) - 1) : k;
+        if (lane == 0) sm.a = mask ? (__ffs(mask) - 1) : k;
     }
     __syncthreads();
-    const int acc = s_a;
-    const int seg = ((V + kSampThreads - 1) / kSampThreads) * 32;
+    const int acc = sm.a;
+    const int seg = ((V + kAccWarps * kAccStep - 1) / (kAccWarps * kAccStep)) * kAccStep;
     const int s0 = min(V, w * seg), s1 = min(V, s0 + seg);
     const float* __restrict__ pr = a.p + ((size_t)b * (k + 1) + acc) * V;
+    const float* __restrict__ qr = a.q + ((size_t)b * k + (acc < k ? acc : 0)) * V;
+    // r_x: the residual max(0, p - q) after a rejection (one f32 subtraction), else p
+    bool resid = acc < k;
+    unsigned long long S = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        unsigned long long tot = 0;
+        int st = 0;
+        for (int base = s0; base < s1; base += kAccStep, ++st) {
+            float pv[8], qv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int x = base + i * 32 + lane;
+                pv[i] = x < s1 ? __ldg(pr + x) : 0.f;
+                qv[i] = (resid && x < s1) ? __ldg(qr + x) : 0.f;
+            }
+            unsigned long long ws = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ws += samp_weight(resid ? fmaxf(__fsub_rn(pv[i], qv[i]), 0.f) : pv[i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+            if (lane == 0) sm.step[w][st] = ws;
+            tot += ws;
+        }
+        if (lane == 0) sm.tot[w] = tot;
+        __syncthreads();
+        S = 0;
+        for (int i = 0; i < kAccWarps; ++i) S += sm.tot[i];
+        if (S != 0 || !resid) break;
+        resid = false;                         // an all-zero residual: draw from p
+        __syncthreads();
+    }
     const float uk = a.u[(size_t)b * (k + 1) + k];
-    int t = -1;
-    if (acc < k) {
-        const float* __restrict__ qr = a.q + ((size_t)b * k + acc) * V;
-        load_segment(row, s0, s1, [&](int x) { return fmaxf(__fsub_rn(__ldg(pr + x), __ldg(qr + x)), 0.f); });
-        __syncthreads();
-        t = draw(row, V, seg, uk, sm);
-    }
-    if (t < 0) {                                  // all kept, or an all-zero residual: draw from p
-        load_segment(row, s0, s1, [&](int x) { return __ldg(pr + x); });
-        __syncthreads();
-        t = draw(row, V, seg, uk, sm);
-    }
-    if (threadIdx.x == 0) {
-        a.acc_len[b] = acc;
-        a.next_tok[b] = t;
+    unsigned long long m = (unsigned long long)(uk * 16777216.0f);
+    m = m > 0xFFFFFFull ? 0xFFFFFFull : m;
+    const unsigned long long thr = m * (S >> 24) + ((m * (S & 0xFFFFFFull)) >> 24);   // < S when S > 0
+    if (w == 0) {
+        // segment: inclusive prefix of the segment totals over lanes 0..15
+        unsigned long long t = lane < kAccWarps ? sm.tot[lane] : 0ull, inc = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long nb = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += nb;
+        }
+        const unsigned hw = __ballot_sync(0xffffffffu, lane < kAccWarps && inc > thr);
+        const int wf = hw ? __ffs(hw) - 1 : 0;
+        unsigned long long before = __shfl_sync(0xffffffffu, inc - t, wf);
+        // step inside that segment
+        const int n_st = (min(V, wf * seg + seg) - min(V, wf * seg) + kAccStep - 1) / kAccStep;
+        unsigned long long u2 = lane < n_st ? sm.step[wf][lane] : 0ull, inc2 = u2;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long nb = __shfl_up_sync(0xffffffffu, inc2, o);
+            if (lane >= o) inc2 += nb;
+        }
+        const unsigned hs = __ballot_sync(0xffffffffu, lane < n_st && before + inc2 > thr);
+        const int sf = hs ? __ffs(hs) - 1 : 0;
+        before += __shfl_sync(0xffffffffu, inc2 - u2, sf);
+        // the token inside that step, in index order
+        const int g0 = min(V, wf * seg), g1 = min(V, g0 + seg);
+        const int base = g0 + sf * kAccStep;
+        int found = -1;
+        for (int i = 0; i < 8 && found < 0; ++i) {
+            const int x = base + i * 32 + lane;
+            float r = 0.f;
+            if (x < g1) r = resid ? fmaxf(__fsub_rn(__ldg(pr + x), __ldg(qr + x)), 0.f) : __ldg(pr + x);
+            unsigned long long incx = samp_weight(r);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long nb = __shfl_up_sync(0xffffffffu, incx, o);
+                if (lane >= o) incx += nb;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, x < g1 && before + incx > thr);
+            if (hit) found = base + i * 32 + __ffs(hit) - 1;
+            before += __shfl_sync(0xffffffffu, incx, 31);
+        }
+        if (lane == 0) {
+            a.acc_len[b] = acc;
+            a.next_tok[b] = S != 0 ? found : -1;
+        }
     }
 }
 
@@ -377,16 +455,9 @@ int launch_sample_rows(const SampleArgs& a, bool pdl, cudaStream_t st) {
 }
 
 static int launch_accept_rows(const AcceptArgs& a, int batch, cudaStream_t st) {
-    if (a.V < 1 || a.V > kSampMaxVocab)
-        return set_error(SPEC_ERR_UNSUPPORTED, "spec_accept: vocab must be in [1, 53248]");
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(accept_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSampMaxVocab * 4);
-        if (e != cudaSuccess) return check_cuda(e, "acceptance kernel attribute");
-        attr_set = true;
-    }
-    cudaError_t e = launch_k(false, accept_rows_kernel, dim3(batch), dim3(kSampThreads), (size_t)a.V * 4, st, a);
+    if (a.V < 1 || a.V > kAccMaxVocab)
+        return set_error(SPEC_ERR_UNSUPPORTED, "spec_accept: vocab must be in [1, 65536]");
+    cudaError_t e = launch_k(false, accept_rows_kernel, dim3(batch), dim3(kAccThreads), 0, st, a);
     return check_cuda(e, "spec_accept launch");
 }
 
