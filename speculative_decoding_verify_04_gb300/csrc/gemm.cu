@@ -379,7 +379,7 @@ SPEC_DEV void head_tile_done(const EpiParams& e, int n_tiles, EpiSmem& sm) {
 // One finished segment of a tile.  `load(ch, v)` gives this thread's 16 values
 // (feature mm = etid(), rows ch*16 .. ch*16+15) of the segment's accumulator;
 // `release()` is called once every value has been read.
-template <typename XT, int U = 2, typename Loader>
+template <typename XT, typename Loader>
 SPEC_DEV void finish_segment(const EpiParams& e, const Split& sp, int tile, int slot, int nc,
                              EpiSmem& sm, Loader& ld, float (&hv)[kRowChunk], bool hv_ready) {
     const int mm = etid();
@@ -422,22 +422,7 @@ SPEC_DEV void finish_segment(const EpiParams& e, const Split& sp, int tile, int 
         float acc[kRowChunk];
 #pragma unroll
         for (int i = 0; i < kRowChunk; ++i) acc[i] = 0.f;
-        // slots in a fixed order (deterministic sums), U slots' loads in flight at a time
-        int q = 0;
-        for (; q + U <= nc; q += U) {
-            const float* src0 = base + ((size_t)q * sp.T_pad + ch * kRowChunk) * kTileN + mm;
-            float v[U][kRowChunk];
-#pragma unroll
-            for (int uu = 0; uu < U; ++uu)
-#pragma unroll
-                for (int i = 0; i < kRowChunk; ++i)
-                    v[uu][i] = (i < nr) ? __ldcg(src0 + ((size_t)uu * sp.T_pad + i) * kTileN) : 0.f;
-#pragma unroll
-            for (int uu = 0; uu < U; ++uu)
-#pragma unroll
-                for (int i = 0; i < kRowChunk; ++i) acc[i] += v[uu][i];
-        }
-        for (; q < nc; ++q) {
+        for (int q = 0; q < nc; ++q) {           // slots in a fixed order: deterministic sums
             const float* src = base + ((size_t)q * sp.T_pad + ch * kRowChunk) * kTileN + mm;
             float v2[kRowChunk];
 #pragma unroll
@@ -861,8 +846,7 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                     if (!w_ok) { ok = false; break; }
                     acc_phase ^= 1u;
                     tc_fence_after();
-                    finish_segment<__nv_bfloat16, 2>(P.e, sp, tile, c - first, last - first + 1, sm, ld, hv,
-                                                                  hv_ready);
+                    finish_segment<__nv_bfloat16>(P.e, sp, tile, c - first, last - first + 1, sm, ld, hv, hv_ready);
                     u = seg_end;
                 }
             }
