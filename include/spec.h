@@ -293,7 +293,8 @@ int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows
  * Ratio test u_j * q_j(x) < p_j(x) exactly (q_j(x) = 0 rejects); the draw
  * (residual max(0, p - q) in f32, or p when that is all zero, or the bonus
  * row p_k) is an integer inverse CDF over w = floor(r * 2^32) driven by
- * u[k].  Bit-exact and deterministic.  async. */
+ * u[k].  Bit-exact and deterministic.  1 <= k <= 32, vocab <= 65536; a
+ * target row of all zeros (invalid input) gives next_tok -1.  async. */
 int spec_accept(const float* p, const float* q, const int32_t* draft, int32_t draft_stride,
                 const float* u, int32_t batch, int32_t k, int32_t vocab, int32_t* acc_len,
                 int32_t* next_tok, void* stream);
