@@ -949,7 +949,7 @@ gemm_f32_kernel(const float* __restrict__ W, const float* __restrict__ X, int x_
 
 // ---------------------------------------------------------------------------
 // host launch
-constexpr int kMaxSlices = 4;
+constexpr int kMaxSlices = 8;
 constexpr double kChainMinPhaseBytes = 16.0 * 1024 * 1024;
 
 static int max_slots_of(const Split& s) {
