@@ -33,6 +33,7 @@
 //          (top1, argmax, top2, sum exp); the last tile of the launch merges
 //          them per row and applies the draft pick or greedy acceptance.
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <cudaTypedefs.h>
@@ -966,10 +967,13 @@ static Split make_split(const spec_model* m, int N, int K, int T_pad) {
     s.n_tiles = (N + kTileN - 1) / kTileN;
     s.kb = (K + kTileK - 1) / kTileK;
     s.units = (long long)s.n_tiles * s.kb;
-    // at most about kMaxSlices CTAs share a tile: the last one to finish adds the
-    // others' partial tiles, so small GEMMs (few k-blocks a tile) take fewer CTAs
-    // rather than a deep reduction at the end of the phase
-    s.G = (int)std::min<long long>(std::min<long long>(m->num_sms, s.units), (long long)kMaxSlices * s.n_tiles);
+    // CTAs a tile: the last one to finish adds the others' partial tiles, one
+    // slot after another (about 1 us each), while each k-block a CTA streams costs
+    // about 0.36 us (16 KB at an SM's share of the bandwidth); about sqrt(0.36 kb)
+    // slices balance the two, at most kMaxSlices.  The large GEMMs still fill
+    // every SM; small ones (few k-blocks a tile) take fewer CTAs.
+    const int slices = std::min(kMaxSlices, std::max(2, (int)std::ceil(std::sqrt(0.36 * s.kb))));
+    s.G = (int)std::min<long long>(std::min<long long>(m->num_sms, s.units), (long long)slices * s.n_tiles);
     s.T_pad = T_pad;
     s.max_slots = max_slots_of(s);
     return s;
