@@ -115,55 +115,64 @@ def peaks():
 
 # ---------------------------------------------------------------------------
 # CPU oracle timing (sampled round, scaled)
-def oracle_round_sample(batch, budget_s=20.0, k=K_DRAFT, ctx=CTX):
-    """Time the float64 oracle on a bounded sample of one round and scale it.
+class OracleRoundSample:
+    """The float64 oracle on a bounded sample of one round, scaled to the round.
 
     Sample: one decoder layer of the 7B shape with 1 row (a draft pass) and
-    with k+1 rows (a verify pass) over a 4096-token context, and the LM head
+    with k+1 rows (a verify pass) over a ``ctx``-token context, and the LM head
     with 1 and k+1 rows.  A round is 5 x 12 one-row layer passes + 4 one-row
-    heads + 20 (k+1)-row layer passes + one (k+1)-row head per sequence.
-    Returns (seconds per round for ``batch`` sequences, sample description,
-    threads).
+    heads + 20 (k+1)-row layer passes + one (k+1)-row head per sequence.  The
+    weights and the context are built once; every ``run`` times the sample.
     """
-    import numpy as np
-    import dataclasses
-    import torch
-    from synthetic import SHAPES, make_weights, weights_to_numpy, make_kv_context
-    from oracle.decoder import Decoder
-    shape = dataclasses.replace(SHAPES["llama7b"], n_layers=1, exit_layer=0)
-    w = weights_to_numpy(make_weights(shape, SEED, device="cpu"))
-    dec = Decoder(shape, w)
-    kc, vc = make_kv_context(shape, 1, ctx, SEED, device="cpu")
-    cache = dec.new_cache(ctx + k + 2)
-    cache.load(kc[:, 0].float().numpy(), vc[:, 0].float().numpy())
-    rng = np.random.default_rng(0)
 
-    def layer(rows):
-        h = rng.standard_normal((rows, shape.d_model)) * 0.02
-        pos = ctx + np.arange(rows)
-        vis = [np.arange(ctx + r + 1) for r in range(rows)]
+    def __init__(self, k=K_DRAFT, ctx=CTX):
+        import numpy as np
+        import dataclasses
+        from synthetic import SHAPES, make_weights, weights_to_numpy, make_kv_context
+        from oracle.decoder import Decoder
+        self.k, self.ctx = k, ctx
+        self.shape = dataclasses.replace(SHAPES["llama7b"], n_layers=1, exit_layer=0)
+        self.dec = Decoder(self.shape, weights_to_numpy(make_weights(self.shape, SEED, device="cpu")))
+        kc, vc = make_kv_context(self.shape, 1, ctx, SEED, device="cpu")
+        self.cache = self.dec.new_cache(ctx + k + 2)
+        self.cache.load(kc[:, 0].float().numpy(), vc[:, 0].float().numpy())
+        self.rng = np.random.default_rng(0)
+
+    def _layer(self, rows):
+        import numpy as np
+        h = self.rng.standard_normal((rows, self.shape.d_model)) * 0.02
+        pos = self.ctx + np.arange(rows)
+        vis = [np.arange(self.ctx + r + 1) for r in range(rows)]
         t = time.perf_counter()
-        dec.layer(0, h, pos, pos, vis, cache)
+        self.dec.layer(0, h, pos, pos, vis, self.cache)
         return time.perf_counter() - t
 
-    def head(rows):
-        h = rng.standard_normal((rows, shape.d_model))
+    def _head(self, rows):
+        h = self.rng.standard_normal((rows, self.shape.d_model))
         t = time.perf_counter()
-        dec.logits(h)
+        self.dec.logits(h)
         return time.perf_counter() - t
 
-    t1, t5, h1, h5 = layer(1), layer(k + 1), head(1), head(k + 1)
-    per_seq = (k + 1) * 12 * t1 + k * h1 + 20 * t5 + h5
-    threads = torch.get_num_threads()
-    try:
-        import threadpoolctl
-        info = threadpoolctl.threadpool_info()
-        threads = max([i.get("num_threads", 1) for i in info] + [1])
-    except Exception:
-        pass
-    desc = (f"one 7B-shape layer at 1 and {k + 1} rows and the LM head at 1 and {k + 1} rows "
-            f"over a {ctx}-token context, scaled to a round ({k + 1}x12 + 20 layer passes, {k + 1} heads)")
-    return per_seq * batch, desc, threads
+    def run(self, batch):
+        """(seconds per round for ``batch`` sequences, sample description, threads)."""
+        import torch
+        k = self.k
+        t1, t5, h1, h5 = self._layer(1), self._layer(k + 1), self._head(1), self._head(k + 1)
+        per_seq = (k + 1) * 12 * t1 + k * h1 + 20 * t5 + h5
+        threads = torch.get_num_threads()
+        try:
+            import threadpoolctl
+            info = threadpoolctl.threadpool_info()
+            threads = max([i.get("num_threads", 1) for i in info] + [1])
+        except Exception:
+            pass
+        desc = (f"one 7B-shape layer at 1 and {k + 1} rows and the LM head at 1 and {k + 1} rows "
+                f"over a {self.ctx}-token context, scaled to a round ({k + 1}x12 + 20 layer passes, {k + 1} heads)")
+        return per_seq * batch, desc, threads
+
+
+def oracle_round_sample(batch, k=K_DRAFT, ctx=CTX):
+    return OracleRoundSample(k, ctx).run(batch)
 
 
 def run_reference(args):
@@ -173,8 +182,9 @@ def run_reference(args):
     cores = os.cpu_count()
     times = []
     desc, threads = "", cores
+    sample = OracleRoundSample()          # weights and context built once, outside the steps
     for i in range(args.warmup + args.steps):
-        t, desc, threads = oracle_round_sample(args.batch)
+        t, desc, threads = sample.run(args.batch)
         if i >= args.warmup:
             times.append(t)
     per_round = statistics.mean(times)
