@@ -59,7 +59,7 @@ extern "C" {
 #define SPEC_ERR_CAPACITY    -2   /* rows, batch or context beyond the limits   */
 #define SPEC_ERR_CUDA        -3   /* a CUDA runtime call failed                 */
 #define SPEC_ERR_DEVICE      -4   /* device error word was set                  */
-#define SPEC_ERR_UNSUPPORTED -5   /* shape or mode this build does not handle   */
+#define SPEC_ERR_UNSUPPORTED -5   /* shape or mode the library does not handle  */
 
 #define SPEC_DTYPE_F32  0
 #define SPEC_DTYPE_BF16 1
@@ -74,7 +74,7 @@ typedef struct spec_model spec_model;
 typedef struct spec_kv spec_kv;
 
 /* Llama-style decoder: RMSNorm, rotate-half RoPE, GQA attention, SwiGLU FFN,
- * untied LM head, no biases.  Limits of this build: head_dim in {64, 128};
+ * untied LM head, no biases.  Limits of the library: head_dim in {64, 128};
  * n_heads a multiple of n_kv_heads; d_model, n_heads*head_dim and d_ff
  * multiples of 64; bf16 weights run on the tcgen05 tensor-core GEMM, f32
  * weights on a CUDA-core GEMM. */
