@@ -153,3 +153,62 @@ def test_paged_pool_exhaustion_sets_the_error():
     spec.spec_prefill(model, kv, 1, cuda_i32(make_tokens(10, shape.vocab, seed=4)))      # no page left
     torch.cuda.synchronize()
     assert model.device_error() & spec.DEVERR_CAPACITY
+
+
+def test_paged_sampling_and_tree_drafts_match_contiguous():
+    """The sampling draft and the layer-skip tree draft write the draft's KV
+    through the page table too: two rounds of each on a paged cache give the
+    contiguous cache's tokens, probabilities and logits bit for bit."""
+    from speculative_decoding_verify_04_gb300 import spec
+    from synthetic import make_uniforms
+    lib()
+    model, dec, shape = model_pair(SHAPES["tiny"], seed=1, max_rows=64, max_batch=2, max_position=512)
+    B, k, cap, n_pages, T = 2, 4, 256, 6, 0.8
+    par = [int(x) for x in tree_parents([3, 2])]
+    n = len(par)
+    kv_c = spec.KVCache(model, B, cap)
+    kv_p = spec.KVCache(model, B, cap, page=PAGE, n_pages=n_pages)
+    for b, ln in enumerate([60, 100]):
+        pr = cuda_i32(make_tokens(ln, shape.vocab, seed=50 + b))
+        spec.spec_prefill(model, kv_c, b, pr)
+        spec.spec_prefill(model, kv_p, b, pr)
+    out = {}
+    for name, kv in (("c", kv_c), ("p", kv_p)):
+        t0 = cuda_i32(make_tokens(B, shape.vocab, seed=60))
+        log = []
+        for rnd in range(2):
+            ud = torch.from_numpy(make_uniforms((B, k), seed=70 + rnd, name="ud")).cuda()
+            ua = torch.from_numpy(make_uniforms((B, k + 1), seed=70 + rnd, name="ua")).cuda()
+            cand = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
+            hL = torch.empty((B, k + 1, shape.d_model), dtype=torch.float32, device="cuda")
+            q = torch.empty((B, k, shape.vocab), dtype=torch.float32, device="cuda")
+            lg = torch.empty((B * (k + 1), shape.vocab), dtype=torch.float32, device="cuda")
+            p = torch.empty_like(lg)
+            acc = torch.empty(B, dtype=torch.int32, device="cuda")
+            nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+            spec.spec_draft_sample(model, kv, t0, k, T, ud, cand, hL, q)
+            spec.spec_verify(model, kv, [k + 1] * B, cand, k + 1, h_in=hL, h_stride=k + 1, logits=lg)
+            spec.spec_probs(lg, p, T)
+            spec.spec_accept(p.view(B, k + 1, shape.vocab), q, cand[:, 1:], ua, acc, nxt)
+            spec.kv_commit(kv, acc)
+            t0 = nxt.clone()
+            # a layer-skip tree round from the emitted token
+            toks = torch.empty((B, n), dtype=torch.int32, device="cuda")
+            th = torch.empty((B, n, shape.d_model), dtype=torch.float32, device="cuda")
+            scratch = torch.empty((B * n, shape.vocab), dtype=torch.float32, device="cuda")
+            tl = torch.empty((B * n, shape.vocab), dtype=torch.float32, device="cuda")
+            path = torch.full((B, 64), -1, dtype=torch.int32, device="cuda")
+            spec.spec_draft_tree(model, kv, t0, par, toks, th, scratch)
+            spec.spec_verify(model, kv, [n] * B, toks, n, h_in=th, h_stride=n, tree_parent=par, logits=tl,
+                             acc_len=acc, next_tok=nxt, path=path)
+            spec.kv_commit(kv, acc, path)
+            torch.cuda.synchronize()
+            assert model.device_error() == 0
+            log.append([x.cpu() for x in (cand, q, lg, p, toks, tl, acc, nxt)] + [kv.get_lengths()])
+            t0 = nxt.clone()
+        out[name] = log
+    for rc, rp in zip(out["c"], out["p"]):
+        for a, b in zip(rc[:-1], rp[:-1]):
+            assert torch.equal(a, b)
+        assert rc[-1] == rp[-1]
+    _check_pages(kv_p, n_pages)
