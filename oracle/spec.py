@@ -145,6 +145,100 @@ def generate_greedy_tree_spec(dec, prompt, n_new, parents, max_ctx=None, log=Non
     return out[:n_new]
 
 
+def child_count(row, width, mass):
+    """Children of a node under the dynamic tree width (FlashSpec page,
+    lnrk.cn/news/47842, §6.2: the draft judges its own confidence; a node it
+    is sure of is not widened, an unsure one gets more branches).
+
+    Reading: the children are the node's best draft tokens, best first, and
+    their number is the fewest whose draft probabilities (softmax of the
+    draft logits at temperature 1, float64) add up to at least ``mass``, at
+    least one and at most ``width``.  ``mass`` <= 0 gives one child (a
+    chain), ``mass`` > 1 always ``width`` (the static tree).
+    """
+    z = np.asarray(row, dtype=np.float64)
+    e = np.exp(z - z.max())
+    p = e / e.sum()
+    cum = 0.0
+    for c, x in enumerate(top_children(row, width), start=1):
+        cum += p[x]
+        if cum >= mass:
+            return c
+    return width
+
+
+def draft_tree_dynamic(dec, cache, s, t0, branching, mass):
+    """Layer-skip draft of a tree whose width follows the draft's confidence.
+
+    As :func:`draft_tree`, level by level, but node i of level l gets
+    ``child_count(draft logits of i, branching[l], mass)`` children, the
+    best draft tokens of its row in order; children are numbered in level
+    order (the children of earlier nodes first).  ``branching`` bounds the
+    tree: at most branching[l] children a node of level l, depth
+    len(branching).  Returns ``(tokens[n], parents[n], h_L[n, d],
+    draft_logits[n, V] (rows of the nodes with children, else zero))``.
+    """
+    L = dec.shape.exit_layer
+    tokens, parents = [int(t0)], [-1]
+    hs, lgs = {}, {}
+    level = [0]
+    for lev in range(len(branching) + 1):
+        vis_all = tree_visibility(s, parents)
+        h = dec.embed([tokens[i] for i in level])
+        h = dec.run_layers(h, 0, L, [s + lev] * len(level), [s + i for i in level], [vis_all[i] for i in level],
+                           cache)
+        for r, i in enumerate(level):
+            hs[i] = h[r]
+        if lev == len(branching):
+            break
+        lg = dec.logits(h)
+        nxt = []
+        for r, i in enumerate(level):
+            lgs[i] = lg[r]
+            for tok in top_children(lg[r], child_count(lg[r], branching[lev], mass)):
+                tokens.append(tok)
+                parents.append(i)
+                nxt.append(len(tokens) - 1)
+        level = nxt
+    n = len(tokens)
+    h_l = np.stack([hs[i] for i in range(n)])
+    logit_rows = np.zeros((n, dec.shape.vocab))
+    for i, row in lgs.items():
+        logit_rows[i] = row
+    return tokens, parents, h_l, logit_rows
+
+
+def tree_round_dynamic(dec, cache, t0, branching, mass):
+    """One greedy round of the layer-skip tree of dynamic width: the draft
+    tree, layers [L, N) over its nodes (tree mask), greedy tree acceptance,
+    commit of the path.  Returns ``(emitted, depth, path, next, tokens,
+    parents, target_logits)``."""
+    s = cache.length
+    L = dec.shape.exit_layer
+    tokens, parents, hL, _ = draft_tree_dynamic(dec, cache, s, t0, branching, mass)
+    logits = verify(dec, cache, s, hL, L, parents=parents)
+    depth, node, path, nxt = accept_greedy_tree(tokens, parents, logits)
+    moves, new_len = commit_tree_moves(s, path)
+    apply_moves(cache, moves)
+    cache.length = new_len
+    return [tokens[i] for i in path[1:]] + [nxt], depth, path, nxt, tokens, parents, logits
+
+
+def generate_greedy_dynamic_tree_spec(dec, prompt, n_new, branching, mass, max_ctx=None, log=None):
+    """Greedy decoding by dynamic-width tree rounds; equals :func:`generate_greedy_ar`."""
+    n_max = sum(int(np.prod(branching[:l])) for l in range(len(branching) + 1))
+    cache = dec.new_cache(max_ctx or (len(prompt) + n_new + n_max + 2))
+    t0 = argmax_lowest(dec.prefill(cache, prompt))
+    out = [t0]
+    while len(out) < n_new:
+        s = cache.length
+        emitted, depth, _, t0, tokens, _, _ = tree_round_dynamic(dec, cache, t0, branching, mass)
+        out += emitted
+        if log is not None:
+            log.append((s, depth, len(tokens)))
+    return out[:n_new]
+
+
 def chain_visibility(s, T):
     return [np.arange(0, s + t + 1) for t in range(T)]
 

@@ -253,3 +253,90 @@ def test_greedy_tree_spec_equals_greedy_ar(deep, branching):
     log = []
     assert S.generate_greedy_tree_spec(deep, pr, 40, tree_parents(branching), log=log) == ar
     assert any(d > 0 for _, d in log)
+
+
+# -- dynamic tree width --------------------------------------------------------
+def test_child_count_hand_example():
+    # draft probabilities 0.15, 0.5, 0.05, 0.3 (ids 0..3): best first 1, 3, 0, 2
+    row = np.log(np.array([0.15, 0.5, 0.05, 0.3])) + 3.0
+    assert [S.child_count(row, 4, m) for m in (0.0, 0.49, 0.79, 0.81, 0.94, 0.96, 2.0)] == [1, 1, 2, 3, 3, 4, 4]
+    assert S.child_count(row, 2, 0.96) == 2 and S.child_count(row, 1, 0.96) == 1
+    # five equal logits: the mass counts probabilities (0.2 each), not logits
+    assert S.child_count(np.zeros(5), 5, 0.5) == 3 and S.child_count(np.zeros(5), 5, 0.39) == 2
+
+
+def test_dynamic_tree_without_mass_is_the_chain_draft(deep):
+    pr = make_tokens(10, deep.shape.vocab, seed=8)
+    c1, c2 = deep.new_cache(64), deep.new_cache(64)
+    t0 = argmax_lowest(deep.prefill(c1, pr))
+    deep.prefill(c2, pr)
+    d, hL, lg, _ = S.draft(deep, c1, c1.length, t0, 3)
+    toks, par, hs, lgs = S.draft_tree_dynamic(deep, c2, c2.length, t0, [4, 2, 2], 0.0)
+    assert par == [-1, 0, 1, 2] and toks == [t0] + list(d)
+    np.testing.assert_array_equal(hs, hL)
+    np.testing.assert_array_equal(lgs[:3], lg)
+
+
+def test_dynamic_tree_at_full_mass_is_the_static_tree(deep):
+    pr = make_tokens(10, deep.shape.vocab, seed=9)
+    c1, c2 = deep.new_cache(64), deep.new_cache(64)
+    t0 = argmax_lowest(deep.prefill(c1, pr))
+    deep.prefill(c2, pr)
+    want = tree_parents([4, 2, 2])
+    toks, hs, lgs = S.draft_tree(deep, c1, c1.length, t0, want)
+    toks2, par, hs2, lgs2 = S.draft_tree_dynamic(deep, c2, c2.length, t0, [4, 2, 2], 2.0)
+    assert par == [int(x) for x in want] and toks2 == toks
+    np.testing.assert_array_equal(hs2, hs)
+    np.testing.assert_array_equal(lgs2, lgs)
+
+
+def _paths(tokens, parents):
+    out = set()
+    for i in range(len(tokens)):
+        p, x = [], i
+        while x >= 0:
+            p.append(tokens[x])
+            x = parents[x]
+        out.add(tuple(reversed(p)))
+    return out
+
+
+def test_dynamic_trees_nest_and_follow_the_rule(deep):
+    """A larger mass never removes a node: every token path of the tree at a
+    smaller mass is a path of the tree at a larger one; each node's child count
+    is child_count of its own draft row and its children are that row's best
+    tokens in order; children are numbered in level order."""
+    pr = make_tokens(12, deep.shape.vocab, seed=10)
+    trees = []
+    widths = set()
+    for mass in (0.0, 0.3, 0.6, 0.9, 2.0):
+        c = deep.new_cache(96)
+        t0 = argmax_lowest(deep.prefill(c, pr))
+        toks, par, hs, lgs = S.draft_tree_dynamic(deep, c, c.length, t0, [4, 2, 2], mass)
+        depth = [0] + [0] * (len(par) - 1)
+        for i in range(1, len(par)):
+            assert 0 <= par[i] < i and par[i] >= par[i - 1]
+            depth[i] = depth[par[i]] + 1
+        for i in range(len(par)):
+            kids = [j for j in range(len(par)) if par[j] == i]
+            if depth[i] < 3:
+                w = [4, 2, 2][depth[i]]
+                assert len(kids) == S.child_count(lgs[i], w, mass)
+                assert [toks[j] for j in kids] == S.top_children(lgs[i], len(kids))
+                widths.add(len(kids))
+            else:
+                assert not kids
+        trees.append(_paths(toks, par))
+    for a, b in zip(trees, trees[1:]):
+        assert a <= b
+    assert len(trees[0]) == 4 and len(trees[-1]) == 29
+    assert 1 in widths and len(widths) > 2
+
+
+@pytest.mark.parametrize("mass", [0.3, 0.7, 0.95])
+def test_greedy_dynamic_tree_spec_equals_greedy_ar(deep, mass):
+    pr = make_tokens(10, deep.shape.vocab, seed=8)
+    ar = S.generate_greedy_ar(deep, pr, 40)
+    log = []
+    assert S.generate_greedy_dynamic_tree_spec(deep, pr, 40, [4, 2, 2], mass, log=log) == ar
+    assert any(d > 0 for _, d, _ in log)
