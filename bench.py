@@ -20,6 +20,12 @@ grows a 29-node token tree level by level (spec_draft_tree), verify runs
 layers 12..31 over all nodes with the tree mask and fused greedy tree
 acceptance, kv_commit compacts the accepted path.
 
+--tree 4,2,2 --tree-mass 0.8 makes the tree's width follow the draft's
+confidence (spec_draft_tree_dynamic): a node gets the fewest of its best draft
+tokens whose draft probability reaches the mass, at most the level's
+branching, one tree a sequence; the node counts are read back and
+spec_verify_trees verifies each sequence's own tree.
+
 --page 64 keeps the KV cache in 64-slot pages (page tables, pages taken before
 each write and returned past the committed length at every commit).
 
@@ -68,6 +74,9 @@ def parse():
                     help="paged KV cache with pages of this many slots (a power of two, at least 64); 0: contiguous")
     ap.add_argument("--tree", default=None,
                     help="greedy layer-skip token tree instead of the chain, e.g. 4,2,2 (children per node by level)")
+    ap.add_argument("--tree-mass", type=float, default=None,
+                    help="with --tree: dynamic width, children of a node = its fewest best draft tokens whose "
+                         "draft probability reaches this mass (at most the level's branching)")
     ap.add_argument("--workload", default="chain", choices=["chain", "adaptive", "tiny", "accept", "tree8"],
                     help="chain: k=4, ctx 4096, batch 1 (or --batch); adaptive: batch 32, contexts 512..8192, "
                          "per-sequence k in [2,16] from the confidence schedule")
@@ -760,6 +769,13 @@ def main():
         hL = torch.empty((B, n_cand, shape.d_model), dtype=torch.float32, device="cuda")
         tree_scratch = torch.empty((B * n_cand, shape.vocab), dtype=torch.float32, device="cuda")
         path = torch.empty((B, 64), dtype=torch.int32, device="cuda")
+    dynamic = args.tree_mass is not None
+    if dynamic:
+        if not tree:
+            raise SystemExit("--tree-mass needs --tree")
+        parents_t = torch.empty((B, n_cand), dtype=torch.int32, device="cuda")
+        n_nodes_t = torch.empty(B, dtype=torch.int32, device="cuda")
+    nodes_log = []
     sampling = args.mode == "sample"
     V = shape.vocab
     if sampling:
@@ -773,6 +789,10 @@ def main():
     rnd = [0]
 
     def draft(ud=None):
+        if dynamic:
+            spec.spec_draft_tree_dynamic(model, kv, t0, tree_arg, args.tree_mass, tokens_t, parents_t, n_nodes_t, hL,
+                                         tree_scratch)
+            return n_nodes_t.tolist()          # the node counts size the verify call (host)
         if tree:
             spec.spec_draft_tree(model, kv, t0, tree, tokens_t, hL, tree_scratch)
         elif sampling:
@@ -780,8 +800,11 @@ def main():
         else:
             spec.spec_draft(model, kv, t0, k, cand, hL)
 
-    def verify(ua=None):
-        if tree:
+    def verify(ua=None, n_host=None):
+        if dynamic:
+            spec.spec_verify_trees(model, kv, n_host, tokens_t, n_cand, parents_t, n_cand, h_in=hL, h_stride=n_cand,
+                                   acc_len=acc, next_tok=nxt, path=path)
+        elif tree:
             spec.spec_verify(model, kv, [n_cand] * B, tokens_t, n_cand, h_in=hL, h_stride=n_cand, tree_parent=tree,
                              acc_len=acc, next_tok=nxt, path=path)
         elif sampling:
@@ -795,10 +818,12 @@ def main():
     def step(i=None):
         j = rnd[0]
         rnd[0] += 1
-        draft(u_draft[j] if sampling else None)
+        n_host = draft(u_draft[j] if sampling else None)
         if i is not None:
             ev_v0[i].record(stream)
-        verify(u_acc[j] if sampling else None)
+            if dynamic:
+                nodes_log.append(sum(n_host))
+        verify(u_acc[j] if sampling else None, n_host)
         if i is not None:
             ev_v1[i].record(stream)
             acc_log[i].copy_(acc)
@@ -859,14 +884,16 @@ def main():
         ud_dev, ua_dev = torch.empty_like(u_draft[0]), torch.empty_like(u_acc[0])
         h2d += 4 * B * k + 4 * B * (k + 1)
     torch.cuda.synchronize()
+    e2e_cand = 0
     tw0 = time.perf_counter()
     for e in range(e_steps):
         t0.copy_(t0_host, non_blocking=True)
         if sampling:
             ud_dev.copy_(ud_host[e], non_blocking=True)
             ua_dev.copy_(ua_host[e], non_blocking=True)
-        draft(ud_dev if sampling else None)
-        verify(ua_dev if sampling else None)
+        n_host = draft(ud_dev if sampling else None)
+        e2e_cand += sum(n_host) if dynamic else B * n_cand
+        verify(ua_dev if sampling else None, n_host)
         spec.kv_commit(kv, acc, path if tree else None)
         res_dev[:, :n_cand].copy_(tokens_t if tree else cand)
         res_dev[:, n_cand].copy_(acc)
@@ -877,10 +904,11 @@ def main():
     e2e_s = (time.perf_counter() - tw0) / e_steps
     if world > 1:
         e2e_s = reduce_max(e2e_s, dist, "cuda")
-    e2e_val = job_rate(world, B * n_cand, e2e_s)
+    e2e_val = job_rate(world, e2e_cand / e_steps, e2e_s)
 
     hbm, peak_kind = peaks()
-    cand_per_step = B * n_cand
+    # candidate rows verified a round: the full tree, or the dynamic trees' node counts
+    cand_per_step = B * n_cand if not dynamic else sum(nodes_log) / len(nodes_log)
     value = job_rate(world, cand_per_step * steps, ms / 1e3)
     g_avg_ms = g_ms / max(g_n, 1)
     g_avg_bytes = g_bytes / max(g_n, 1)
@@ -895,6 +923,9 @@ def main():
         "greedy", f"sampling (T {TEMP}, top-p {TOP_P:.7g}, rejection sampling)")
     if tree:
         workload = WORKLOAD.replace("chain k=4", f"token tree {args.tree} ({n_cand} nodes, layer-skip draft)")
+    if dynamic:
+        workload = WORKLOAD.replace("chain k=4", f"token tree up to {args.tree} ({n_cand} nodes) of dynamic width "
+                                                 f"(confidence mass {args.tree_mass:g}), layer-skip draft")
     line = {
         "metric": METRIC,
         "value": value,
@@ -910,7 +941,8 @@ def main():
         "data": "synthetic (seeded random-init weights and KV context; no dataset)",
         "config": {"workload": workload if args.layers is None else workload + f" (reduced: {shape.n_layers} layers)",
                    "mode": args.mode,
-                   "batch": B, "k": k if not tree else None, "tree": args.tree, "ctx": CTX,
+                   "batch": B, "k": k if not tree else None, "tree": args.tree, "tree_mass": args.tree_mass,
+                   "ctx": CTX,
                    "kv": f"paged, {args.page}-slot pages" if args.page else "contiguous", "exit_layer": shape.exit_layer, "n_layers": shape.n_layers,
                    "l2": "inputs larger than L2 (13.5 GB weights re-streamed each round)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -932,11 +964,12 @@ def main():
                      "peak_source": peak_kind, "launches": g_n, "avg_launch_us": g_avg_ms * 1e3,
                      "avg_launch_bytes": g_avg_bytes},
         "attention": {"launches": a_n, "total_ms_per_step": a_ms / steps},
+        "mean_tree_nodes": (sum(nodes_log) / len(nodes_log) / B) if dynamic else None,
         "pdl": os.environ.get("SPEC_PDL", "1") != "0",
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": 4 * B * (n_cand + 2)},
+                "d2h_bytes_per_step": 4 * B * (n_cand + 2 + (1 if dynamic else 0))},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sec, desc, thr = oracle_round_sample(B)

@@ -69,6 +69,7 @@ extern "C" {
 #define SPEC_DEVERR_CAPACITY  2   /* a row slot at or beyond the KV capacity    */
 #define SPEC_DEVERR_TIMEOUT   4   /* a bounded pipeline wait ran out            */
 #define SPEC_DEVERR_POSITION  8   /* a position id beyond the rotary table      */
+#define SPEC_DEVERR_TREE     16   /* a device tree parent outside [0, node)     */
 
 typedef struct spec_model spec_model;
 typedef struct spec_kv spec_kv;
@@ -281,6 +282,48 @@ int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows
                 int32_t tok_stride, const int32_t* tree_parent, float* logits,
                 spec_row_stats* stats, int32_t* acc_len, int32_t* next_tok,
                 int32_t* path, void* stream);
+
+/* Layer-skip draft of a token tree whose width follows the draft's
+ * confidence, one tree a sequence (FlashSpec page, lnrk.cn/news/47842,
+ * section 6.2: nodes the draft is sure of are not widened, unsure ones get
+ * more branches).  As spec_draft_tree, level by level, but node i of level l
+ * gets c children: its c best draft tokens (ties to the lower id), c the
+ * fewest whose draft probabilities (softmax of the draft logits, float32)
+ * add up to at least `mass`, 1 <= c <= branching[l].  Children are numbered
+ * in level order after the nodes so far.  mass <= 0 gives a chain of depth
+ * `depth`; mass > 1 the full tree of `branching`.
+ *   t0         device int32 [batch]: each tree's root token
+ *   branching  host int32 [depth]: at most this many children a node of
+ *              level l, each in [1, min(16, V)]; the full tree has n_max <= 64
+ *              nodes
+ *   tokens, parents  device int32 [batch][n_max] out: node tokens (tokens[b][0]
+ *              = t0[b]) and parents (parents[b][0] = -1); entries at and past
+ *              n_nodes[b] are padding (token 0, parent 0)
+ *   n_nodes    device int32 [batch] out: nodes of each tree
+ *   h_L        device f32 [batch][n_max][d] out: layer-L state of every node
+ *   logits     device f32 [batch * n_max][V]: scratch for the draft rows
+ * Every draft pass runs over the full tree's n_max rows a sequence (the node
+ * counts stay on the device); KV layers [0, L) are written at slots s_b ..
+ * s_b + n_max - 1, lengths unchanged.  Follow with spec_verify_trees
+ * (n_rows = n_nodes read back, h_in = h_L, strides n_max) and kv_commit with
+ * the accepted path.  batch * n_max <= max_rows.  async. */
+int spec_draft_tree_dynamic(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0,
+                            const int32_t* branching, int32_t depth, float mass,
+                            int32_t* tokens, int32_t* parents, int32_t* n_nodes, float* h_L,
+                            float* logits, void* stream);
+
+/* spec_verify with one tree a sequence: the parents of sequence b's nodes
+ * are parents[b * par_stride + i] on the device (parent[0] ignored, the
+ * others in [0, i); a parent outside that range sets SPEC_DEVERR_TREE and
+ * reads as the root).  n_rows[b] is the node count of sequence b's tree
+ * (<= par_stride).  Acceptance (acc_len, next_tok and path, all three or
+ * none) runs as its own kernel after the forward, with the tree rule of
+ * spec_verify.  The attention always runs as its own kernel.  async. */
+int spec_verify_trees(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows,
+                      const float* h_in, int32_t h_stride, const int32_t* tokens,
+                      int32_t tok_stride, const int32_t* parents, int32_t par_stride,
+                      float* logits, spec_row_stats* stats, int32_t* acc_len,
+                      int32_t* next_tok, int32_t* path, void* stream);
 
 /* Rejection-sampling acceptance of a chain (no model needed).
  *   p      device f32 [batch][k+1][vocab]  target probabilities

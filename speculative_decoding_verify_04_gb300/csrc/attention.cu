@@ -5,7 +5,9 @@
 // ancestors and itself: a chain row sees new rows 0..j (causal), a tree node
 // sees its root-to-node path ("FlashSpec" page, lnrk.cn/news/47842, sections
 // 2.2 and 5.2: level-order tree batch under an ancestor mask, padding never
-// visible).  Both cases are one 64-bit mask per row over the new slots.
+// visible).  Both cases are one 64-bit mask per row over the new slots.  A
+// tree is one for the batch (tree 1: the plan's first kMaxSeqRows entries) or
+// one a sequence (tree 2: entries b * kMaxSeqRows + j).
 //
 // Work split (flash-decoding): CTA (split, kv head, sequence x query block)
 // owns up to 16 query vectors -- the (row, head) pairs of one KV head's group,
@@ -147,7 +149,8 @@ attention_kernel(AttnParams a, int n_rb) {
         unsigned long long mk;
         if (a.tree) {
             mk = 0ull;
-            for (int x = j; x >= 0; x = a.plan.tree_parent[x]) mk |= 1ull << x;
+            const int* tp = a.plan.tree_parent + (a.tree == 2 ? (size_t)b * kMaxSeqRows : 0);
+            for (int x = j; x >= 0; x = tp[x]) mk |= 1ull << x;
         } else {
             mk = (j >= 63) ? ~0ull : ((2ull << j) - 1ull);
         }
@@ -319,7 +322,8 @@ attention_decode_kernel(AttnParams a) {
         if (r < nq) {
             const int j = r / G;
             if (a.tree) {
-                for (int x = j; x >= 0; x = a.plan.tree_parent[x]) mk[r] |= 1ull << x;
+                const int* tp = a.plan.tree_parent + (a.tree == 2 ? (size_t)b * kMaxSeqRows : 0);
+                for (int x = j; x >= 0; x = tp[x]) mk[r] |= 1ull << x;
             } else {
                 mk[r] = (j >= 63) ? ~0ull : ((2ull << j) - 1ull);
             }
@@ -540,7 +544,8 @@ attention_mma_kernel(AttnParams a, int n_qb) {
         if (t < nq) {
             const int j = (q0 + t) / G;
             if (a.tree) {
-                for (int x = j; x >= 0; x = a.plan.tree_parent[x]) mk |= 1ull << x;
+                const int* tp = a.plan.tree_parent + (a.tree == 2 ? (size_t)b * kMaxSeqRows : 0);
+            for (int x = j; x >= 0; x = tp[x]) mk |= 1ull << x;
             } else {
                 mk = (j >= 63) ? ~0ull : ((2ull << j) - 1ull);
             }

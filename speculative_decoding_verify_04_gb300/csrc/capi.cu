@@ -82,13 +82,19 @@ __global__ void rope_table_kernel(float* cs, float* sn, int max_pos, int half, d
 struct PlanArgs {
     PlanParams p;
     int row0[kMaxPlanBatch];
+    const int* dev_parent;   // tree mode: nullable device [batch][dev_stride] parents, one tree a sequence
+    int dev_stride;
 };
 
 // Row plan.  mode 0 chain: row j of sequence b at slot / position s_b + j.
-// mode 1 tree: slot s_b + j, position s_b + depth(j).  mode 2 draft pass j:
-// one row per sequence at slot / position s_b + j, seeing slots [0, s_b + j]
-// (the earlier passes' rows count as context: base s_b + j, local row 0).
-__global__ void plan_kernel(PlanArgs a, RowPlan plan, const int* __restrict__ len, int T) {
+// mode 1 tree: slot s_b + j, position s_b + depth(j); one tree for the batch
+// (the host's parents, written to the first kMaxSeqRows entries of the tree
+// arrays) or, with dev_parent, one tree a sequence (parents read on the
+// device; row j of sequence b writes entry b * kMaxSeqRows + j).  mode 2
+// draft pass j: one row per sequence at slot / position s_b + j, seeing slots
+// [0, s_b + j] (the earlier passes' rows count as context: base s_b + j,
+// local row 0).
+__global__ void plan_kernel(PlanArgs a, RowPlan plan, const int* __restrict__ len, int T, int* err) {
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
@@ -100,7 +106,7 @@ __global__ void plan_kernel(PlanArgs a, RowPlan plan, const int* __restrict__ le
         plan.seq_nrows[t] = (p.mode == 2) ? 1 : p.n_rows[t];
         plan.seq_base[t] = len[t] + extra;
     }
-    if (t < kMaxSeqRows) {
+    if (t < kMaxSeqRows && !a.dev_parent) {
         plan.tree_parent[t] = p.parent[t];
         plan.tree_depth[t] = p.depth[t];
     }
@@ -122,7 +128,24 @@ __global__ void plan_kernel(PlanArgs a, RowPlan plan, const int* __restrict__ le
     plan.row_seq[t] = b;
     plan.row_local[t] = j;
     plan.row_slot[t] = s + j;
-    plan.row_pos[t] = s + (p.mode == 1 ? p.depth[j] : j);
+    int dep = j;
+    if (p.mode == 1 && a.dev_parent) {
+        // depth by walking to the root; a parent outside [0, x) is an error and reads as the root
+        const int* par = a.dev_parent + (size_t)b * a.dev_stride;
+        int pj = -1;
+        dep = 0;
+        for (int x = j; x > 0; ++dep) {
+            int q = par[x];
+            if (q < 0 || q >= x) { dev_error(err, SPEC_DEVERR_TREE); q = 0; }
+            if (x == j) pj = q;
+            x = q;
+        }
+        plan.tree_parent[(size_t)b * kMaxSeqRows + j] = pj;
+        plan.tree_depth[(size_t)b * kMaxSeqRows + j] = dep;
+    } else if (p.mode == 1) {
+        dep = p.depth[j];
+    }
+    plan.row_pos[t] = s + dep;
 }
 
 // First residual rows of a forward: from the layer-L state (h_in) or the token
@@ -224,6 +247,142 @@ tree_expand_kernel(const float* __restrict__ logits, int V, int rows_per_seq, in
         }
         __syncthreads();
     }
+}
+
+// Tree of dynamic width (FlashSpec page, lnrk.cn/news/47842, section 6.2: the
+// draft widens the nodes it is unsure of).  Node i of level l gets the fewest
+// of its best draft tokens whose draft probabilities (softmax of its draft
+// logits, float32) reach `mass`, at least one and at most branching[l]; the
+// children of a level are numbered in level order after the nodes so far.
+// The tree lives in the caller's tokens / parents arrays ([batch][n_max]) and
+// its node count in n_nodes[batch]; rows past the count are padding (token 0
+// under the root) that the draft passes compute and nothing reads.  Per
+// sequence the staging block holds the level being expanded (first node,
+// node count), each node's child count and its best tokens.
+constexpr int kTreeStage = 2 + kMaxSeqRows + kMaxSeqRows * kMaxTreeKids;
+
+__global__ void tree_init_kernel(const int* __restrict__ t0, int* tokens, int* parents, int* n_nodes, int* stage,
+                                 int batch, int n_max) {
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= batch * n_max) return;
+    const int b = i / n_max, j = i % n_max;
+    tokens[i] = j == 0 ? t0[b] : 0;
+    parents[i] = j == 0 ? -1 : 0;
+    if (j == 0) {
+        n_nodes[b] = 1;
+        stage[(size_t)b * kTreeStage + 0] = 0;
+        stage[(size_t)b * kTreeStage + 1] = 1;
+    }
+}
+
+// One CTA per (sequence, node of the level): max and sum of exp over the row,
+// then rounds of block-wide argmax (skipping the ids taken) until the taken
+// tokens' probability reaches `mass` or `width` tokens are taken.
+__global__ void __launch_bounds__(256)
+tree_width_kernel(const float* __restrict__ logits, int V, int rows_per_seq, int width, float mass, int* stage) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float s_v[8];
+    __shared__ int s_i[8];
+    __shared__ int taken[kMaxTreeKids];
+    __shared__ int s_stop;
+    const int b = blockIdx.x, y = blockIdx.y, t = threadIdx.x, lane = t & 31, w = t >> 5;
+    int* st = stage + (size_t)b * kTreeStage;
+    const int start = st[0], count = st[1];
+    if (y >= count) return;
+    const int i = start + y;
+    const float* row = logits + ((size_t)b * rows_per_seq + i) * V;
+    float mx = -INFINITY;
+    for (int x = t; x < V; x += 256) mx = fmaxf(mx, row[x]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_v[w] = mx;
+    __syncthreads();
+    mx = s_v[0];
+    for (int q = 1; q < 8; ++q) mx = fmaxf(mx, s_v[q]);
+    __syncthreads();
+    float sum = 0.f;
+    for (int x = t; x < V; x += 256) sum += expf(row[x] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) s_v[w] = sum;
+    __syncthreads();
+    sum = 0.f;
+    for (int q = 0; q < 8; ++q) sum += s_v[q];
+    __syncthreads();
+    float cum = 0.f;
+    int c = 0;
+    for (int k = 0; k < width; ++k) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int x = t; x < V; x += 256) {
+            bool skip = false;
+            for (int q = 0; q < k; ++q) skip |= taken[q] == x;
+            const float v = row[x];
+            if (!skip && (v > bv || (v == bv && x < bi))) { bv = v; bi = x; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0) { s_v[w] = bv; s_i[w] = bi; }
+        __syncthreads();
+        if (t == 0) {
+            float v = s_v[0];
+            int id = s_i[0];
+            for (int q = 1; q < 8; ++q)
+                if (s_v[q] > v || (s_v[q] == v && s_i[q] < id)) { v = s_v[q]; id = s_i[q]; }
+            taken[k] = id;
+            st[2 + kMaxSeqRows + y * kMaxTreeKids + k] = id;
+            cum += expf(v - mx) / sum;
+            s_stop = cum >= mass;
+        }
+        __syncthreads();
+        c = k + 1;
+        if (s_stop) break;
+    }
+    if (t == 0) st[2 + y] = c;
+}
+
+// One thread per sequence: the children of the level's nodes in order.
+__global__ void tree_assign_kernel(int* tokens, int* parents, int* n_nodes, int* stage, int batch, int n_max,
+                                   int* err) {
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= batch) return;
+    int* st = stage + (size_t)b * kTreeStage;
+    const int start = st[0], count = st[1], n = n_nodes[b];
+    int at = n;
+    for (int y = 0; y < count; ++y) {
+        const int c = st[2 + y];
+        for (int k = 0; k < c; ++k) {
+            if (at >= n_max) { dev_error(err, SPEC_DEVERR_TREE); break; }
+            tokens[(size_t)b * n_max + at] = st[2 + kMaxSeqRows + y * kMaxTreeKids + k];
+            parents[(size_t)b * n_max + at] = start + y;
+            ++at;
+        }
+    }
+    st[0] = n;
+    st[1] = at - n;
+    n_nodes[b] = at;
+}
+
+// Greedy tree acceptance for one tree a sequence, from the row summaries of
+// the verify forward and the plan's per-sequence tree arrays.
+__global__ void accept_trees_kernel(const spec_row_stats* __restrict__ rs, RowPlan plan, const int* tokens,
+                                    int tok_stride, int batch, int* acc_len, int* next_tok, int* path) {
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= batch) return;
+    accept_tree_one(rs, plan.seq_row0[b], plan.seq_nrows[b], tokens + (size_t)b * tok_stride,
+                    plan.tree_parent + (size_t)b * kMaxSeqRows, plan.tree_depth + (size_t)b * kMaxSeqRows,
+                    acc_len + b, next_tok + b, path ? path + (size_t)b * kMaxSeqRows : nullptr);
 }
 
 __global__ void add_len_kernel(int* len, int seq, int n, int cap, int* err) {
@@ -339,7 +498,8 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
     const spec_model_config& c = m->cfg;
     const int qdim = c.n_heads * c.head_dim;
     // attention as the first phase of the chain that follows it (one launch per layer)
-    const bool fused = T <= kMaxTPad && attn_phase_ok(m, kv, batch, max_rows_per_seq);
+    // (the phase reads one tree for the batch: a tree a sequence takes the separate kernel)
+    const bool fused = tree != 2 && T <= kMaxTPad && attn_phase_ok(m, kv, batch, max_rows_per_seq);
     GemmStep pend[5];
     int np = 0;
     for (int l = lo; l < hi; ++l) {
@@ -430,16 +590,20 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
     return SPEC_OK;
 }
 
-static int launch_plan(spec_model* m, const PlanParams& p, int T, const int* len, cudaStream_t st) {
+static int launch_plan(spec_model* m, const PlanParams& p, int T, const int* len, cudaStream_t st,
+                       const int* dev_parent = nullptr, int dev_stride = 0) {
     PlanArgs a{};
     a.p = p;
+    a.dev_parent = dev_parent;
+    a.dev_stride = dev_stride;
     int r = 0;
     for (int b = 0; b < p.batch; ++b) {
         a.row0[b] = r;
         r += (p.mode == 2) ? 1 : p.n_rows[b];
     }
     const int n = std::max(std::max(T, p.batch), kMaxSeqRows);
-    cudaError_t le = launch_k(m->pdl, plan_kernel, dim3((n + 127) / 128), dim3(128), 0, st, a, m->plan, len, T);
+    cudaError_t le = launch_k(m->pdl, plan_kernel, dim3((n + 127) / 128), dim3(128), 0, st, a, m->plan, len, T,
+                              m->err);
     if (le != cudaSuccess) return check_cuda(le, "plan launch");
     ++m->launches;
     return check_cuda(cudaGetLastError(), "plan launch");
@@ -640,7 +804,7 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
     const size_t w_ac = take((size_t)m->n_attn_counters * 4);
     const size_t w_err = take(64);
     const size_t w_pkv = take(64);
-    const size_t w_plan = take((size_t)(4 * R + 3 * c.max_batch + 2 * kMaxSeqRows + 64) * 4);
+    const size_t w_plan = take((size_t)(4 * R + 3 * c.max_batch + (2 * kMaxSeqRows + kTreeStage) * c.max_batch + 64) * 4);
     const size_t w_dl = take((size_t)c.max_batch * V * 4);
     m->ws_bytes = off;
     if ((rc = check_cuda(cudaMalloc(&m->ws, off), "cudaMalloc(workspace)"))) return fail(rc);
@@ -669,8 +833,9 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
     m->plan.seq_row0 = pl; pl += c.max_batch;
     m->plan.seq_nrows = pl; pl += c.max_batch;
     m->plan.seq_base = pl; pl += c.max_batch;
-    m->plan.tree_parent = pl; pl += kMaxSeqRows;
-    m->plan.tree_depth = pl; pl += kMaxSeqRows;
+    m->plan.tree_parent = pl; pl += (size_t)c.max_batch * kMaxSeqRows;
+    m->plan.tree_depth = pl; pl += (size_t)c.max_batch * kMaxSeqRows;
+    // tree_stage(m) follows: kTreeStage ints a sequence
 
     // ---- tensor maps (bf16 path)
     if (m->bf16) {
@@ -1054,25 +1219,105 @@ extern "C" int spec_draft_tree(spec_model* m, spec_kv* kv, int32_t batch, const 
     return SPEC_OK;
 }
 
-extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows, const float* h_in,
-                           int32_t h_stride, const int32_t* tokens, int32_t tok_stride, const int32_t* tree_parent,
-                           float* logits, spec_row_stats* stats, int32_t* acc_len, int32_t* next_tok, int32_t* path,
-                           void* stream) {
+// The dynamic tree's staging block sits after the plan's tree arrays.
+static int* tree_stage(spec_model* m) { return m->plan.tree_depth + (size_t)m->cfg.max_batch * kMaxSeqRows; }
+
+extern "C" int spec_draft_tree_dynamic(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0,
+                                       const int32_t* branching, int32_t depth, float mass, int32_t* tokens,
+                                       int32_t* parents, int32_t* n_nodes, float* h_L, float* logits, void* stream) {
+    if (!m || !kv || !t0 || !branching || !tokens || !parents || !n_nodes || !h_L || !logits)
+        return set_error(SPEC_ERR_ARG, "spec_draft_tree_dynamic: null pointer");
+    if (kv->m != m) return set_error(SPEC_ERR_ARG, "spec_draft_tree_dynamic: cache of another model");
+    const spec_model_config& c = m->cfg;
+    if (c.exit_layer < 1) return set_error(SPEC_ERR_ARG, "spec_draft_tree_dynamic: exit_layer must be >= 1");
+    if (batch < 1 || batch > kv->batch) return set_error(SPEC_ERR_ARG, "spec_draft_tree_dynamic: bad batch");
+    if (depth < 1) return set_error(SPEC_ERR_ARG, "spec_draft_tree_dynamic: depth must be >= 1");
+    if (mass != mass) return set_error(SPEC_ERR_ARG, "spec_draft_tree_dynamic: mass is NaN");
+    // the widest tree: level l holds at most lw[l] nodes, levels up to l at most cum[l]
+    int lw[kMaxSeqRows + 1], cum[kMaxSeqRows + 1];
+    lw[0] = 1;
+    cum[0] = 1;
+    for (int l = 0; l < depth; ++l) {
+        if (branching[l] < 1 || branching[l] > kMaxTreeKids || branching[l] > c.vocab)
+            return set_error(SPEC_ERR_ARG, "spec_draft_tree_dynamic: branching must be in [1, min(16, vocab)]");
+        if ((long long)lw[l] * branching[l] + cum[l] > kMaxSeqRows)
+            return set_error(SPEC_ERR_ARG, "spec_draft_tree_dynamic: the widest tree has more than 64 nodes");
+        lw[l + 1] = lw[l] * branching[l];
+        cum[l + 1] = cum[l] + lw[l + 1];
+    }
+    const int n_max = cum[depth];
+    if ((long long)batch * n_max > c.max_rows)
+        return set_error(SPEC_ERR_CAPACITY, "spec_draft_tree_dynamic: batch * nodes of the widest tree > max_rows");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (kv->paged) {
+        int need[kMaxPlanBatch];
+        for (int b = 0; b < batch; ++b) need[b] = n_max;
+        SPEC_TRY(kv_ensure_pages(kv, batch, need, true, st));
+    }
+    int* stage = tree_stage(m);
+    launch_k(m->pdl, tree_init_kernel, dim3((batch * n_max + 255) / 256), dim3(256), 0, st, t0, tokens, parents,
+             n_nodes, stage, batch, n_max);
+    ++m->launches;
+    SPEC_CUDA(cudaGetLastError(), "dynamic tree init");
+    PlanParams p{};
+    p.batch = batch;
+    p.mode = 1;
+    for (int lev = 0; lev <= depth; ++lev) {
+        // layers [0, L) over every row the tree can hold up to this level
+        const int rows = cum[lev];
+        for (int b = 0; b < batch; ++b) p.n_rows[b] = rows;
+        const int T = batch * rows;
+        SPEC_TRY(launch_plan(m, p, T, kv->len, st, parents, n_max));
+        SPEC_TRY(launch_prologue(m, T, nullptr, 0, tokens, n_max, 0, 0, st));
+        const bool expand = lev < depth;
+        HeadSpec hs{};
+        hs.mode = HEAD_STATS;
+        hs.T = T;
+        hs.r0 = 0;
+        hs.logits = logits;
+        hs.logits_stride = c.vocab;
+        hs.logits_row0 = 0;
+        hs.batch = batch;
+        SPEC_TRY(run_layers(m, kv, T, batch, rows, 0, c.exit_layer, 2, expand, expand ? &hs : nullptr, st));
+        if (expand) {
+            launch_k(m->pdl, tree_width_kernel, dim3(batch, lw[lev]), dim3(256), 0, st, (const float*)logits, c.vocab,
+                     rows, (int)branching[lev], mass, stage);
+            launch_k(m->pdl, tree_assign_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, tokens, parents, n_nodes,
+                     stage, batch, n_max, m->err);
+            m->launches += 2;
+            SPEC_CUDA(cudaGetLastError(), "dynamic tree expansion");
+        } else {
+            launch_k(m->pdl, copy_rows_kernel, dim3(T), dim3(256), 0, st, (const float*)m->h, h_L, T, c.d_model, 1, 0);
+            ++m->launches;
+            SPEC_CUDA(cudaGetLastError(), "dynamic tree state copy");
+        }
+    }
+    return SPEC_OK;
+}
+
+// Verification forward: one tree for the batch (tree_parent, host), one tree a
+// sequence (dev_parent, device [batch][par_stride]) or a chain (neither).
+static int verify_impl(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows, const float* h_in,
+                       int32_t h_stride, const int32_t* tokens, int32_t tok_stride, const int32_t* tree_parent,
+                       const int32_t* dev_parent, int32_t par_stride, float* logits, spec_row_stats* stats,
+                       int32_t* acc_len, int32_t* next_tok, int32_t* path, cudaStream_t st) {
     if (!m || !kv || !n_rows || !tokens) return set_error(SPEC_ERR_ARG, "spec_verify: null pointer");
     if (kv->m != m) return set_error(SPEC_ERR_ARG, "spec_verify: cache of another model");
     const spec_model_config& c = m->cfg;
     if (batch < 1 || batch > kv->batch) return set_error(SPEC_ERR_ARG, "spec_verify: bad batch");
     if ((acc_len == nullptr) != (next_tok == nullptr)) return set_error(SPEC_ERR_ARG, "acc_len and next_tok go together");
-    if (tree_parent && acc_len && !path) return set_error(SPEC_ERR_ARG, "tree acceptance needs path");
+    const bool trees = dev_parent != nullptr;
+    if ((tree_parent || trees) && acc_len && !path) return set_error(SPEC_ERR_ARG, "tree acceptance needs path");
     if (h_in && c.exit_layer < 1) return set_error(SPEC_ERR_ARG, "h_in needs exit_layer >= 1");
     int T = 0, max_r = 0;
     PlanParams p{};
     p.batch = batch;
-    p.mode = tree_parent ? 1 : 0;
+    p.mode = (tree_parent || trees) ? 1 : 0;
     for (int b = 0; b < batch; ++b) {
         if (n_rows[b] < 1 || n_rows[b] > kMaxSeqRows) return set_error(SPEC_ERR_ARG, "n_rows[b] must be in [1, 64]");
         if (h_in && n_rows[b] > h_stride) return set_error(SPEC_ERR_ARG, "n_rows[b] > h_stride");
         if (n_rows[b] > tok_stride) return set_error(SPEC_ERR_ARG, "n_rows[b] > tok_stride");
+        if (trees && n_rows[b] > par_stride) return set_error(SPEC_ERR_ARG, "n_rows[b] > par_stride");
         p.n_rows[b] = n_rows[b];
         T += n_rows[b];
         max_r = std::max(max_r, (int)n_rows[b]);
@@ -1091,13 +1336,13 @@ extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int3
         for (int b = 0; b < batch; ++b)
             if (n_rows[b] != n) return set_error(SPEC_ERR_ARG, "tree mode: every sequence has the tree's node count");
     }
-    cudaStream_t st = (cudaStream_t)stream;
     const int lo = h_in ? c.exit_layer : 0;
     SPEC_TRY(kv_ensure_pages(kv, batch, p.n_rows, true, st));
-    SPEC_TRY(launch_plan(m, p, T, kv->len, st));
+    SPEC_TRY(launch_plan(m, p, T, kv->len, st, dev_parent, par_stride));
     SPEC_TRY(launch_prologue(m, T, h_in, h_stride, tokens, tok_stride, 0, lo, st));
     HeadSpec hs{};
-    hs.mode = acc_len ? (tree_parent ? HEAD_ACCEPT_TREE : HEAD_ACCEPT_CHAIN) : HEAD_STATS;
+    // one tree a sequence: summaries in the head, acceptance in its own kernel
+    hs.mode = (acc_len && !trees) ? (tree_parent ? HEAD_ACCEPT_TREE : HEAD_ACCEPT_CHAIN) : HEAD_STATS;
     hs.T = T;
     hs.r0 = 0;
     hs.logits = logits;
@@ -1110,7 +1355,31 @@ extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int3
     hs.next_tok = next_tok;
     hs.path = path;
     hs.batch = batch;
-    return run_layers(m, kv, T, batch, max_r, lo, c.n_layers, tree_parent ? 1 : 0, true, &hs, st);
+    SPEC_TRY(run_layers(m, kv, T, batch, max_r, lo, c.n_layers, trees ? 2 : (tree_parent ? 1 : 0), true, &hs, st));
+    if (trees && acc_len) {
+        launch_k(m->pdl, accept_trees_kernel, dim3((batch + 127) / 128), dim3(128), 0, st,
+                 (const spec_row_stats*)m->row_stats, m->plan, tokens, tok_stride, batch, acc_len, next_tok, path);
+        ++m->launches;
+        SPEC_CUDA(cudaGetLastError(), "tree acceptance");
+    }
+    return SPEC_OK;
+}
+
+extern "C" int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows, const float* h_in,
+                           int32_t h_stride, const int32_t* tokens, int32_t tok_stride, const int32_t* tree_parent,
+                           float* logits, spec_row_stats* stats, int32_t* acc_len, int32_t* next_tok, int32_t* path,
+                           void* stream) {
+    return verify_impl(m, kv, batch, n_rows, h_in, h_stride, tokens, tok_stride, tree_parent, nullptr, 0, logits,
+                       stats, acc_len, next_tok, path, (cudaStream_t)stream);
+}
+
+extern "C" int spec_verify_trees(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows, const float* h_in,
+                                 int32_t h_stride, const int32_t* tokens, int32_t tok_stride, const int32_t* parents,
+                                 int32_t par_stride, float* logits, spec_row_stats* stats, int32_t* acc_len,
+                                 int32_t* next_tok, int32_t* path, void* stream) {
+    if (!parents) return set_error(SPEC_ERR_ARG, "spec_verify_trees: null parents");
+    return verify_impl(m, kv, batch, n_rows, h_in, h_stride, tokens, tok_stride, nullptr, parents, par_stride, logits,
+                       stats, acc_len, next_tok, path, (cudaStream_t)stream);
 }
 
 extern "C" int spec_profile(spec_model* m, int32_t enable) {

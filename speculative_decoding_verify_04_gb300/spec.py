@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libspec.so")
 
 SPEC_DTYPE_F32 = 0
 SPEC_DTYPE_BF16 = 1
-DEVERR_TOKEN, DEVERR_CAPACITY, DEVERR_TIMEOUT, DEVERR_POSITION = 1, 2, 4, 8
+DEVERR_TOKEN, DEVERR_CAPACITY, DEVERR_TIMEOUT, DEVERR_POSITION, DEVERR_TREE = 1, 2, 4, 8, 16
 MAX_SEQ_ROWS = 64
 EXPORTS = [
     "spec_last_error", "spec_device_info", "spec_model_create", "spec_model_destroy", "spec_device_error",
@@ -28,6 +28,7 @@ EXPORTS = [
     "kv_commit", "spec_row_probs", "spec_schedule_k", "spec_profile", "spec_profile_read", "spec_launch_count",
     "spec_verify_noalloc", "spec_draft_sample", "spec_probs", "spec_sample", "spec_schedule_aimd",
     "spec_schedule_decay", "spec_draft_tree", "spec_kv_create_paged", "spec_kv_free_pages", "spec_kv_page_table",
+    "spec_draft_tree_dynamic", "spec_verify_trees",
 ]
 
 
@@ -85,6 +86,8 @@ def load(path: str = LIB_PATH):
         "spec_schedule_aimd": ([P, P, P, I, POINTER(AIMDSchedule), P, P], I),
         "spec_schedule_decay": ([P, P, I, I, P, P], I),
         "spec_draft_tree": ([P, P, I, P, POINTER(I), I, P, P, P, P], I),
+        "spec_draft_tree_dynamic": ([P, P, I, P, POINTER(I), I, c_float, P, P, P, P, P, P], I),
+        "spec_verify_trees": ([P, P, I, POINTER(I), P, I, P, I, P, I, P, P, P, P, P, P], I),
         "spec_kv_create_paged": ([P, I, I, I, I, POINTER(P)], I),
         "spec_kv_free_pages": ([P, POINTER(I), P], I),
         "spec_kv_page_table": ([P, POINTER(I), P], I),
@@ -305,6 +308,51 @@ def spec_draft_tree(model, kv, t0, tree_parent, tokens, h_L, logits, stream=None
     _need(logits, torch.float32, "logits", B * n * model.cfg.vocab)
     _check(load().spec_draft_tree(model.handle, kv.handle, B, _ptr(t0), _i32_array(tree_parent), n, _ptr(tokens),
                                   _ptr(h_L), _ptr(logits), _stream(stream)))
+
+
+def tree_size(branching):
+    """Nodes of the full tree of a branching list (root included)."""
+    n, w = 1, 1
+    for b in branching:
+        w *= int(b)
+        n += w
+    return n
+
+
+def spec_draft_tree_dynamic(model, kv, t0, branching, mass, tokens, parents, n_nodes, h_L, logits, stream=None):
+    """Layer-skip draft of a tree whose width follows the draft's confidence:
+    each node of level l gets its fewest best draft tokens whose probability
+    reaches ``mass`` (1 .. branching[l]).  tokens, parents [B, n_max], n_nodes [B],
+    h_L [B, n_max, d], logits [B * n_max, V] scratch; n_max = tree_size(branching)."""
+    B = t0.numel()
+    n = tree_size(branching)
+    _need(t0, torch.int32, "t0")
+    _need(tokens, torch.int32, "tokens", B * n)
+    _need(parents, torch.int32, "parents", B * n)
+    _need(n_nodes, torch.int32, "n_nodes", B)
+    _need(h_L, torch.float32, "h_L", B * n * model.cfg.d_model)
+    _need(logits, torch.float32, "logits", B * n * model.cfg.vocab)
+    _check(load().spec_draft_tree_dynamic(model.handle, kv.handle, B, _ptr(t0), _i32_array(branching), len(branching),
+                                          float(mass), _ptr(tokens), _ptr(parents), _ptr(n_nodes), _ptr(h_L),
+                                          _ptr(logits), _stream(stream)))
+
+
+def spec_verify_trees(model, kv, n_rows, tokens, tok_stride, parents, par_stride, h_in=None, h_stride=0, logits=None,
+                      stats=None, acc_len=None, next_tok=None, path=None, stream=None):
+    """spec_verify with one tree a sequence: ``parents`` [B, par_stride] on the device."""
+    B = len(n_rows)
+    T = sum(int(n) for n in n_rows)
+    _need(tokens, torch.int32, "tokens", B * tok_stride)
+    _need(parents, torch.int32, "parents", B * par_stride)
+    _need(h_in, torch.float32, "h_in", B * h_stride * model.cfg.d_model if h_in is not None else None)
+    _need(logits, torch.float32, "logits", T * model.cfg.vocab)
+    _need(stats, torch.float32, "stats", T * 4)
+    _need(acc_len, torch.int32, "acc_len", B)
+    _need(next_tok, torch.int32, "next_tok", B)
+    _need(path, torch.int32, "path", B * MAX_SEQ_ROWS)
+    _check(load().spec_verify_trees(model.handle, kv.handle, B, _i32_array(n_rows), _ptr(h_in), h_stride,
+                                    _ptr(tokens), tok_stride, _ptr(parents), par_stride, _ptr(logits), _ptr(stats),
+                                    _ptr(acc_len), _ptr(next_tok), _ptr(path), _stream(stream)))
 
 
 def _rows2d(t, name):
