@@ -277,52 +277,63 @@ __global__ void tree_init_kernel(const int* __restrict__ t0, int* tokens, int* p
     }
 }
 
-// One CTA per (sequence, node of the level): max and sum of exp over the row,
-// then rounds of block-wide argmax (skipping the ids taken) until the taken
-// tokens' probability reaches `mass` or `width` tokens are taken.
-__global__ void __launch_bounds__(256)
+// One CTA per (sequence, node of the level), one pass over the row: each
+// thread keeps a running max and sum of exp and its own `width` best
+// (logit, id) pairs, ties to the lower id; a block tournament of the threads'
+// list heads then ranks the row's best tokens (the owner of id x is thread
+// x % kWidthThreads), and the count stops at the first rank where their
+// probability reaches `mass` (at most `width`).
+constexpr int kWidthThreads = 256;
+
+__global__ void __launch_bounds__(kWidthThreads)
 tree_width_kernel(const float* __restrict__ logits, int V, int rows_per_seq, int width, float mass, int* stage) {
     pdl_wait();
     pdl_trigger();
-    __shared__ float s_v[8];
-    __shared__ int s_i[8];
-    __shared__ int taken[kMaxTreeKids];
-    __shared__ int s_stop;
+    constexpr int NW = kWidthThreads / 32;
+    __shared__ float s_v[NW], s_m[NW], s_s[NW];
+    __shared__ int s_i[NW];
     const int b = blockIdx.x, y = blockIdx.y, t = threadIdx.x, lane = t & 31, w = t >> 5;
     int* st = stage + (size_t)b * kTreeStage;
     const int start = st[0], count = st[1];
     if (y >= count) return;
     const int i = start + y;
     const float* row = logits + ((size_t)b * rows_per_seq + i) * V;
-    float mx = -INFINITY;
-    for (int x = t; x < V; x += 256) mx = fmaxf(mx, row[x]);
+    float tv[kMaxTreeKids];
+    int ti[kMaxTreeKids];
+    for (int q = 0; q < kMaxTreeKids; ++q) { tv[q] = -INFINITY; ti[q] = INT_MAX; }
+    float m = -INFINITY, sum = 0.f;
+#pragma unroll 4
+    for (int x = t; x < V; x += kWidthThreads) {
+        const float v = __ldg(row + x);
+        if (v > m) { sum = sum * expf(m - v) + 1.f; m = v; } else { sum += expf(v - m); }
+        if (v > tv[width - 1]) {            // x grows: an equal value ranks after the kept ones
+            int q = width - 1;
+            while (q > 0 && v > tv[q - 1]) { tv[q] = tv[q - 1]; ti[q] = ti[q - 1]; --q; }
+            tv[q] = v;
+            ti[q] = x;
+        }
+    }
+    // the row's max and sum of exp
+    float mx = m;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) s_v[w] = mx;
+    if (lane == 0) s_m[w] = mx;
     __syncthreads();
-    mx = s_v[0];
-    for (int q = 1; q < 8; ++q) mx = fmaxf(mx, s_v[q]);
-    __syncthreads();
-    float sum = 0.f;
-    for (int x = t; x < V; x += 256) sum += expf(row[x] - mx);
+    mx = s_m[0];
+    for (int q = 1; q < NW; ++q) mx = fmaxf(mx, s_m[q]);
+    float part = sum * expf(m - mx);        // a thread without elements adds 0 * 0
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) s_v[w] = sum;
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) s_s[w] = part;
     __syncthreads();
-    sum = 0.f;
-    for (int q = 0; q < 8; ++q) sum += s_v[q];
-    __syncthreads();
+    float total = 0.f;
+    for (int q = 0; q < NW; ++q) total += s_s[q];
+    // tournament: `width` rounds of block argmax over the list heads
+    int head = 0, c = 0;
     float cum = 0.f;
-    int c = 0;
     for (int k = 0; k < width; ++k) {
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-        for (int x = t; x < V; x += 256) {
-            bool skip = false;
-            for (int q = 0; q < k; ++q) skip |= taken[q] == x;
-            const float v = row[x];
-            if (!skip && (v > bv || (v == bv && x < bi))) { bv = v; bi = x; }
-        }
+        float bv = head < width ? tv[head] : -INFINITY;
+        int bi = head < width ? ti[head] : INT_MAX;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -331,21 +342,19 @@ tree_width_kernel(const float* __restrict__ logits, int V, int rows_per_seq, int
         }
         if (lane == 0) { s_v[w] = bv; s_i[w] = bi; }
         __syncthreads();
+        float v = s_v[0];
+        int id = s_i[0];
+        for (int q = 1; q < NW; ++q)
+            if (s_v[q] > v || (s_v[q] == v && s_i[q] < id)) { v = s_v[q]; id = s_i[q]; }
+        if (head < width && ti[head] == id) ++head;
         if (t == 0) {
-            float v = s_v[0];
-            int id = s_i[0];
-            for (int q = 1; q < 8; ++q)
-                if (s_v[q] > v || (s_v[q] == v && s_i[q] < id)) { v = s_v[q]; id = s_i[q]; }
-            taken[k] = id;
             st[2 + kMaxSeqRows + y * kMaxTreeKids + k] = id;
-            cum += expf(v - mx) / sum;
-            s_stop = cum >= mass;
+            cum += expf(v - mx) / total;
+            if (c == 0 && cum >= mass) c = k + 1;
         }
         __syncthreads();
-        c = k + 1;
-        if (s_stop) break;
     }
-    if (t == 0) st[2 + y] = c;
+    if (t == 0) st[2 + y] = c > 0 ? c : width;
 }
 
 // One thread per sequence: the children of the level's nodes in order.
@@ -1280,7 +1289,7 @@ extern "C" int spec_draft_tree_dynamic(spec_model* m, spec_kv* kv, int32_t batch
         hs.batch = batch;
         SPEC_TRY(run_layers(m, kv, T, batch, rows, 0, c.exit_layer, 2, expand, expand ? &hs : nullptr, st));
         if (expand) {
-            launch_k(m->pdl, tree_width_kernel, dim3(batch, lw[lev]), dim3(256), 0, st, (const float*)logits, c.vocab,
+            launch_k(m->pdl, tree_width_kernel, dim3(batch, lw[lev]), dim3(kWidthThreads), 0, st, (const float*)logits, c.vocab,
                      rows, (int)branching[lev], mass, stage);
             launch_k(m->pdl, tree_assign_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, tokens, parents, n_nodes,
                      stage, batch, n_max, m->err);
