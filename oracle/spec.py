@@ -26,6 +26,11 @@ s + i, each seeing the committed context, its ancestors and itself (padding
 and siblings masked).  The page's "parent offset + 1" rule is the depth; its
 remark that depth ids broke its outputs concerns a target trained with
 injected position ids, which a plain target does not have.
+
+Layer-skip trees (same page, §6.2, with the first-L-layer draft): the draft
+grows the tree level by level, children taking their parent's best draft
+tokens, either in a fixed branching or with a width that follows the
+draft's confidence (child_count).
 """
 from __future__ import annotations
 
