@@ -155,7 +155,11 @@ int spec_device_info(int32_t* num_sms, int32_t* cc_major, int32_t* cc_minor);
  * interleaved in blocks of 64), builds the rotary tables and workspaces, and
  * synchronises `stream` before returning: the caller may free its copies
  * afterwards.  sync.  Errors: ARG (null / non-positive sizes), UNSUPPORTED
- * (outside the limits above), CUDA (allocation or copy failed). */
+ * (outside the limits above), CUDA (allocation or copy failed).
+ * The decoder is a Llama-style target: a 7B-class model in the self-speculative
+ * decoding page, section 4.1; a 7B LLaMA architecture in the FlashSpec page,
+ * section 2.1.
+ */
 int spec_model_create(const spec_model_config* cfg, const void* const* weights,
                       void* stream, spec_model** out);
 void spec_model_destroy(spec_model* m);
@@ -165,7 +169,10 @@ int spec_device_error(spec_model* m, int32_t* host_bits);
 
 /* KV cache for `batch` sequences of up to `max_ctx` slots each, every layer,
  * K and V, in the model dtype: layout [layer][seq][kv_head][slot][hd]
- * (one allocation, never grown).  Lengths start at 0.  sync. */
+ * (one allocation, never grown).  Lengths start at 0.  sync.
+ * One static allocation, as the FlashSpec page, lnrk.cn/news/47842, section
+ * 4.3 advises.
+ */
 int spec_kv_create(spec_model* m, int32_t batch, int32_t max_ctx, spec_kv** out);
 
 /* Paged KV cache ("self-speculative decoding" page, m.lqnn.cn/news/278124,
@@ -217,7 +224,9 @@ int spec_prefill(spec_model* m, spec_kv* kv, int32_t seq, const int32_t* tokens,
  *   h_L      device f32 [batch][k+1][d] out: layer-L residual state of each row
  *   draft_logits device f32 [batch][k][V] out, nullable: the k draft rows
  * Writes KV layers [0, L) at slots s_b .. s_b+k; lengths unchanged.  async.
- * Requires exit_layer >= 1. */
+ * Requires exit_layer >= 1.
+ * Self-speculative decoding page, m.lqnn.cn/news/278124, sections 2.1 and 4.2.
+ */
 int spec_draft(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0, int32_t k,
                int32_t* cand, float* h_L, float* draft_logits, void* stream);
 
@@ -276,7 +285,10 @@ int spec_draft_tree(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* t0
  *   path     device int32 [batch][64]: accepted rows root first (tree mode
  *            with fused acceptance; nullable in chain mode).
  * Writes KV of the forward's layers at slots s_b .. s_b+n_rows[b]-1; lengths
- * unchanged.  async. */
+ * unchanged.  async.
+ * Self-speculative decoding page, sections 2.1 and 4.3; FlashSpec page,
+ * sections 2.2, 3.2, 4.1 and 5.2.
+ */
 int spec_verify(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows,
                 const float* h_in, int32_t h_stride, const int32_t* tokens,
                 int32_t tok_stride, const int32_t* tree_parent, float* logits,
@@ -318,7 +330,9 @@ int spec_draft_tree_dynamic(spec_model* m, spec_kv* kv, int32_t batch, const int
  * reads as the root).  n_rows[b] is the node count of sequence b's tree
  * (<= par_stride).  Acceptance (acc_len, next_tok and path, all three or
  * none) runs as its own kernel after the forward, with the tree rule of
- * spec_verify.  The attention always runs as its own kernel.  async. */
+ * spec_verify.  The attention always runs as its own kernel.  async.
+ * FlashSpec page, lnrk.cn/news/47842, sections 2.2 and 6.2.
+ */
 int spec_verify_trees(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows,
                       const float* h_in, int32_t h_stride, const int32_t* tokens,
                       int32_t tok_stride, const int32_t* parents, int32_t par_stride,
@@ -337,7 +351,9 @@ int spec_verify_trees(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* 
  * (residual max(0, p - q) in f32, or p when that is all zero, or the bonus
  * row p_k) is an integer inverse CDF over w = floor(r * 2^32) driven by
  * u[k].  Bit-exact and deterministic.  1 <= k <= 32, vocab <= 65536; a
- * target row of all zeros (invalid input) gives next_tok -1.  async. */
+ * target row of all zeros (invalid input) gives next_tok -1.  async.
+ * Self-speculative decoding page, m.lqnn.cn/news/278124, sections 2.4 and 4.3.
+ */
 int spec_accept(const float* p, const float* q, const int32_t* draft, int32_t draft_stride,
                 const float* u, int32_t batch, int32_t k, int32_t vocab, int32_t* acc_len,
                 int32_t* next_tok, void* stream);
@@ -362,14 +378,19 @@ int spec_probs(const float* logits, int64_t lg_stride, int32_t rows, int32_t voc
  * S = sum w, t = floor(m * S / 2^24) for u = m * 2^-24, token = smallest x
  * whose inclusive prefix sum of w exceeds t (-1 for a row of zero weights).
  *   probs device f32, row r at probs + r * p_stride; u device f32 [rows];
- *   tokens device int32 [rows] out.  vocab <= 53248.  async. */
+ *   tokens device int32 [rows] out.  vocab <= 53248.  async.
+ * The draws of the self-speculative decoding page, sections 2.4 and 4.3, in an
+ * exact integer form.
+ */
 int spec_sample(const float* probs, int64_t p_stride, int32_t rows, int32_t vocab,
                 const float* u, int32_t* tokens, void* stream);
 
 /* Greedy acceptance from target logits (the unfused form of spec_verify's
  * fused acceptance).  logits device f32 [batch][n_rows][vocab]; tokens device
  * int32 [batch][n_rows]; tree_parent host int32 [n_rows] or NULL (chain);
- * path device int32 [batch][64], nullable in chain mode.  async. */
+ * path device int32 [batch][64], nullable in chain mode.  async.
+ * Self-speculative decoding page, section 4.3; FlashSpec page, section 4.1.
+ */
 int spec_accept_greedy(const float* logits, const int32_t* tokens,
                        const int32_t* tree_parent, int32_t batch, int32_t n_rows,
                        int32_t vocab, int32_t* acc_len, int32_t* next_tok,
@@ -379,13 +400,18 @@ int spec_accept_greedy(const float* logits, const int32_t* tokens,
  * [batch].  Chain (path NULL): length s_b + acc_len[b] + 1.  Tree: path
  * device int32 [batch][path_stride] (root first) -- the rows of depth
  * 1..acc_len[b] move from slot s_b + path[b][d] to slot s_b + d in every
- * layer, then the length becomes s_b + acc_len[b] + 1.  async. */
+ * layer, then the length becomes s_b + acc_len[b] + 1.  async.
+ * Self-speculative decoding page, sections 3.3 and 4.5; FlashSpec page,
+ * section 4.1.
+ */
 int kv_commit(spec_kv* kv, int32_t batch, const int32_t* acc_len, const int32_t* path,
               int32_t path_stride, void* stream);
 
 /* Probabilities of the two largest logits of each row, from row summaries:
  * out[2r] = 1 / sum_exp, out[2r+1] = exp(top2 - top1) / sum_exp (float64).
- * stats device [rows]; out device f64 [rows][2].  async. */
+ * stats device [rows]; out device f64 [rows][2].  async.
+ * The confidence inputs of the DSpark page, 0539edu.com/news/4524681, section 2.2.
+ */
 int spec_row_probs(const spec_row_stats* stats, int32_t rows, double* out, void* stream);
 
 /* Confidence-scheduled draft length, one round, sequences [0, batch):
@@ -398,7 +424,9 @@ int spec_row_probs(const spec_row_stats* stats, int32_t rows, double* out, void*
  * conf = 0.4*mean(top1) + 0.3*min(5*mean(top1 - top2), 1) + 0.3*ema;
  * k_next = clamp(trunc(min_k + (max_k-min_k)*(conf-low)/(high-low)), min_k, max_k).
  * Float64 with one rounding per written operation, left to right, no
- * contraction; means are left-to-right sums divided by the count.  async. */
+ * contraction; means are left-to-right sums divided by the count.  async.
+ * DSpark page, 0539edu.com/news/4524681, sections 2.2 and 2.3.
+ */
 int spec_schedule_k(const double* top_probs, const int32_t* n_rows, const int32_t* acc_len,
                     double* ema, int32_t batch, const spec_k_schedule* sch, int32_t* k_next,
                     double* conf, void* stream);
@@ -409,7 +437,9 @@ int spec_schedule_k(const double* top_probs, const int32_t* n_rows, const int32_
  *   state    device int32 [batch][2 * window + 2]: each sequence's window
  *            (count, next slot, kept[window], drafted[window]); zero it
  *            before the first round
- *   k_next   device int32 [batch] out.  async. */
+ *   k_next   device int32 [batch] out.  async.
+ * Self-speculative decoding page, m.lqnn.cn/news/278124, section 3.2.
+ */
 int spec_schedule_aimd(const int32_t* acc_len, const int32_t* k_cur, int32_t* state, int32_t batch,
                        const spec_aimd_schedule* sch, int32_t* k_next, void* stream);
 
