@@ -34,6 +34,8 @@ draft's confidence (child_count).
 """
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 
 from .accept import (accept_greedy_chain, accept_greedy_tree, accept_sampling_chain,
@@ -301,6 +303,49 @@ def spec_round_greedy(dec, cache, t0, k):
     a, nxt = accept_greedy_chain(d, logits)
     cache.length = commit_chain(s, a)
     return list(d[:a]) + [nxt], a, nxt, logits
+
+
+def exit_layer_for_context(s, table):
+    """Exit layer for a committed context of ``s`` slots under a caller's table.
+
+    The self-speculative decoding page (m.lqnn.cn/news/278124, §5.3) asks for
+    a shallower exit on short contexts and a deeper one on long contexts, to
+    hold the acceptance rate as the draft's attention grows; it gives the
+    direction, not the numbers.  ``table`` holds (min_context, exit_layer)
+    pairs in increasing min_context, the first at 0: the pair with the
+    largest min_context <= s applies.
+    """
+    L = None
+    for lo, layer in table:
+        if s >= lo:
+            L = int(layer)
+    return L
+
+
+def with_exit_layer(dec, L):
+    """The same decoder and weights with draft exit layer ``L``."""
+    return type(dec)(dataclasses.replace(dec.shape, exit_layer=int(L)), dec.w)
+
+
+def generate_greedy_spec_context_exit(dec, prompt, n_new, k, table, max_ctx=None, log=None):
+    """Greedy self-speculative decoding whose exit layer follows the committed
+    context length: before each round's draft, L = exit_layer_for_context(s,
+    table).  A round writes every layer of its rows (layers [0, L) in the
+    draft, [L, N) in the verify), so the next round at another L finds its
+    whole context; equals :func:`generate_greedy_ar` for any table.  ``log``
+    receives ``(s, L, a)`` per round; returns ``(tokens, cache)``.
+    """
+    cache = dec.new_cache(max_ctx or (len(prompt) + n_new + k + 2))
+    t0 = argmax_lowest(dec.prefill(cache, prompt))
+    out = [t0]
+    while len(out) < n_new:
+        s = cache.length
+        L = exit_layer_for_context(s, table)
+        emitted, a, t0, _ = spec_round_greedy(with_exit_layer(dec, L), cache, t0, k)
+        out += emitted
+        if log is not None:
+            log.append((s, L, a))
+    return out[:n_new], cache
 
 
 def spec_round_sampling(dec, cache, t0, k, temp, top_p, u_draft, u):

@@ -340,3 +340,32 @@ def test_greedy_dynamic_tree_spec_equals_greedy_ar(deep, mass):
     log = []
     assert S.generate_greedy_dynamic_tree_spec(deep, pr, 40, [4, 2, 2], mass, log=log) == ar
     assert any(d > 0 for _, d, _ in log)
+
+
+# -- exit layer that follows the context length ------------------------------------
+def test_exit_layer_for_context_table():
+    table = [(0, 1), (16, 2), (40, 3)]
+    assert [S.exit_layer_for_context(s, table) for s in (0, 15, 16, 39, 40, 1000)] == [1, 1, 2, 2, 3, 3]
+
+
+def test_context_exit_layer_generation_is_lossless(deep):
+    """The exit layer moves from 1 to 2 to 3 as the context grows: the output
+    equals plain greedy decoding, and every layer of every committed row equals
+    a fresh prefill of the committed tokens (each round wrote all its layers)."""
+    pr = make_tokens(10, deep.shape.vocab, seed=8)
+    n_new, k = 40, 3
+    ar = S.generate_greedy_ar(deep, pr, n_new)
+    log = []
+    out, cache = S.generate_greedy_spec_context_exit(deep, pr, n_new, k, [(0, 1), (20, 2), (35, 3)], log=log)
+    assert out == ar
+    d3 = S.with_exit_layer(deep, 3)
+    assert d3.shape.exit_layer == 3 and d3.w is deep.w and deep.shape.exit_layer == 2
+    assert {L for _, L, _ in log} == {1, 2, 3}
+    assert all(L == (1 if s < 20 else 2 if s < 35 else 3) for s, L, _ in log)
+    n = min(cache.length, len(pr) + n_new - 1)
+    committed = list(pr) + out[:n - len(pr)]
+    fresh = deep.new_cache(n)
+    deep.prefill(fresh, np.array(committed))
+    for l in range(deep.n_layers):
+        np.testing.assert_allclose(cache.k[l][:n], fresh.k[l][:n], rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(cache.v[l][:n], fresh.v[l][:n], rtol=1e-9, atol=1e-11)
