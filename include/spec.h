@@ -167,6 +167,19 @@ void spec_model_destroy(spec_model* m);
 /* Read and clear the model's device error word (SPEC_DEVERR_* bits). sync. */
 int spec_device_error(spec_model* m, int32_t* host_bits);
 
+/* Exit layer L of the calls that follow: the drafts run layers [0, L), a
+ * verify from h_in runs layers [L, N).  Lets L follow the committed context
+ * length, shallower on short contexts and deeper on long ones.  The value is
+ * read when a call is enqueued: change it between rounds, never between a
+ * round's draft and its verify (h_in must come from a draft at the same L).
+ * A round writes every layer of its rows (layers [0, L) in the draft,
+ * [L, N) in the verify), so a later round at another L finds its whole
+ * context.  0 <= exit_layer < n_layers (0: verify from embeddings only).
+ * Host only.  Self-speculative decoding page, m.lqnn.cn/news/278124,
+ * section 5.3.
+ */
+int spec_set_exit_layer(spec_model* m, int32_t exit_layer);
+
 /* KV cache for `batch` sequences of up to `max_ctx` slots each, every layer,
  * K and V, in the model dtype: layout [layer][seq][kv_head][slot][hd]
  * (one allocation, never grown).  Lengths start at 0.  sync.

@@ -878,6 +878,15 @@ extern "C" int spec_device_error(spec_model* m, int32_t* host_bits) {
     return SPEC_OK;
 }
 
+extern "C" int spec_set_exit_layer(spec_model* m, int32_t exit_layer) {
+    if (!m) return set_error(SPEC_ERR_ARG, "spec_set_exit_layer: null model");
+    if (exit_layer < 0 || exit_layer >= m->cfg.n_layers)
+        return set_error(SPEC_ERR_ARG, "spec_set_exit_layer: exit_layer must be in [0, n_layers)");
+    // read by every later call when it is enqueued: nothing on the device depends on it
+    m->cfg.exit_layer = exit_layer;
+    return SPEC_OK;
+}
+
 // page = 0: contiguous cache (one page of max_ctx slots per sequence)
 static int kv_create(spec_model* m, int32_t batch, int32_t max_ctx, int32_t page, int32_t n_pages, spec_kv** out) {
     *out = nullptr;

@@ -28,7 +28,7 @@ EXPORTS = [
     "kv_commit", "spec_row_probs", "spec_schedule_k", "spec_profile", "spec_profile_read", "spec_launch_count",
     "spec_verify_noalloc", "spec_draft_sample", "spec_probs", "spec_sample", "spec_schedule_aimd",
     "spec_schedule_decay", "spec_draft_tree", "spec_kv_create_paged", "spec_kv_free_pages", "spec_kv_page_table",
-    "spec_draft_tree_dynamic", "spec_verify_trees",
+    "spec_draft_tree_dynamic", "spec_verify_trees", "spec_set_exit_layer",
 ]
 
 
@@ -87,6 +87,7 @@ def load(path: str = LIB_PATH):
         "spec_schedule_decay": ([P, P, I, I, P, P], I),
         "spec_draft_tree": ([P, P, I, P, POINTER(I), I, P, P, P, P], I),
         "spec_draft_tree_dynamic": ([P, P, I, P, POINTER(I), I, c_float, P, P, P, P, P, P], I),
+        "spec_set_exit_layer": ([P, I], I),
         "spec_verify_trees": ([P, P, I, POINTER(I), P, I, P, I, P, I, P, P, P, P, P, P], I),
         "spec_kv_create_paged": ([P, I, I, I, I, POINTER(P)], I),
         "spec_kv_free_pages": ([P, POINTER(I), P], I),
@@ -165,6 +166,11 @@ class Model:
         _check(lib.spec_model_create(ctypes.byref(cfg), arr, _stream(stream), ctypes.byref(h)))
         self.handle = h
         self.n_layers = cfg.n_layers
+
+    def set_exit_layer(self, exit_layer):
+        """Exit layer of the calls that follow (between rounds only)."""
+        _check(load().spec_set_exit_layer(self.handle, int(exit_layer)))
+        self.cfg.exit_layer = int(exit_layer)
 
     def profile(self, enable):
         _check(load().spec_profile(self.handle, 1 if enable else 0))
