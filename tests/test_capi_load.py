@@ -52,3 +52,12 @@ def test_header_compiles_as_plain_c():
     r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-x", "c", HEADER],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the compiled library the binding raises: there is no fallback."""
+    import pytest
+    from speculative_decoding_verify_04_gb300 import spec
+    monkeypatch.setattr(spec, "_lib", None)
+    with pytest.raises(spec.SpecError, match="missing"):
+        spec.load(str(tmp_path / "libspec.so"))
