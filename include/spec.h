@@ -207,6 +207,16 @@ int spec_kv_free_pages(spec_kv* kv, int32_t* host_free, void* stream);
 /* Page table, host int32 [batch][ceil(max_ctx / page)] (-1: no page; a
  * contiguous cache reports page b for sequence b).  sync. */
 int spec_kv_page_table(spec_kv* kv, int32_t* host_table, void* stream);
+
+/* Raw contents of one physical page of the pool, read without the page
+ * table: host buffer [n_kv_heads][page][head_dim] of the model dtype (bf16
+ * or f32) for K (which = 0) or V (which = 1) of `layer`.  A contiguous cache
+ * is read as pages of max_ctx slots, page b holding sequence b.  For
+ * inspection (tests, debugging): lets a caller check where the page table
+ * put each slot.  SPEC_ERR_ARG for a page, layer or `which` out of range.
+ * sync.  Self-speculative decoding page, m.lqnn.cn/news/278124, section 3.3
+ * (the pages a rollback keeps). */
+int spec_kv_read_page(spec_kv* kv, int32_t which, int32_t layer, int32_t page, void* host_dst, void* stream);
 void spec_kv_destroy(spec_kv* kv);
 
 /* Committed lengths: set from / copy to host int32 [batch].  sync. */
@@ -469,20 +479,24 @@ int spec_schedule_decay(const int32_t* generated, const int32_t* total, int32_t 
 
 /* spec_verify without any device memory of its own per call: same arguments,
  * results and stream semantics as spec_verify.  This entry point has no
- * counterpart in the method the pages describe; it exists for callers that
- * cannot call cudaMalloc where they verify (for example while another
- * component is capturing the stream into a CUDA graph, or when all device
- * memory is already handed to the caller's own pool).  The call's scratch --
- * the GEMM split-K partial tiles and arrival counters and the attention split
- * partials and counters -- comes from a 32 MiB static __device__ array that
- * every GPU loading the library keeps until the process exits.  The first call
- * on a device looks up the array's device address (cudaGetSymbolAddress) and
- * caches it; make that first call before any stream capture.  The array is
- * shared by every call and keeps the last call's contents, so each call clears
- * the counters it needs on `stream`; calls that overlap on the GPU (other
- * streams, other threads) race on the array and must not be issued.  Returns
+ * counterpart in the method the pages describe.  It is for callers that
+ * cannot call cudaMalloc where they verify: a serving runtime that hands all
+ * of the device's memory to its own pool at start-up (an allocation at verify
+ * time would fail or take memory the pool owns), or a latency-critical loop
+ * that cannot afford the device-wide synchronisation that cudaMalloc and
+ * cudaFree may imply.  The call's scratch -- the GEMM split-K partial tiles
+ * and arrival counters and the attention split partials and counters -- comes
+ * from a 32 MiB static __device__ array that every GPU loading the library
+ * keeps until the process exits.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture.  The array is shared by every call
+ * and keeps the last call's contents, so each call clears the counters it
+ * needs on `stream`; calls that overlap on the GPU (other streams, other
+ * threads) race on the array and must not be issued.  Returns
  * SPEC_ERR_CAPACITY with a message when a call needs more scratch than the
- * array holds.  Makes no cudaMalloc / cudaFree or other allocating call.  async. */
+ * array holds, and checks its other arguments as spec_verify does before it
+ * enqueues anything.  Makes no cudaMalloc / cudaFree or other allocating
+ * call.  async. */
 int spec_verify_noalloc(spec_model* m, spec_kv* kv, int32_t batch, const int32_t* n_rows,
                         const float* h_in, int32_t h_stride, const int32_t* tokens,
                         int32_t tok_stride, const int32_t* tree_parent, float* logits,

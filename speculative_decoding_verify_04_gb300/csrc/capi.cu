@@ -965,6 +965,20 @@ extern "C" int spec_kv_page_table(spec_kv* kv, int32_t* host_table, void* stream
     return SPEC_OK;
 }
 
+extern "C" int spec_kv_read_page(spec_kv* kv, int32_t which, int32_t layer, int32_t page, void* host_dst,
+                                 void* stream) {
+    if (!kv || !host_dst) return set_error(SPEC_ERR_ARG, "spec_kv_read_page: null pointer");
+    const spec_model_config& c = kv->m->cfg;
+    if (which < 0 || which > 1 || layer < 0 || layer >= c.n_layers || page < 0 || page >= kv->n_pages)
+        return set_error(SPEC_ERR_ARG, "spec_kv_read_page: which, layer or page out of range");
+    const size_t page_bytes = (size_t)c.n_kv_heads * kv->page * c.head_dim * kv->m->elem;
+    const char* src = static_cast<const char*>(which ? kv->v : kv->k) +
+                      ((size_t)layer * kv->n_pages + page) * page_bytes;
+    SPEC_CUDA(cudaMemcpyAsync(host_dst, src, page_bytes, cudaMemcpyDeviceToHost, (cudaStream_t)stream), "read page");
+    SPEC_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "read page sync");
+    return SPEC_OK;
+}
+
 extern "C" void spec_kv_destroy(spec_kv* kv) {
     if (!kv) return;
     cudaFree(kv->k);

@@ -1,14 +1,14 @@
 // spec_verify_noalloc: the verification forward with its per-call scratch in a
 // static device array instead of the model's workspace.
 //
-// Some callers cannot call cudaMalloc at the point where they verify: code
-// that runs while a stream is being captured into a CUDA graph by someone
-// else, runtimes whose device memory is fully handed to their own pool at
-// start-up, or latency-critical loops where an allocation's implicit
-// synchronisation is not acceptable.  For them this entry point takes the
-// GEMM split-K partial tiles and arrival counters, and the attention split
-// partials and counters, from `g_verify_scratch` below.  Every GPU that loads
-// the library holds this array (kScratchBytes) until the process exits.
+// Some callers cannot call cudaMalloc at the point where they verify: a
+// serving runtime that hands all of the device's memory to its own pool at
+// start-up, or a latency-critical loop that cannot afford the device-wide
+// synchronisation cudaMalloc and cudaFree may imply.  For them this entry
+// point takes the GEMM split-K partial tiles and arrival counters, and the
+// attention split partials and counters, from `g_verify_scratch` below.  Every
+// GPU that loads the library holds this array (kScratchBytes) until the
+// process exits.
 #include <mutex>
 
 #include "model.cuh"
@@ -64,7 +64,9 @@ extern "C" int spec_verify_noalloc(spec_model* m, spec_kv* kv, int32_t batch, co
                                    const float* h_in, int32_t h_stride, const int32_t* tokens, int32_t tok_stride,
                                    const int32_t* tree_parent, float* logits, spec_row_stats* stats,
                                    int32_t* acc_len, int32_t* next_tok, int32_t* path, void* stream) {
-    if (!m || !kv || !n_rows) return set_error(SPEC_ERR_ARG, "spec_verify_noalloc: null pointer");
+    // the cheap checks spec_verify makes, before anything is sized or enqueued
+    if (!m || !kv || !n_rows || !tokens) return set_error(SPEC_ERR_ARG, "spec_verify_noalloc: null pointer");
+    if (kv->m != m) return set_error(SPEC_ERR_ARG, "spec_verify_noalloc: cache of another model");
     if (batch < 1 || batch > kv->batch) return set_error(SPEC_ERR_ARG, "spec_verify_noalloc: bad batch");
     const spec_model_config& c = m->cfg;
     int T = 0, max_r = 1;
@@ -73,6 +75,7 @@ extern "C" int spec_verify_noalloc(spec_model* m, spec_kv* kv, int32_t batch, co
         T += n_rows[b];
         max_r = n_rows[b] > max_r ? n_rows[b] : max_r;
     }
+    if (T > c.max_rows) return set_error(SPEC_ERR_CAPACITY, "spec_verify_noalloc: sum of n_rows > max_rows");
     // scratch this call needs: counters (zeroed), GEMM partial tiles, attention partials
     const int tp = m->bf16 ? ((std::min(T, kMaxTPad) + 15) / 16) * 16 : 32;
     const int qdim = c.n_heads * c.head_dim;

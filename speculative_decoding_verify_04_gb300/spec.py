@@ -28,7 +28,7 @@ EXPORTS = [
     "kv_commit", "spec_row_probs", "spec_schedule_k", "spec_profile", "spec_profile_read", "spec_launch_count",
     "spec_verify_noalloc", "spec_draft_sample", "spec_probs", "spec_sample", "spec_schedule_aimd",
     "spec_schedule_decay", "spec_draft_tree", "spec_kv_create_paged", "spec_kv_free_pages", "spec_kv_page_table",
-    "spec_draft_tree_dynamic", "spec_verify_trees", "spec_set_exit_layer",
+    "spec_draft_tree_dynamic", "spec_verify_trees", "spec_set_exit_layer", "spec_kv_read_page",
 ]
 
 
@@ -92,6 +92,7 @@ def load(path: str = LIB_PATH):
         "spec_kv_create_paged": ([P, I, I, I, I, POINTER(P)], I),
         "spec_kv_free_pages": ([P, POINTER(I), P], I),
         "spec_kv_page_table": ([P, POINTER(I), P], I),
+        "spec_kv_read_page": ([P, I, I, I, P, P], I),
         "spec_accept_greedy": ([P, P, POINTER(I), I, I, I, P, P, P, P], I),
         "kv_commit": ([P, I, P, P, I, P], I),
         "spec_row_probs": ([P, I, P, P], I),
@@ -234,6 +235,15 @@ class KVCache:
         arr = (c_int32 * (self.batch * cols))()
         _check(load().spec_kv_page_table(self.handle, arr, _stream(stream)))
         return [list(arr[b * cols:(b + 1) * cols]) for b in range(self.batch)]
+
+    def read_page(self, which, layer, page, stream=None):
+        """Raw physical page ``page`` of the K (which 0) or V (which 1) pool of
+        ``layer``, read without the page table: host tensor [Hkv][page slots][hd]."""
+        s = self.model.shape
+        slots = self.page if self.page else self.max_ctx
+        out = torch.empty((s.n_kv_heads, slots, s.head_dim), dtype=self.model.torch_dtype).pin_memory()
+        _check(load().spec_kv_read_page(self.handle, which, layer, page, c_void_p(out.data_ptr()), _stream(stream)))
+        return out
 
     def set_lengths(self, lens, stream=None):
         _check(load().spec_kv_set_lengths(self.handle, _i32_array(lens), _stream(stream)))

@@ -212,3 +212,89 @@ def test_paged_sampling_and_tree_drafts_match_contiguous():
             assert torch.equal(a, b)
         assert rc[-1] == rp[-1]
     _check_pages(kv_p, n_pages)
+
+
+def test_paged_tables_and_rows_match_the_oracle_allocator():
+    """The paged cache against the oracle's page allocator (oracle/paged.py),
+    call by call: after every prefill, draft, commit and change of lengths the
+    GPU's page table and free count equal the allocator's.  The model's layers
+    past the exit layer add nothing (zero O and down projections), so every
+    round keeps all k drafts and sequences grow by k + 1 slots a round; a
+    rollback midway hands pages from one sequence to the others.  At the end
+    every committed K/V row of every layer is read from the raw pool at the
+    (page, row) the allocator names -- not through the library's page table --
+    and compared with the oracle decoder's cache."""
+    from speculative_decoding_verify_04_gb300 import spec
+    from oracle import spec as OS
+    from oracle.decoder import Decoder
+    from oracle.paged import PagePool
+    from synthetic import make_weights, weights_to_numpy
+    lib()
+    shape = SHAPES["tiny"]
+    w = make_weights(shape, 2, device="cuda")
+    for layer in w["layers"][shape.exit_layer:]:
+        layer["wo"].zero_()
+        layer["w_down"].zero_()
+    dec = Decoder(shape, weights_to_numpy(w))
+    model = spec.Model(shape, w, max_rows=64, max_batch=4, max_position=512)
+    del w
+    B, k, cap, n_pages = 3, 4, 320, 9
+    kv = spec.KVCache(model, B, cap, page=PAGE, n_pages=n_pages)
+    pool = PagePool(B, cap, PAGE, n_pages)
+    caches = [dec.new_cache(cap) for _ in range(B)]
+
+    def same():
+        assert kv.page_table() == pool.table
+        assert kv.free_pages() == pool.free_count()
+
+    prompts = [make_tokens(n, shape.vocab, seed=20 + b) for b, n in enumerate([40, 70, 130])]
+    t0 = []
+    for b, pr in enumerate(prompts):
+        nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+        spec.spec_prefill(model, kv, b, cuda_i32(pr), next_tok=nxt)
+        pool.ensure_relative([c.length for c in caches[:b + 1]], [0] * b + [len(pr)])
+        same()
+        t0.append(int(np.argmax(dec.prefill(caches[b], pr))))
+    cand = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
+    hL = torch.empty((B, k + 1, shape.d_model), dtype=torch.float32, device="cuda")
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    moved = False
+    for rnd in range(10):
+        if rnd == 5:
+            # roll sequences 0 and 1 back: their pages past the new lengths return to the pool
+            lens = [10, 64, caches[2].length]
+            kv.set_lengths(lens)
+            pool.set_lengths(lens)
+            same()
+            for b in range(B):
+                caches[b].length = lens[b]
+            t0 = [int(x) for x in make_tokens(B, shape.vocab, seed=29)]
+            moved = True
+        lens = [c.length for c in caches]
+        spec.spec_draft(model, kv, cuda_i32(t0), k, cand, hL)
+        pool.ensure_relative(lens, [k + 1] * B)
+        same()
+        spec.spec_verify(model, kv, [k + 1] * B, cand, k + 1, h_in=hL, h_stride=k + 1, acc_len=acc, next_tok=nxt)
+        spec.kv_commit(kv, acc)
+        torch.cuda.synchronize()
+        outs = [OS.spec_round_greedy(dec, caches[b], t0[b], k) for b in range(B)]
+        assert acc.cpu().tolist() == [o[1] for o in outs] == [k] * B
+        assert nxt.cpu().tolist() == [o[2] for o in outs]
+        assert kv.get_lengths() == [c.length for c in caches]
+        pool.release([c.length for c in caches])
+        same()
+        t0 = [o[2] for o in outs]
+    assert moved and model.device_error() == 0
+    # committed rows, read from the raw pool at the allocator's (page, row)
+    pages = {}
+    for b in range(B):
+        for s in range(caches[b].length):
+            page, row = pool.locate(b, s)
+            assert page >= 0
+            for layer in range(shape.n_layers):
+                for which, ref in ((0, caches[b].k[layer]), (1, caches[b].v[layer])):
+                    key = (which, layer, page)
+                    if key not in pages:
+                        pages[key] = kv.read_page(which, layer, page).float().numpy()
+                    np.testing.assert_allclose(pages[key][:, row, :], ref[s], atol=2e-3, rtol=0)

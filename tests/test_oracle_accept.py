@@ -446,3 +446,46 @@ def test_decay_k_table():
         assert A.decay_k(t, 100, 6) == k, (t, A.decay_k(t, 100, 6))
     assert A.decay_k(1, 8, 4) == 4          # 3.5 -> 4 (even)
     assert A.decay_k(3, 8, 4) == 2          # 2.5 -> 2 (even)
+
+
+# -- top-1 / top-2 probabilities of the confidence score (DSpark page, 0539edu.com/news/4524681, §2.2) --
+def test_top12_two_logits_is_logistic():
+    # two tokens: p(top) = 1 / (1 + e^-(l0 - l1)), p(second) = 1 - p(top)
+    for l0, l1 in [(1.5, -0.25), (0.0, 3.0), (-7.0, -7.5)]:
+        p1, p2 = A.top12_probs([l0, l1])
+        hi, lo = max(l0, l1), min(l0, l1)
+        want = 1.0 / (1.0 + np.exp(-(hi - lo)))
+        assert abs(p1 - want) < 1e-15 and abs(p2 - (1.0 - want)) < 1e-15
+
+
+def test_top12_hand_row_with_log_integer_logits():
+    # logits log(4), log(2), log(1), log(1): probabilities 4/8, 2/8, 1/8, 1/8 whatever the order
+    row = np.log(np.array([1.0, 4.0, 1.0, 2.0]))
+    p1, p2 = A.top12_probs(row)
+    assert abs(p1 - 0.5) < 1e-15 and abs(p2 - 0.25) < 1e-15
+    # a constant shift of every logit changes nothing
+    q1, q2 = A.top12_probs(row + 40.0)
+    assert abs(q1 - 0.5) < 1e-14 and abs(q2 - 0.25) < 1e-14
+
+
+def test_top12_tie_at_the_top_counts_both():
+    # the two largest logits tie: both probabilities are e^0 / sum = 2 / (2 + e^-1 + e^-2)
+    row = [0.0, 3.0, 2.0, 3.0, 1.0]
+    p1, p2 = A.top12_probs(row)
+    want = 1.0 / (2.0 + np.exp(-1.0) + np.exp(-2.0) + np.exp(-3.0))
+    assert abs(p1 - want) < 1e-15 and p1 == p2
+
+
+def test_top12_uniform_row():
+    for V in (2, 7, 1024):
+        p1, p2 = A.top12_probs(np.full(V, -1.25))
+        assert abs(p1 - 1.0 / V) < 1e-15 and abs(p2 - 1.0 / V) < 1e-15
+
+
+def test_top12_are_probabilities_not_logits():
+    # a clear winner: top1 near 1, top2 the second probability, both in (0, 1]
+    row = [10.0, 0.0, -1.0]
+    p1, p2 = A.top12_probs(row)
+    S = 1.0 + np.exp(-10.0) + np.exp(-11.0)
+    assert abs(p1 - 1.0 / S) < 1e-15 and abs(p2 - np.exp(-10.0) / S) < 1e-18
+    assert 0.0 < p2 < p1 <= 1.0
