@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single-thread-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--no-subs", action="store_true",
+                    help="default run only: skip the sub-records of the other configurations")
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers of the same shape (small case for profiler captures)")
     ap.add_argument("--exit-layer", type=int, default=None)
@@ -184,28 +187,171 @@ def oracle_round_sample(batch, k=K_DRAFT, ctx=CTX):
     return OracleRoundSample(k, ctx).run(batch)
 
 
+class OracleVerifySample(OracleRoundSample):
+    """The oracle's verify step on a bounded sample: one 7B-shape layer and the
+    LM head at k+1 rows over a ``ctx``-token context, scaled to the 20 layers
+    and the head of a verify step."""
+
+    def run(self, batch):
+        k = self.k
+        t, h = self._layer(k + 1), self._head(k + 1)
+        per_seq = 20 * t + h
+        desc = (f"one 7B-shape layer and the LM head at {k + 1} rows over a {self.ctx}-token context, "
+                f"scaled to a verify step (20 layers + head)")
+        return per_seq * batch, desc, _blas_threads()
+
+
+def _blas_threads():
+    import torch
+    threads = torch.get_num_threads()
+    try:
+        import threadpoolctl
+        threads = max([i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()] + [1])
+    except Exception:
+        pass
+    return threads
+
+
+class OracleFull:
+    """The whole 7B-shaped oracle for the reference arm: all 32 layers (float64
+    arithmetic over bf16 weights widened to float32, as the oracle stands), the
+    4096-token synthetic context, and one draft's layer-12 states of the k+1
+    candidate rows (setup, untimed).  ``verify_step`` runs layers 12..31 over the
+    k+1 rows and the LM head, the unit of the metric; ``round`` a whole round
+    (draft, verify, greedy acceptance, commit) from a fixed committed length."""
+
+    def __init__(self, k=K_DRAFT, ctx=CTX):
+        import numpy as np
+        from synthetic import SHAPES, make_weights, weights_to_numpy, make_kv_context, make_tokens
+        from oracle.decoder import Decoder
+        from oracle import spec as OS
+        self.k, self.ctx, self.OS = k, ctx, OS
+        self.shape = SHAPES["llama7b"]
+        w = make_weights(self.shape, SEED, device="cpu")
+        self.dec = Decoder(self.shape, weights_to_numpy(w))
+        del w
+        kc, vc = make_kv_context(self.shape, 1, ctx, SEED * 1000, device="cpu")
+        self.cache = self.dec.new_cache(ctx + k + 2)
+        self.cache.load(kc[:, 0].float().numpy(), vc[:, 0].float().numpy())
+        del kc, vc
+        self.t0 = int(make_tokens(1, self.shape.vocab, SEED, "t0")[0])
+        _, self.hL, _, _ = OS.draft(self.dec, self.cache, ctx, self.t0, k)
+        # the rows' state entering each quarter of the verify layers (for the bounded steps)
+        L, N = self.shape.exit_layer, self.shape.n_layers
+        self.bounds = [L + (N - L) * q // 4 for q in range(5)]
+        T = k + 1
+        self.slots = ctx + np.arange(T)
+        self.vis = OS.chain_visibility(ctx, T)
+        self.h_at = [np.asarray(self.hL, dtype=np.float64)]
+        for q in range(3):
+            self.h_at.append(self.dec.run_layers(self.h_at[-1], self.bounds[q], self.bounds[q + 1], self.slots,
+                                                 self.slots, self.vis, self.cache))
+
+    def verify_step(self):
+        t = time.perf_counter()
+        self.OS.verify(self.dec, self.cache, self.ctx, self.hL, self.shape.exit_layer)
+        return time.perf_counter() - t
+
+    def verify_quarter(self, q):
+        """A quarter of the verify step: its share of the layers from the state the
+        earlier quarters leave (the fourth quarter adds the LM head)."""
+        t = time.perf_counter()
+        h = self.dec.run_layers(self.h_at[q], self.bounds[q], self.bounds[q + 1], self.slots, self.slots,
+                                self.vis, self.cache)
+        if q == 3:
+            self.dec.logits(h)
+        return time.perf_counter() - t
+
+    def round(self):
+        from oracle.accept import accept_greedy_chain, commit_chain
+        t = time.perf_counter()
+        d, hL, _, _ = self.OS.draft(self.dec, self.cache, self.ctx, self.t0, self.k)
+        logits = self.OS.verify(self.dec, self.cache, self.ctx, hL, self.shape.exit_layer)
+        a, _ = accept_greedy_chain(d, logits)
+        commit_chain(self.ctx, a)                 # the committed length; the cache stays at ctx
+        return time.perf_counter() - t
+
+
+def oracle_tiny_generation():
+    """Config 1 in full: the tiny f32 decoder's 64-token greedy speculative generation (seconds)."""
+    from synthetic import SHAPES, make_weights, weights_to_numpy, make_tokens
+    from oracle.decoder import Decoder
+    from oracle import spec as OS
+    shape = SHAPES["tiny"]
+    dec = Decoder(shape, weights_to_numpy(make_weights(shape, 1, device="cpu")))
+    t = time.perf_counter()
+    OS.generate_greedy_spec(dec, make_tokens(32, shape.vocab, 1), 64, 4)
+    return time.perf_counter() - t
+
+
+def single_thread_sample():
+    """Runs in a child process whose BLAS pool has one thread: the verify-step
+    sample (one 7B layer and the head at k+1 rows) and config 1 in full."""
+    sec, desc, thr = OracleVerifySample().run(1)
+    print(json.dumps({"verify_step_s": sec, "sample": desc, "threads": thr, "tiny_generation_s": oracle_tiny_generation()}))
+
+
 def run_reference(args):
+    """The reference arm: the pages ship no code to install, so the reference is
+    the oracle (oracle/, float64 numpy), unchanged, on this machine's host cores.
+    One step = one complete verify step of the 7B-shaped configuration (layers
+    12..31 over the k+1 candidate rows and the LM head over a 4096-token
+    context), the unit of the metric.  Besides: one complete round, config 1 in
+    full, and a single-thread run of a bounded sample beside the all-cores one."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    if args.single_thread_sample:
+        return single_thread_sample()
     cores = os.cpu_count()
-    times = []
-    desc, threads = "", cores
-    sample = OracleRoundSample()          # weights and context built once, outside the steps
+    full = OracleFull()
+    # bounded steps: step i runs quarter i mod 4 of the verify step (5 of its 20 layers, the
+    # fourth with the LM head); the verify step's time is the sum of the quarters' means
+    quarters = [[] for _ in range(4)]
     for i in range(args.warmup + args.steps):
-        t, desc, threads = sample.run(args.batch)
+        t = full.verify_quarter(i % 4)
         if i >= args.warmup:
-            times.append(t)
-    per_round = statistics.mean(times)
-    cand = args.batch * (K_DRAFT + 1)
-    val = cand / per_round
+            quarters[i % 4].append(t)
+    for q in range(4):            # every quarter timed at least once
+        if not quarters[q]:
+            quarters[q].append(full.verify_quarter(q))
+    per_step = sum(statistics.mean(x) for x in quarters)
+    val = (K_DRAFT + 1) / per_step
+    whole_verify_s = full.verify_step()
+    round_s = full.round()
+    del full
+    tiny_all = oracle_tiny_generation()
+    sample_all = OracleVerifySample().run(1)[0]
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    one = None
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--impl", "reference",
+                            "--single-thread-sample"], env=env, capture_output=True, text=True, timeout=600)
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as exc:          # reported, not fatal: the all-cores figures stand
+        one = {"error": str(exc)[:200]}
+    threads = _blas_threads()
     line = {
         "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": per_round * 1e3, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random weights and KV context)",
-        "config": {"workload": WORKLOAD, "batch": args.batch, "k": K_DRAFT, "ctx": CTX},
+        "config": {"workload": WORKLOAD, "batch": 1, "k": K_DRAFT, "ctx": CTX, "value": VALUE_DEF},
         "impl": "reference",
-        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": "the 7B-shaped verify step (layers 12..31 and the LM head over 5 rows, context "
+                                   "4096): each timed step runs one quarter of it (5 layers, the fourth with the "
+                                   "head), cycling; ms_per_step is the sum of the quarters' means",
+                         "nproc": cores},
+        "oracle_verify_step_whole_s": whole_verify_s,
+        "oracle_round_s": round_s,
+        "oracle_round_candidate_tokens_per_s": (K_DRAFT + 1) / round_s,
+        "oracle_tiny_generation_s": tiny_all,
+        "oracle_tiny_accepted_tokens_per_s": 64 / tiny_all,
+        "single_thread_vs_all_cores": {
+            "sample": "one 7B-shape layer and the LM head at 5 rows over a 4096-token context, scaled to a verify "
+                      "step; and config 1's 64-token generation",
+            "all_cores": {"threads": threads, "verify_step_s": sample_all, "tiny_generation_s": tiny_all},
+            "one_thread": one},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -269,6 +415,20 @@ def job_rate(world, units_per_rank, seconds):
     return world * units_per_rank / seconds
 
 
+def shard_range(n, world, rank):
+    """Sequences [start, stop) of one global batch of ``n`` that rank ``rank`` of
+    ``world`` runs: contiguous shares whose sizes differ by at most one, in rank
+    order.  The batched workloads draw every input from streams keyed by the
+    sequence's index in the global batch, so the shards of all ranks together
+    are exactly the undivided batch."""
+    base, extra = divmod(n, world)
+    start = rank * base + min(rank, extra)
+    return start, start + base + (1 if rank < extra else 0)
+
+
+VALUE_DEF = ("verified candidate tokens/s: candidate rows verified per verify step over the verify step's device "
+             "time (spec_verify: layers L..N-1 over every candidate row, the LM head and the fused acceptance); "
+             "ms_per_step is the whole round (draft, verify, acceptance, commit)")
 ADAPTIVE = ("llama7b-shape layer-skip self-spec (draft 12/32 layers), batch 32, contexts U{512..8192}, "
             "per-sequence k in [2,16] from the confidence schedule, greedy")
 B_ADAPT, K_MIN, K_MAX, K_START, EMA_START = 32, 2, 16, 2, 0.5
@@ -382,10 +542,7 @@ def run_tiny(args, spec, world, rank, local, dist):
         t = time.perf_counter() - tw
         line["cpu_baseline"] = {"value": n_new / t, "unit": "tokens/s (accepted)", "cores": os.cpu_count(),
                                 "kind": "oracle", "sample": "one whole 64-token generation"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    return line
 
 
 def run_accept(args, spec, world, rank, local, dist):
@@ -399,8 +556,9 @@ def run_accept(args, spec, world, rank, local, dist):
     import numpy as np
     import torch
     from synthetic import make_accept_inputs
-    B, k, V = 256, 5, 32000
-    p, q, x, u = make_accept_inputs(B, k, V, seed=2 + rank)
+    B, k, V = 256, 5, 32000          # sequences per rank; the global batch is world x 256
+    first, _ = shard_range(B * world, world, rank)
+    p, q, x, u = make_accept_inputs(B, k, V, seed=2, first=first)
     pg, qg = torch.from_numpy(p).cuda(), torch.from_numpy(q).cuda()
     xg, ug = torch.from_numpy(x.astype(np.int32)).cuda(), torch.from_numpy(u).cuda()
     acc = torch.empty(B, dtype=torch.int32, device="cuda")
@@ -444,7 +602,9 @@ def run_accept(args, spec, world, rank, local, dist):
     }
     line = _line(args, world, steps, warm, sec, B * k * steps, "f32",
                  {"workload": "acceptance alone: batch 256, k=5, vocab 32000, logits N(0,3^2), draft = target + N(0,1)",
-                  "l2": "inputs larger than L2 (360 MB of p and q)"}, extra)
+                  "l2": "inputs larger than L2 (360 MB of p and q)",
+                  "parallelism": "data parallel over sequences (one global batch, sharded)" if world > 1
+                  else "single GPU"}, extra)
     line["value_note"] = "draft tokens decided per second"
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import accept as A
@@ -455,10 +615,7 @@ def run_accept(args, spec, world, rank, local, dist):
         t = (time.perf_counter() - tw) / n
         line["cpu_baseline"] = {"value": k / t, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                 "sample": f"{n} of the 256 sequences, one at a time"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    return line
 
 
 def run_tree8(args, spec, world, rank, local, dist):
@@ -542,10 +699,7 @@ def run_tree8(args, spec, world, rank, local, dist):
         t = time.perf_counter() - tw
         line["cpu_baseline"] = {"value": n / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": "one tree verification over a 2048-slot synthetic context"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    return line
 
 
 def run_adaptive(args, spec, world, rank, local, dist):
@@ -559,15 +713,16 @@ def run_adaptive(args, spec, world, rank, local, dist):
     shape = SHAPES["llama7b"]
     B = B_ADAPT
     steps, warm = args.steps, args.warmup
-    lens = [int(x) for x in make_ragged_contexts(B, 512, 8192, seed=5 + 1000 * rank)]
+    first, _ = shard_range(B * world, world, rank)
+    lens = [int(x) for x in make_ragged_contexts(B * world, 512, 8192, seed=5)[first:first + B]]
     cap = max(lens) + (steps + warm + 2) * (K_MAX + 1) + 8
-    w = make_weights(shape, SEED + rank, device="cuda")
+    w = make_weights(shape, SEED, device="cuda")
     model = spec.Model(shape, w, max_rows=B * (K_MAX + 1), max_batch=B, max_position=cap + 8)
     del w
     torch.cuda.empty_cache()
     kv = spec.KVCache(model, B, cap)
     for b in range(B):
-        kc, vc = make_kv_context(shape, 1, lens[b], SEED * 1000 + rank * 100 + b, device="cuda")
+        kc, vc = make_kv_context(shape, 1, lens[b], SEED * 1000 + first + b, device="cuda")
         kv.import_rows(b, 0, kc[:, 0].contiguous(), vc[:, 0].contiguous())
         del kc, vc
     torch.cuda.synchronize()
@@ -576,7 +731,7 @@ def run_adaptive(args, spec, world, rank, local, dist):
 
     d = shape.d_model
     R = B * (K_MAX + 1)
-    t0 = torch.from_numpy(make_tokens(B, shape.vocab, SEED, "t0")).cuda()
+    t0 = torch.from_numpy(make_tokens(B * world, shape.vocab, SEED, "t0")[first:first + B]).cuda()
     cand_buf = torch.empty(R, dtype=torch.int32, device="cuda")
     hl_buf = torch.empty(R * d, dtype=torch.float32, device="cuda")
     stats = torch.empty((R, 4), dtype=torch.float32, device="cuda")
@@ -657,7 +812,7 @@ def run_adaptive(args, spec, world, rank, local, dist):
     verify_bytes = steps * (n_ver * layer_w + V * d * 2) + n_ver * 2 * shape.n_kv_heads * shape.head_dim * 2 * mean_ctx * B * steps
     line = {
         "metric": METRIC,
-        "value": job_rate(world, rows, wall_s),
+        "value": job_rate(world, rows, verify_s),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": steps,
@@ -668,14 +823,17 @@ def run_adaptive(args, spec, world, rank, local, dist):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded random-init weights and KV contexts; no dataset)",
-        "config": {"workload": ADAPTIVE, "batch": B, "k_range": [K_MIN, K_MAX], "ctx_range": [512, 8192],
+        "config": {"workload": ADAPTIVE, "batch": B, "global_batch": B * world, "k_range": [K_MIN, K_MAX],
+                   "ctx_range": [512, 8192], "value": VALUE_DEF,
                    "ctx_mean": sum(lens) / B, "exit_layer": shape.exit_layer, "n_layers": shape.n_layers,
                    "l2": "inputs larger than L2 (weights and ~45 GB of KV re-streamed each round)",
                    "parallelism": "data parallel over sequences" if world > 1 else "single GPU"},
+        "round_candidate_tokens_per_s": job_rate(world, rows, wall_s),
         "accepted_tokens_per_s": job_rate(world, accepted, wall_s),
         "rows_per_round": rows / steps,
         "max_k_seen": log["kmax"],
         "verify_ms": verify_s * 1e3 / steps,
+        "verify_bytes": verify_bytes / steps,
         "verify_candidate_tokens_per_s": job_rate(world, rows, verify_s),
         "verify_hbm_gbs": verify_bytes / verify_s / 1e9,
         "verify_hbm_frac": verify_bytes / verify_s / 1e9 / hbm,
@@ -693,62 +851,42 @@ def run_adaptive(args, spec, world, rank, local, dist):
         sec, desc, thr = oracle_round_sample(B, k=kbar, ctx=int(sum(lens) / B))
         line["cpu_baseline"] = {"value": B * (kbar + 1) / sec, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                                 "sample": desc}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    return line
 
 
-def main():
-    args = parse()
-    if args.impl == "reference":
-        return run_reference(args)
-
+def run_chain(args, spec, world, rank, local, dist, batch=None):
+    """The benchmark's main workload: layer-skip greedy (or sampling, tree) rounds
+    on the 7B-shaped model at context 4096, ``batch`` (default ``--batch``)
+    sequences a rank.  Returns the JSON line."""
     import torch
-    import torch.distributed as dist
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-    import __graft_entry__
-    __graft_entry__.build()
-    from speculative_decoding_verify_04_gb300 import spec
     from synthetic import SHAPES, make_weights, make_kv_context, make_tokens, make_uniforms
-    if args.workload in ("tiny", "accept", "tree8"):
-        return {"tiny": run_tiny, "accept": run_accept, "tree8": run_tree8}[args.workload](
-            args, spec, world, rank, local, dist)
-    if args.workload == "adaptive":
-        return run_adaptive(args, spec, world, rank, local, dist)
-
     import dataclasses
     shape = SHAPES["llama7b"]
     if args.layers is not None:
         shape = dataclasses.replace(shape, n_layers=args.layers,
                                     exit_layer=args.exit_layer if args.exit_layer is not None else args.layers // 2)
-    B, k = args.batch, K_DRAFT
+    B, k = (batch or args.batch), K_DRAFT
+    first, _ = shard_range(B * world, world, rank)
     steps, warm = args.steps, args.warmup
     tree_arg = [int(x) for x in args.tree.split(",")] if args.tree else None
     n_cand = 1 + sum(math.prod(tree_arg[:i + 1]) for i in range(len(tree_arg))) if tree_arg else k + 1
     per_round = len(tree_arg) + 1 if tree_arg else k + 1         # most tokens a round commits
     rounds_total = warm + 2 * steps + max(3, steps // 2) + 1
     grow = rounds_total * per_round + n_cand + 8
-    w = make_weights(shape, SEED + rank, device="cuda")
+    w = make_weights(shape, SEED, device="cuda")
     model = spec.Model(shape, w, max_rows=max(64, B * n_cand), max_batch=B, max_position=CTX + grow + 64)
     del w
     torch.cuda.empty_cache()
     kv = spec.KVCache(model, B, CTX + grow, page=args.page or None)
     for b in range(B):
-        kc, vc = make_kv_context(shape, 1, CTX, SEED * 1000 + rank * 100 + b, device="cuda")
+        kc, vc = make_kv_context(shape, 1, CTX, SEED * 1000 + first + b, device="cuda")
         kv.import_rows(b, 0, kc[:, 0].contiguous(), vc[:, 0].contiguous())
         del kc, vc
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     kv.set_lengths([CTX] * B)
 
-    t0 = torch.from_numpy(make_tokens(B, shape.vocab, SEED, "t0")).cuda()
+    t0 = torch.from_numpy(make_tokens(B * world, shape.vocab, SEED, "t0")[first:first + B]).cuda()
     cand = torch.empty((B, k + 1), dtype=torch.int32, device="cuda")
     hL = torch.empty((B, k + 1, shape.d_model), dtype=torch.float32, device="cuda")
     acc = torch.zeros(B, dtype=torch.int32, device="cuda")
@@ -909,7 +1047,7 @@ def main():
     hbm, peak_kind = peaks()
     # candidate rows verified a round: the full tree, or the dynamic trees' node counts
     cand_per_step = B * n_cand if not dynamic else sum(nodes_log) / len(nodes_log)
-    value = job_rate(world, cand_per_step * steps, ms / 1e3)
+    value = job_rate(world, cand_per_step, verify_ms / 1e3)
     g_avg_ms = g_ms / max(g_n, 1)
     g_avg_bytes = g_bytes / max(g_n, 1)
     achieved = g_avg_bytes / (g_avg_ms / 1e3) / 1e9 if g_n else None
@@ -940,15 +1078,20 @@ def main():
         "dtype": "bf16",
         "data": "synthetic (seeded random-init weights and KV context; no dataset)",
         "config": {"workload": workload if args.layers is None else workload + f" (reduced: {shape.n_layers} layers)",
+                   "value": VALUE_DEF,
                    "mode": args.mode,
-                   "batch": B, "k": k if not tree else None, "tree": args.tree, "tree_mass": args.tree_mass,
+                   "batch": B, "global_batch": B * world, "k": k if not tree else None, "tree": args.tree, "tree_mass": args.tree_mass,
                    "ctx": CTX,
                    "kv": f"paged, {args.page}-slot pages" if args.page else "contiguous", "exit_layer": shape.exit_layer, "n_layers": shape.n_layers,
                    "l2": "inputs larger than L2 (13.5 GB weights re-streamed each round)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": ("replicas (one sequence a rank)" if B == 1 else
+                                   "data parallel over sequences (one global batch, sharded)") if world > 1
+                   else "single GPU"},
+        "round_candidate_tokens_per_s": job_rate(world, cand_per_step * steps, ms / 1e3),
         "accepted_tokens_per_s": world * (accepted + B * steps) / (ms / 1e3),
         "acceptance_rate": accepted / (B * steps * (per_round - 1)),
         "verify_ms": verify_ms,
+        "verify_bytes": verify_bytes,
         "verify_candidate_tokens_per_s": world * cand_per_step / (verify_ms / 1e3),
         "verify_hbm_gbs": verify_bytes / (verify_ms / 1e3) / 1e9,
         "verify_hbm_frac": verify_bytes / (verify_ms / 1e3) / 1e9 / hbm,
@@ -969,12 +1112,70 @@ def main():
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": 4 * B * (n_cand + 2 + (1 if dynamic else 0))},
+                "d2h_bytes_per_step": 4 * B * (n_cand + 2 + (1 if dynamic else 0)),
+                "note": "candidate tokens over whole rounds through the public API, the round's inputs copied in "
+                        "from pinned host memory and its tokens read back every round"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sec, desc, thr = oracle_round_sample(B)
+        sec, desc, thr = OracleVerifySample().run(B)
         line["cpu_baseline"] = {"value": cand_per_step / sec, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                                 "sample": desc}
+    return line
+
+
+
+
+SUBS = (("llama7b_chain_k4_ctx4096_batch8", "chain8"), ("llama7b_adaptive_k_batch32_ctx512_8192", "adaptive"),
+        ("accept_batch256_k5_vocab32000", "accept"), ("tree8_d1024_ctx2048_tree422", "tree8"),
+        ("tiny_fp32_64_tokens", "tiny"))
+SUB_KEYS = ("value", "unit", "steps", "warmup", "ms_per_step", "higher_is_better", "dtype", "config", "value_note",
+            "round_candidate_tokens_per_s", "accepted_tokens_per_s", "verify_ms", "verify_candidate_tokens_per_s",
+            "verify_hbm_gbs", "verify_hbm_frac", "verify_bytes", "roofline", "attention", "mean_accepted",
+            "sequences_per_s", "rows_per_round", "gpu_launches", "clocks", "e2e")
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import argparse as _ap
+    import gc
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from speculative_decoding_verify_04_gb300 import spec
+    runs = {"tiny": run_tiny, "accept": run_accept, "tree8": run_tree8, "adaptive": run_adaptive}
+    if args.workload in runs:
+        line = runs[args.workload](args, spec, world, rank, local, dist)
+    else:
+        line = run_chain(args, spec, world, rank, local, dist)
+        default = (args.batch == 1 and args.mode == "greedy" and not args.tree and not args.page and
+                   args.layers is None)
+        if default and not args.no_subs:
+            # the other configurations, each timed the same way (CUDA events on the
+            # launching stream, warm-up first, clocks sampled), as sub-records of this line
+            sub_args = _ap.Namespace(**vars(args))
+            sub_args.steps, sub_args.warmup, sub_args.no_cpu_baseline = min(args.steps, 20), max(3, args.warmup), True
+            subs = {}
+            for name, kind in SUBS:
+                gc.collect()
+                torch.cuda.empty_cache()
+                if kind == "chain8":
+                    sub = run_chain(sub_args, spec, world, rank, local, dist, batch=8)
+                else:
+                    sub = runs[kind](sub_args, spec, world, rank, local, dist)
+                subs[name] = {k2: sub[k2] for k2 in SUB_KEYS if k2 in sub}
+            line["sub_workloads"] = subs
+            line["gpu_launches_sub_workloads"] = sum(int(v.get("gpu_launches") or 0) for v in subs.values())
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -167,6 +167,19 @@ void spec_model_destroy(spec_model* m);
 /* Read and clear the model's device error word (SPEC_DEVERR_* bits). sync. */
 int spec_device_error(spec_model* m, int32_t* host_bits);
 
+/* Failure injection for tests of the bounded-wait abort path (no counterpart
+ * in the pages' method).  The next GEMM chain launch of this model that has
+ * two or more phases runs with CTA `cta` withholding its arrival at the grid
+ * barrier after the first phase, and every grid-barrier wait of that launch
+ * gives up after `wait_ns` nanoseconds instead of 2 s.  The launch then ends
+ * through its abort path: the waiting CTAs raise SPEC_DEVERR_TIMEOUT, let
+ * their copies in flight land, drain their MMAs, free their tensor memory and
+ * exit; the last one out resets the barrier counters, so the next call runs
+ * normally.  That call's results are invalid.  Nothing faults or hangs: the
+ * kernel returns within about `wait_ns`.  cta in [0, SMs), wait_ns in
+ * [1e6, 2e9].  One-shot; host only. */
+int spec_test_stall_next_chain(spec_model* m, int32_t cta, int64_t wait_ns);
+
 /* Exit layer L of the calls that follow: the drafts run layers [0, L), a
  * verify from h_in runs layers [L, N).  Lets L follow the committed context
  * length, shallower on short contexts and deeper on long ones.  The value is

@@ -509,6 +509,9 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
     // attention as the first phase of the chain that follows it (one launch per layer)
     // (the phase reads one tree for the batch: a tree a sequence takes the separate kernel)
     const bool fused = tree != 2 && T <= kMaxTPad && attn_phase_ok(m, kv, batch, max_rows_per_seq);
+    // otherwise the same phase as a launch of its own: K/V through the TMA ring, the
+    // committed slots streamed before the wait for the previous kernel
+    const bool ring = !fused && tree != 2 && T <= kMaxTPad && attn_ring_ok(m, kv, batch, max_rows_per_seq);
     GemmStep pend[5];
     int np = 0;
     for (int l = lo; l < hi; ++l) {
@@ -523,7 +526,7 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             SPEC_TRY(launch_gemm_chain(m, pend, np, st));
             np = 0;
         }
-        if (fused) {   // attention phase
+        if (fused || ring) {   // attention phase (of the chain that follows, or alone)
             GemmStep at{};
             at.kind = PH_ATTN;
             at.g.tmW = &kv->tm_k;
@@ -543,7 +546,8 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             at.at.linear = max_rows_per_seq * (c.n_heads / c.n_kv_heads) <= kAttnSimtQ;
             at.at.kc = kv->k;
             at.at.vc = kv->v;
-            pend[np++] = at;
+            if (fused) pend[np++] = at;
+            else SPEC_TRY(launch_gemm_chain(m, &at, 1, st));
         } else {   // attention
             AttnParams a{};
             a.q = m->q;
@@ -703,6 +707,13 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
         // of two or more sequences (measured faster there; the separate kernel is faster for one)
         const char* ae = getenv("SPEC_ATTN_PHASE");
         m->attn_phase = (ae && ae[0] == '1') ? 1 : ((ae && ae[0] == '0') ? 0 : -1);
+        // SPEC_L2_AHEAD=n: GEMM weight units a chain CTA prefetches into L2 at each phase start
+        const char* le = getenv("SPEC_L2_AHEAD");
+        if (le) m->l2_ahead = std::max(0, std::min(256, atoi(le)));
+        // SPEC_ATTN_RING=1: attention outside a chain runs as a one-phase ring launch
+        // (measured slower than the register-tile kernel at batch 1, so off by default)
+        const char* re = getenv("SPEC_ATTN_RING");
+        m->attn_ring = re && re[0] == '1';
     }
     m->elem = m->bf16 ? 2 : 4;
     if (m->bf16) {
@@ -875,6 +886,15 @@ extern "C" int spec_device_error(spec_model* m, int32_t* host_bits) {
     SPEC_CUDA(cudaMemcpy(&v, m->err, 4, cudaMemcpyDeviceToHost), "read device error");
     SPEC_CUDA(cudaMemset(m->err, 0, 4), "clear device error");
     *host_bits = v;
+    return SPEC_OK;
+}
+
+extern "C" int spec_test_stall_next_chain(spec_model* m, int32_t cta, int64_t wait_ns) {
+    if (!m) return set_error(SPEC_ERR_ARG, "spec_test_stall_next_chain: null model");
+    if (cta < 0 || cta >= m->num_sms || wait_ns < 1000000 || wait_ns > 2000000000)
+        return set_error(SPEC_ERR_ARG, "spec_test_stall_next_chain: cta in [0, SMs), wait_ns in [1 ms, 2 s]");
+    m->test_stall_cta = cta;
+    m->test_wait_ns = (unsigned long long)wait_ns;
     return SPEC_OK;
 }
 

@@ -117,11 +117,19 @@ size_t attn_phase_part_floats(const spec_model* m) {
     return (size_t)m->num_sms * 2 * kAttnMaxQ * (m->cfg.head_dim + 2);
 }
 
-bool attn_phase_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq) {
+static bool attn_phase_fits(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq) {
     const int G = m->cfg.n_heads / m->cfg.n_kv_heads;
-    const bool wanted = m->attn_phase == 1 || (m->attn_phase == -1 && batch >= 2);
-    return wanted && kv->tmaps && max_rows_per_seq * G <= kAttnMaxQ && batch <= kMaxPlanBatch &&
+    return kv->tmaps && max_rows_per_seq * G <= kAttnMaxQ && batch <= kMaxPlanBatch &&
            m->attn_part_floats >= attn_phase_part_floats(m) && m->n_attn_counters >= batch * m->cfg.n_kv_heads;
+}
+
+bool attn_phase_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq) {
+    const bool wanted = m->attn_phase == 1 || (m->attn_phase == -1 && batch >= 2);
+    return wanted && attn_phase_fits(m, kv, batch, max_rows_per_seq);
+}
+
+bool attn_ring_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq) {
+    return m->attn_ring && attn_phase_fits(m, kv, batch, max_rows_per_seq);
 }
 
 // ---------------------------------------------------------------------------
@@ -504,6 +512,9 @@ struct GemmChain {
     int attn;      // index of the attention phase, -1 if none (at most one)
     int* bar;      // per launch: CTAs that finished a phase, summed over phases
     int* done;     // CTAs that finished the chain; the last one resets both counters
+    unsigned long long wait_ns;   // limit of the grid-barrier waits
+    int l2_ahead;  // weight units of a GEMM phase, past the ring's first fill, prefetched into L2 early
+    int stall_cta; // failure injection (tests): this CTA withholds its arrival after phase 0; -1 none
 };
 
 SPEC_DEV int ld_acquire_gpu(const int* p) {
@@ -516,15 +527,15 @@ SPEC_DEV void red_release_gpu_add(int* p, int v) {
 }
 // orders this thread's generic-proxy global accesses with later async-proxy (TMA) ones
 SPEC_DEV void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-// bounded wait until every CTA has finished `phases` phases
-SPEC_DEV bool grid_wait(const int* bar, int target, volatile int* abort_flag, int* err) {
+// bounded wait until every CTA has finished `phases` phases (at most limit_ns)
+SPEC_DEV bool grid_wait(const int* bar, int target, volatile int* abort_flag, int* err, uint64_t limit_ns) {
     if (ld_acquire_gpu(bar) >= target) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (ld_acquire_gpu(bar) >= target) return true;
         if ((it & 63u) == 0u) {
             if (abort_flag && *abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 if (abort_flag) *abort_flag = 1;
                 dev_error(err, SPEC_DEVERR_TIMEOUT);
                 return false;
@@ -619,10 +630,25 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
             // phase 0) waits for it; weight tiles and committed KV slots do not
             auto dep_wait = [&](int p) -> bool {
                 if (p == 0) { pdl_wait(); return true; }
-                if (!grid_wait(ch.bar, G * p, abort_flag, err)) return false;
+                if (!grid_wait(ch.bar, G * p, abort_flag, err, ch.wait_ns)) return false;
                 fence_proxy_async_global();     // the rows were written by other CTAs' epilogues
                 return true;
             };
+            // L2 prefetch of phase q's weight units [stages, stages + l2_ahead) of this CTA's
+            // range: issued when the producer has nothing else to issue (before the previous
+            // kernel completes, and when the previous phase's last unit is out), so HBM keeps
+            // streaming through the phase boundary; the ring's later loads of them hit L2
+            auto prefetch_phase = [&](int q) {
+                if (q >= ch.n || ch.ph[q].kind != PH_GEMM || ch.l2_ahead <= 0) return;
+                const Split& sq = ch.ph[q].sp;
+                long long qb, qe;
+                cta_units(sq, c, qb, qe);
+                qb += L.stages;
+                qe = min(qe, qb + ch.l2_ahead);
+                for (long long u = qb; u < qe; ++u)
+                    tma_prefetch_l2_2d(&ch.ph[q].tmW, (int)(u % sq.kb) * kTileK, (int)(u / sq.kb) * kTileN);
+            };
+            prefetch_phase(0);
             for (int p = 0; ok && p < ch.n; ++p) {
                 P = &ch.ph[p];
                 n_def = 0;
@@ -699,6 +725,7 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                         ++a_issued;
                         if (++a_slot == R.n) { a_slot = 0; a_phase ^= 1u; }
                     }
+                    prefetch_phase(p + 1);
                     // wait for the dependency even without a dependent unit: the grid
                     // barrier of the next phase is only meaningful once the previous
                     // kernel (which resets it) has completed
@@ -736,7 +763,9 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                     ++issued;
                     if (++stage == L.stages) { stage = 0; phase ^= 1u; }
                     if (++kbi == sp.kb) { kbi = 0; ++tile; }
+                    if (i == n_units - 1) prefetch_phase(p + 1);
                 }
+                if (n_units == 0) prefetch_phase(p + 1);
                 if (ok && !dep) {
                     if (!dep_wait(p)) { ok = false; }
                     else {
@@ -811,7 +840,7 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
         for (int p = 0; ok && p < ch.n; ++p) {
             const GemmPhase& P = ch.ph[p];
             if (p > 0) {
-                if (etid() == 0) sm.wait_ok = grid_wait(ch.bar, G * p, abort_flag, err) ? 1 : 0;
+                if (etid() == 0) sm.wait_ok = grid_wait(ch.bar, G * p, abort_flag, err, ch.wait_ns) ? 1 : 0;
                 named_bar(1, 128);
                 const int w_ok = sm.wait_ok;
                 named_bar(1, 128);
@@ -854,7 +883,7 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
             if (ok && ch.n > 1) {
                 // this CTA's share of phase p is written: count it (release)
                 named_bar(1, 128);
-                if (etid() == 0) {
+                if (etid() == 0 && !(c == ch.stall_cta && p == 0)) {
                     fence_proxy_async_global();
                     __threadfence();
                     red_release_gpu_add(ch.bar, 1);
@@ -1070,6 +1099,14 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
     ch.n = n;
     ch.bar = chain_bar(m);
     ch.done = chain_done(m);
+    ch.wait_ns = kWaitLimitNs;
+    ch.l2_ahead = m->l2_ahead;
+    ch.stall_cta = -1;
+    if (n > 1 && m->test_stall_cta >= 0) {      // one-shot failure injection (tests)
+        ch.stall_cta = m->test_stall_cta;
+        ch.wait_ns = m->test_wait_ns;
+        m->test_stall_cta = -1;
+    }
     TcLayout L = tc_layout(T_pad, m->max_rows_pad, ch.attn >= 0);
     const size_t smem = tc_smem_bytes(L);
     if (smem > 227 * 1024) return set_error(SPEC_ERR_CAPACITY, "GEMM chain: shared memory layout too large");
@@ -1081,6 +1118,7 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
         attr_set = true;
     }
     const int slot = prof_start(m, st);
+    const int kind = (n == 1 && ch.attn == 0) ? PROF_ATTN : PROF_GEMM;    // an attention launch of its own
     if (ch.attn >= 0 && ch.ph[ch.attn].e.kvp.shift >= 0)
         launch_k(m->pdl, gemm_tc_kernel<true, true>, dim3(G), dim3(kTcThreads), smem, st, ch, L);
     else if (ch.attn >= 0)
@@ -1088,7 +1126,7 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
     else
         launch_k(m->pdl, gemm_tc_kernel<false>, dim3(G), dim3(kTcThreads), smem, st, ch, L);
     ++m->launches;
-    prof_stop(m, slot, st, PROF_GEMM, bytes);
+    prof_stop(m, slot, st, kind, kind == PROF_GEMM ? bytes : 0.0);
     return check_cuda(cudaGetLastError(), "GEMM launch");
 }
 

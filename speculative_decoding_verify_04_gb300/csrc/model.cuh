@@ -157,6 +157,11 @@ struct spec_model {
     bool chain = true;               // bf16: consecutive GEMMs of a layer share one launch
     int attn_phase = -1;             // bf16: attention as the first phase of each layer's chain:
                                      // 1 always, 0 never, -1 for calls of two or more sequences
+    int l2_ahead = 0;                // bf16 chains: weight units prefetched into L2 at phase starts
+    int test_stall_cta = -1;         // failure injection for tests (spec_test_stall_next_chain)
+    unsigned long long test_wait_ns = 0;
+    bool attn_ring = false;          // bf16: attention outside a chain runs as its own one-phase
+                                     // ring launch (TMA-fed) rather than the register-tile kernel
 
     // tracing: kernel launches issued, and (when enabled) CUDA events around
     // every GEMM / attention launch with the launch's algorithmic bytes
@@ -320,6 +325,8 @@ int launch_gemm_chain(spec_model* m, const GemmStep* steps, int n, cudaStream_t 
 // Attention phase usable for this launch (bf16, cache maps, <= 16 queries per
 // sequence and KV head, workspace large enough)?
 bool attn_phase_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq);
+// The same attention as a launch of its own (a chain of one attention phase)?
+bool attn_ring_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq);
 size_t attn_phase_part_floats(const spec_model* m);
 bool make_kv_tmaps(spec_kv* kv);
 size_t gemm_partial_floats_needed(const spec_model* m, int N, int K, int T_pad);

@@ -29,6 +29,7 @@ EXPORTS = [
     "spec_verify_noalloc", "spec_draft_sample", "spec_probs", "spec_sample", "spec_schedule_aimd",
     "spec_schedule_decay", "spec_draft_tree", "spec_kv_create_paged", "spec_kv_free_pages", "spec_kv_page_table",
     "spec_draft_tree_dynamic", "spec_verify_trees", "spec_set_exit_layer", "spec_kv_read_page",
+    "spec_test_stall_next_chain",
 ]
 
 
@@ -93,6 +94,7 @@ def load(path: str = LIB_PATH):
         "spec_kv_free_pages": ([P, POINTER(I), P], I),
         "spec_kv_page_table": ([P, POINTER(I), P], I),
         "spec_kv_read_page": ([P, I, I, I, P, P], I),
+        "spec_test_stall_next_chain": ([P, I, ctypes.c_int64], I),
         "spec_accept_greedy": ([P, P, POINTER(I), I, I, I, P, P, P, P], I),
         "kv_commit": ([P, I, P, P, I, P], I),
         "spec_row_probs": ([P, I, P, P], I),
@@ -167,6 +169,11 @@ class Model:
         _check(lib.spec_model_create(ctypes.byref(cfg), arr, _stream(stream), ctypes.byref(h)))
         self.handle = h
         self.n_layers = cfg.n_layers
+
+    def test_stall_next_chain(self, cta, wait_ns):
+        """Failure injection (tests): the next multi-phase GEMM chain launch has CTA
+        ``cta`` withhold its first grid-barrier arrival and gives up after ``wait_ns``."""
+        _check(load().spec_test_stall_next_chain(self.handle, cta, int(wait_ns)))
 
     def set_exit_layer(self, exit_layer):
         """Exit layer of the calls that follow (between rounds only)."""

@@ -189,26 +189,35 @@ def _softmax64(z):
     return e / e.sum(axis=-1, keepdims=True)
 
 
-def make_accept_inputs(batch, k, vocab, seed, sigma=3.0, noise=1.0):
+def make_accept_inputs(batch, k, vocab, seed, sigma=3.0, noise=1.0, first=0):
     """Inputs of the stand-alone acceptance call.
 
     Target logits are i.i.d. N(0, sigma^2) at k+1 positions; draft logits are
     the first k target rows plus N(0, noise^2).  ``p`` and ``q`` are their
     softmax at temperature 1, formed in float64 and rounded to float32 once.
     Draft tokens ``x[b, j]`` are drawn from ``q[b, j]`` (float64 CDF,
-    independent stream); ``u[b, :]`` holds k+1 uniforms from :func:`make_uniforms`.
+    independent stream); ``u[b, :]`` holds k+1 uniforms (integer multiples of
+    2^-24).  Every sequence has streams of its own, keyed by its index in the
+    whole batch, ``first + b``: the sequences ``first .. first + batch - 1`` are
+    the same whether they are drawn alone or as part of a larger batch (so a
+    batch split over several processes reproduces the undivided one).
     """
-    rng = _rng(seed, "accept.logits")
-    zp = rng.standard_normal((batch, k + 1, vocab)) * sigma
-    zq = zp[:, :k, :] + rng.standard_normal((batch, k, vocab)) * noise
-    p = _softmax64(zp).astype(np.float32)
-    q = _softmax64(zq)
-    draw = _rng(seed, "accept.draft").random((batch, k))
-    cdf = np.cumsum(q, axis=-1)
+    p = np.empty((batch, k + 1, vocab), dtype=np.float32)
+    q = np.empty((batch, k, vocab), dtype=np.float32)
     x = np.empty((batch, k), dtype=np.int32)
+    u = np.empty((batch, k + 1), dtype=np.float32)
     for b in range(batch):
+        g = first + b
+        rng = _rng(seed, f"accept.logits.{g}")
+        zp = rng.standard_normal((k + 1, vocab)) * sigma
+        zq = zp[:k, :] + rng.standard_normal((k, vocab)) * noise
+        p[b] = _softmax64(zp).astype(np.float32)
+        qb = _softmax64(zq)
+        q[b] = qb.astype(np.float32)
+        draw = _rng(seed, f"accept.draft.{g}").random(k)
+        cdf = np.cumsum(qb, axis=-1)
         for j in range(k):
-            x[b, j] = min(int(np.searchsorted(cdf[b, j], draw[b, j] * cdf[b, j, -1], side="right")),
-                          vocab - 1)
-    u = make_uniforms((batch, k + 1), seed, "accept.u")
-    return p, q.astype(np.float32), x, u
+            x[b, j] = min(int(np.searchsorted(cdf[j], draw[j] * cdf[j, -1], side="right")), vocab - 1)
+        m = _rng(seed, f"accept.u.{g}").integers(0, 1 << 24, size=k + 1, dtype=np.int64)
+        u[b] = (m.astype(np.float64) * 2.0 ** -24).astype(np.float32)
+    return p, q, x, u

@@ -15,13 +15,27 @@ def lib():
     return spec.load()
 
 
+def to_cuda(w):
+    """The weight dict of ``make_weights`` moved to the GPU."""
+    return {"embed": w["embed"].cuda(), "lm_head": w["lm_head"].cuda(), "final_norm": w["final_norm"].cuda(),
+            "layers": [{k: v.cuda() for k, v in lw.items()} for lw in w["layers"]]}
+
+
 def model_pair(shape, seed, n_layers=None, max_rows=64, max_batch=8, max_position=4096, device="cuda"):
-    """(library Model, oracle Decoder, shape) over the same seeded weights."""
+    """(library Model, oracle Decoder, shape) over the same seeded weights.
+
+    ``device`` is where the weights are drawn: the CPU and the GPU generators
+    give different values for one seed, so a test whose seed was chosen by
+    running the oracle on the CPU (to keep its top-1/top-2 gaps away from
+    near-ties) draws them with ``device="cpu"``; they are then copied to the GPU.
+    """
     from speculative_decoding_verify_04_gb300 import spec
     from oracle.decoder import Decoder
     if n_layers is not None:
         shape = dataclasses.replace(shape, n_layers=n_layers)
     w = make_weights(shape, seed, device=device)
+    if device != "cuda":
+        w = to_cuda(w)
     wn = weights_to_numpy(w)
     model = spec.Model(shape, w, max_rows=max_rows, max_batch=max_batch, max_position=max_position)
     del w

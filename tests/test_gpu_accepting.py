@@ -14,47 +14,54 @@ model, so two constructed models exercise acceptance:
   draft's, every draft token is the target's choice and every round keeps all
   k (on the GPU bit for bit: the draft's and the verifier's LM head read the
   same residual rows);
-* partial-accept: the same two projections are scaled by 0.1, so the full
-  model stays close to the draft and rounds keep anything from 0 to k.
+* partial-accept: the same two projections are scaled down (by 0.1 in the
+  f32 model, by 0.2 in the bf16 one), so the full model stays close to the
+  draft and rounds keep anything from 0 to k.
 
 Each round runs spec_draft -> spec_verify (greedy acceptance fused into the
 LM head) -> kv_commit and is compared with the oracle: draft tokens, draft
 and target logits, accepted count, next token, committed lengths, and at the
-end every committed K/V row of every layer.  The seeds are chosen so that the
-oracle's top-1/top-2 logit gap stays above 1e-3 (f32) or 2.5e-2 (bf16) at
-every compared position, so no comparison is excused by a near-tie and every
-round is compared.
+end every committed K/V row of every layer.  The bf16 model has the 7B layer
+shape (d 4096, 32 heads x 128, FFN 11008) with a 512-token vocabulary, so its
+logits have the benchmark's scale and the 2e-2 tolerance applies as stated.
+Its rounds start from a seeded committed context of 64 slots given to both
+sides (as the 7B-shaped tests do).  Weights are drawn on the CPU, and the
+seeds are chosen so that the oracle's top-1/top-2 logit gap stays at or above
+3e-2 at every compared position (1e-3 for the f32 model, whose logits are
+exact to ~1e-6): no comparison is excused by a near-tie, so every round is
+compared.
 """
 import numpy as np
 import pytest
 import torch
 
-from _gpu_util import cuda_i32, lib
+from _gpu_util import cuda_i32, lib, to_cuda
 from oracle import spec as OS
 from oracle.accept import accept_greedy_chain, argmax_lowest, commit_chain
 from oracle.decoder import Decoder
-from synthetic import ModelShape, make_tokens, make_weights, weights_to_numpy
+from synthetic import ModelShape, make_kv_context, make_tokens, make_weights, weights_to_numpy
 
 pytestmark = pytest.mark.gpu
 
-K, PROMPT = 4, 16
+K, PROMPT, CTX = 4, 16, 64      # f32 models: a prefilled prompt; bf16: a synthetic context of CTX slots
 F32 = ModelShape(2, 256, 4, 4, 64, 1024, 1024, 1, "f32")
-BF16 = ModelShape(3, 256, 4, 2, 64, 512, 512, 1, "bf16", init_std=0.2)
+BF16 = ModelShape(3, 4096, 32, 32, 128, 11008, 512, 1, "bf16")
 # name: (shape, seed, scale of the upper layers' O and down projections, rounds, logit tolerance)
 CASES = {
     "f32_all": (F32, 2, 0.0, 10, 2e-3),
     "f32_partial": (F32, 1, 0.1, 10, 2e-3),
-    "bf16_all": (BF16, 1, 0.0, 8, 2e-2),
-    "bf16_partial": (BF16, 8, 0.1, 8, 2e-2),
+    "bf16_all": (BF16, 4, 0.0, 6, 2e-2),
+    "bf16_partial": (BF16, 4, 0.2, 6, 2e-2),
 }
 
 
 def _weights(shape, seed, scale):
-    w = make_weights(shape, seed, device="cuda")
+    # drawn on the CPU (the seeds were chosen by running the oracle on these values)
+    w = make_weights(shape, seed, device="cpu")
     for layer in w["layers"][shape.exit_layer:]:
         for name in ("wo", "w_down"):
             layer[name] = (layer[name].float() * scale).to(layer[name].dtype)
-    return w
+    return to_cuda(w)
 
 
 @pytest.mark.parametrize("case", list(CASES))
@@ -64,16 +71,26 @@ def test_accepting_rounds_match_the_oracle(case):
     shape, seed, scale, rounds, tol = CASES[case]
     w = _weights(shape, seed, scale)
     dec = Decoder(shape, weights_to_numpy(w))
-    cap = PROMPT + rounds * (K + 1) + K + 8
+    cap = max(PROMPT, CTX) + rounds * (K + 1) + K + 8
     model = spec.Model(shape, w, max_rows=64, max_batch=1, max_position=cap + 8)
     del w
     kv = spec.KVCache(model, 1, cap)
-    prompt = make_tokens(PROMPT, shape.vocab, seed=seed)
-    t0 = torch.empty(1, dtype=torch.int32, device="cuda")
-    spec.spec_prefill(model, kv, 0, cuda_i32(prompt), next_tok=t0)
     cache = dec.new_cache(cap)
-    t_ref = argmax_lowest(dec.prefill(cache, prompt))
-    assert int(t0.item()) == t_ref
+    if shape.dtype == "bf16":
+        # a seeded committed context given to both sides (bf16 values, exact in both), as in
+        # the 7B-shaped tests: only the rounds' own rows carry the cache's bf16 rounding
+        kc, vc = make_kv_context(shape, 1, CTX, seed * 100, device="cpu")
+        kv.import_rows(0, 0, kc[:, 0].contiguous().cuda(), vc[:, 0].contiguous().cuda())
+        kv.set_lengths([CTX])
+        cache.load(kc[:, 0].float().numpy(), vc[:, 0].float().numpy())
+        t_ref = int(make_tokens(1, shape.vocab, seed, "t0")[0])
+        t0 = cuda_i32([t_ref])
+    else:
+        prompt = make_tokens(PROMPT, shape.vocab, seed=seed)
+        t0 = torch.empty(1, dtype=torch.int32, device="cuda")
+        spec.spec_prefill(model, kv, 0, cuda_i32(prompt), next_tok=t0)
+        t_ref = argmax_lowest(dec.prefill(cache, prompt))
+        assert int(t0.item()) == t_ref
 
     cand = torch.empty((1, K + 1), dtype=torch.int32, device="cuda")
     hL = torch.empty((1, K + 1, shape.d_model), dtype=torch.float32, device="cuda")
@@ -109,9 +126,14 @@ def test_accepting_rounds_match_the_oracle(case):
         t0 = nxt.clone()
     if scale > 0.0:
         assert sum(kept) > 0 and any(0 < a < K for a in kept), kept
+    # committed K/V rows: bf16 storage rounds an element to 2^-9 of its own size and
+    # the rotation mixes pairs of elements, so the bound scales with the row's largest
+    # element (2e-2 plus 1e-2 of it), not with the element itself
     n = cache.length
     kk, vv = kv.export_rows(0, 0, shape.n_layers, 0, n)
     for layer in range(shape.n_layers):
-        np.testing.assert_allclose(kk[layer].float().cpu().numpy(), cache.k[layer][:n], atol=tol, rtol=1e-2)
-        np.testing.assert_allclose(vv[layer].float().cpu().numpy(), cache.v[layer][:n], atol=tol, rtol=1e-2)
+        for got, ref in ((kk[layer], cache.k[layer][:n]), (vv[layer], cache.v[layer][:n])):
+            g = got.float().cpu().numpy()
+            bound = tol + 1e-2 * np.abs(ref).max(axis=-1, keepdims=True)
+            assert (np.abs(g - ref) <= bound).all(), (layer, float(np.abs(g - ref).max()))
     assert model.device_error() == 0
