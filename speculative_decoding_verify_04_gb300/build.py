@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libspec.so")
-SOURCES = ["capi.cu", "gemm.cu", "attention.cu", "accept.cu", "sample.cu", "noalloc.cu"]
+SOURCES = ["capi.cu", "gemm.cu", "attention.cu", "attn_ring.cu", "accept.cu", "sample.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

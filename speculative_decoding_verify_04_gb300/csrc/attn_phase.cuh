@@ -519,6 +519,25 @@ SPEC_DEV void attn_unit_q1_early(const uint8_t* tile, uint64_t* release, const f
     }
 }
 
+// Wait for ring position `pos` (slot pos % n, k = pos / n-th use of the slot) to
+// be full.  The warps take the positions in turn, so a warp may reach a slot
+// before the slot's previous position -- another warp's -- has landed; a parity
+// wait on the full barrier alone would then see that earlier phase and return
+// at once.  So the warp first waits for the previous position's release (the
+// empty barrier's phase k - 1): only this warp can release position pos, so the
+// empty barrier is either in phase k - 1 or k and its parity decides.  After
+// that release the full barrier is in phase k or k + 1, and the parity of phase
+// k decides too.  Bounded; the result is the same on every lane.
+SPEC_DEV bool ring_wait_full(uint64_t* full, uint64_t* empty, long long pos, int n, volatile int* abort_flag,
+                             int* err) {
+    const int slot = (int)(pos % n);
+    const uint32_t par = (uint32_t)((pos / n) & 1);
+    bool ok = true;
+    if (pos >= n) ok = mbar_wait(empty + slot, par ^ 1u, abort_flag, err);
+    if (ok) ok = mbar_wait(full + slot, par, abort_flag, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Running (max, sum) of the segment per query from the four warps' (fixed order).
 
 SPEC_DEV void attn_merge_ml(AttnSmem& S, int t) {
@@ -557,9 +576,8 @@ SPEC_DEV void attn_segment_simt(const AttnPhase& A, AttnSmem& S, const AttnRing&
     const float* qs = reinterpret_cast<const float*>(S.q);     // [kAttnSimtQ][128] query rows (f32)
     const long long u0 = su + ((warp - (int)((su - ub) & 3)) & 3);
     int slot = (int)((ring + (u0 - ub)) % R.n);                  // stepped by 4 below
-    uint32_t par = (uint32_t)(((ring + (u0 - ub)) / R.n) & 1);
     for (long long u = u0; u < seg_end; u += 4) {
-        const bool w_ok = __all_sync(0xffffffffu, mbar_wait(R.full + slot, par, abort_flag, err));
+        const bool w_ok = ring_wait_full(R.full, R.empty, ring + (u - ub), R.n, abort_flag, err);
         if (!w_ok) break;
         const int key0 = (int)(u - seg_first) * KU;
         kv_bytes += (unsigned long long)(min(key0 + KU, n_keys) - key0) * HD * 4;
@@ -571,7 +589,7 @@ SPEC_DEV void attn_segment_simt(const AttnPhase& A, AttnSmem& S, const AttnRing&
             __syncwarp();
             if (lane == 0) mbar_arrive(R.empty + slot);
         }
-        for (slot += 4; slot >= R.n; slot -= R.n) par ^= 1u;
+        for (slot += 4; slot >= R.n; slot -= R.n) {}
     }
     if (lane == 0) {
 #pragma unroll
@@ -674,16 +692,15 @@ SPEC_DEV bool consume_attn(const AttnPhase& A, AttnSmem& S, const AttnRing& R, i
             // this warp's units: those whose index in the CTA's range is warp (mod 4)
             const long long u0 = su + ((warp - (int)((su - ub) & 3)) & 3);
             int slot = (int)((ring + (u0 - ub)) % R.n);              // stepped by 4 below
-            uint32_t par = (uint32_t)(((ring + (u0 - ub)) / R.n) & 1);
-            for (long long u = u0; u < seg_end; u += 4) {
-                const bool w_ok = __all_sync(0xffffffffu, mbar_wait(R.full + slot, par, abort_flag, err));
+                    for (long long u = u0; u < seg_end; u += 4) {
+                const bool w_ok = ring_wait_full(R.full, R.empty, ring + (u - ub), R.n, abort_flag, err);
                 if (!w_ok) break;
                 const int key0 = (int)(u - seg_first) * KU;
                 attn_unit_mma<HD>(R.slot(slot), S.q, key0, base, n_keys, mk0, mk1, o, m_r, l_r, lane);
                 kv_bytes += (unsigned long long)(min(key0 + KU, n_keys) - key0) * HD * 4;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(R.empty + slot);
-                for (slot += 4; slot >= R.n; slot -= R.n) par ^= 1u;
+                for (slot += 4; slot >= R.n; slot -= R.n) {}
             }
             // merge the four warps' states (fixed order)
             if (cq == 0) {

@@ -68,6 +68,25 @@ __global__ void to_f32_kernel(const T* __restrict__ src, float* __restrict__ dst
     if (i < n) dst[i] = to_f32<T>(src[i]);
 }
 
+// Tile-major copy of a bf16 GEMM weight [N][K] (N a multiple of 128, K of 64).
+// Block (tile, k-block) -- 128 rows x 64 columns -- becomes 16 contiguous KB in
+// the order the tensor-core operand takes in shared memory: row r at r * 128
+// bytes, its 16-byte chunk c at chunk c ^ (r % 8) (the 128-byte swizzle).  One
+// 16 KB bulk copy then fills a ring stage exactly as a swizzled 2-D tensor copy
+// of the row-major matrix does, and a CTA's run of k-blocks is one sequential
+// stream of HBM.  Indices in 16-byte chunks.
+__global__ void tile_weights_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int N, int K) {
+    const int cpr = K / 8;                       // chunks a row
+    const int kbs = K / 64;                      // k-blocks a row
+    const long long n_chunks = (long long)N * cpr;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_chunks;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int n = (int)(i / cpr), cc = (int)(i % cpr);
+        const int tile = n >> 7, r = n & 127, kb = cc >> 3, c = cc & 7;
+        dst[((long long)tile * kbs + kb) * 1024 + r * 8 + (c ^ (r & 7))] = src[i];
+    }
+}
+
 // cos/sin of pos * theta^(-2i/hd), evaluated in float64 and rounded once
 __global__ void rope_table_kernel(float* cs, float* sn, int max_pos, int half, double theta) {
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -509,9 +528,8 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
     // attention as the first phase of the chain that follows it (one launch per layer)
     // (the phase reads one tree for the batch: a tree a sequence takes the separate kernel)
     const bool fused = tree != 2 && T <= kMaxTPad && attn_phase_ok(m, kv, batch, max_rows_per_seq);
-    // otherwise the same phase as a launch of its own: K/V through the TMA ring, the
-    // committed slots streamed before the wait for the previous kernel
-    const bool ring = !fused && tree != 2 && T <= kMaxTPad && attn_ring_ok(m, kv, batch, max_rows_per_seq);
+    // otherwise, for a few query vectors per (sequence, KV head), the TMA-ring kernel
+    const bool ring = !fused && tree != 2 && m->attn_ring && attn_ring_fits(m, kv, batch, max_rows_per_seq);
     GemmStep pend[5];
     int np = 0;
     for (int l = lo; l < hi; ++l) {
@@ -526,7 +544,7 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             SPEC_TRY(launch_gemm_chain(m, pend, np, st));
             np = 0;
         }
-        if (fused || ring) {   // attention phase (of the chain that follows, or alone)
+        if (fused) {   // attention phase of the chain that follows
             GemmStep at{};
             at.kind = PH_ATTN;
             at.g.tmW = &kv->tm_k;
@@ -546,8 +564,7 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             at.at.linear = max_rows_per_seq * (c.n_heads / c.n_kv_heads) <= kAttnSimtQ;
             at.at.kc = kv->k;
             at.at.vc = kv->v;
-            if (fused) pend[np++] = at;
-            else SPEC_TRY(launch_gemm_chain(m, &at, 1, st));
+            pend[np++] = at;
         } else {   // attention
             AttnParams a{};
             a.q = m->q;
@@ -565,7 +582,8 @@ static int run_layers(spec_model* m, spec_kv* kv, int T, int batch, int max_rows
             a.tree = tree;
             a.kvp = kv->pages();
             a.err = m->err;
-            SPEC_TRY(launch_attention(m, a, max_rows_per_seq, st));
+            if (ring) SPEC_TRY(launch_attention_ring(m, kv, a, st));
+            else SPEC_TRY(launch_attention(m, a, max_rows_per_seq, st));
         }
         {   // O projection + residual
             EpiParams o = e;
@@ -707,13 +725,11 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
         // of two or more sequences (measured faster there; the separate kernel is faster for one)
         const char* ae = getenv("SPEC_ATTN_PHASE");
         m->attn_phase = (ae && ae[0] == '1') ? 1 : ((ae && ae[0] == '0') ? 0 : -1);
-        // SPEC_L2_AHEAD=n: GEMM weight units a chain CTA prefetches into L2 at each phase start
-        const char* le = getenv("SPEC_L2_AHEAD");
-        if (le) m->l2_ahead = std::max(0, std::min(256, atoi(le)));
-        // SPEC_ATTN_RING=1: attention outside a chain runs as a one-phase ring launch
-        // (measured slower than the register-tile kernel at batch 1, so off by default)
+        // SPEC_ATTN_RING=1 (one CTA an SM) or 2 (two): attention outside a chain with few query
+        // vectors takes the TMA-ring kernel; otherwise the register-tile kernel
         const char* re = getenv("SPEC_ATTN_RING");
-        m->attn_ring = re && re[0] == '1';
+        m->attn_ring = re && (re[0] == '1' || re[0] == '2');
+        m->attn_ring_pairs = (re && re[0] == '2') ? 1 : 0;
     }
     m->elem = m->bf16 ? 2 : 4;
     if (m->bf16) {
@@ -856,6 +872,42 @@ extern "C" int spec_model_create(const spec_model_config* cfg, const void* const
     m->plan.tree_parent = pl; pl += (size_t)c.max_batch * kMaxSeqRows;
     m->plan.tree_depth = pl; pl += (size_t)c.max_batch * kMaxSeqRows;
     // tree_stage(m) follows: kTreeStage ints a sequence
+
+    // ---- tile-major GEMM weights (bf16 path; SPEC_TILED_W=0 keeps them row-major)
+    if (m->bf16) {
+        const char* te = getenv("SPEC_TILED_W");
+        struct Mat { void* w; int N, K; };
+        std::vector<Mat> mats;
+        for (int l = 0; l < c.n_layers; ++l) {
+            LayerWeights& L = m->layers[l];
+            mats.push_back({L.qkv, m->qkv_n, d});
+            mats.push_back({L.o, d, qdim});
+            mats.push_back({L.gu, m->gu_n, d});
+            mats.push_back({L.down, d, F});
+        }
+        mats.push_back({m->head, V, d});
+        bool fits = !(te && te[0] == '0');
+        size_t most = 0;
+        for (const Mat& x : mats) {
+            fits &= x.N % kTileN == 0 && x.K % kTileK == 0;
+            most = std::max(most, (size_t)x.N * x.K * 2);
+        }
+        if (fits) {
+            void* tmp = nullptr;
+            if ((rc = check_cuda(cudaMalloc(&tmp, most), "cudaMalloc(weight tiling)"))) return fail(rc);
+            for (const Mat& x : mats) {
+                const size_t bytes = (size_t)x.N * x.K * 2;
+                tile_weights_kernel<<<4 * m->num_sms, 256, 0, st>>>((const uint4*)x.w, (uint4*)tmp, x.N, x.K);
+                rc = check_cuda(cudaGetLastError(), "weight tiling");
+                if (!rc) rc = check_cuda(cudaMemcpyAsync(x.w, tmp, bytes, cudaMemcpyDeviceToDevice, st), "weight tiling copy");
+                if (rc) { cudaFree(tmp); return fail(rc); }
+            }
+            rc = check_cuda(cudaStreamSynchronize(st), "weight tiling sync");
+            cudaFree(tmp);
+            if (rc) return fail(rc);
+            m->w_tiled = true;
+        }
+    }
 
     // ---- tensor maps (bf16 path)
     if (m->bf16) {

@@ -145,11 +145,6 @@ SPEC_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* ba
         :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
-// Prefetch of one tensor-map box into L2 (no shared memory, no completion).
-SPEC_DEV void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
-}
 SPEC_DEV uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -128,10 +128,6 @@ bool attn_phase_ok(const spec_model* m, const spec_kv* kv, int batch, int max_ro
     return wanted && attn_phase_fits(m, kv, batch, max_rows_per_seq);
 }
 
-bool attn_ring_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq) {
-    return m->attn_ring && attn_phase_fits(m, kv, batch, max_rows_per_seq);
-}
-
 // ---------------------------------------------------------------------------
 // split bookkeeping shared by host and device
 struct Split {
@@ -500,6 +496,7 @@ constexpr int kMaxStages = 8;
 struct GemmPhase {
     CUtensorMap tmW;
     CUtensorMap tmX;
+    const uint8_t* wt;  // tile-major weights (16 KB per (tile, k-block)), or null: 2-D tensor copies via tmW
     Split sp;
     EpiParams e;
     AttnPhase at;
@@ -513,7 +510,6 @@ struct GemmChain {
     int* bar;      // per launch: CTAs that finished a phase, summed over phases
     int* done;     // CTAs that finished the chain; the last one resets both counters
     unsigned long long wait_ns;   // limit of the grid-barrier waits
-    int l2_ahead;  // weight units of a GEMM phase, past the ring's first fill, prefetched into L2 early
     int stall_cta; // failure injection (tests): this CTA withholds its arrival after phase 0; -1 none
 };
 
@@ -634,21 +630,6 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                 fence_proxy_async_global();     // the rows were written by other CTAs' epilogues
                 return true;
             };
-            // L2 prefetch of phase q's weight units [stages, stages + l2_ahead) of this CTA's
-            // range: issued when the producer has nothing else to issue (before the previous
-            // kernel completes, and when the previous phase's last unit is out), so HBM keeps
-            // streaming through the phase boundary; the ring's later loads of them hit L2
-            auto prefetch_phase = [&](int q) {
-                if (q >= ch.n || ch.ph[q].kind != PH_GEMM || ch.l2_ahead <= 0) return;
-                const Split& sq = ch.ph[q].sp;
-                long long qb, qe;
-                cta_units(sq, c, qb, qe);
-                qb += L.stages;
-                qe = min(qe, qb + ch.l2_ahead);
-                for (long long u = qb; u < qe; ++u)
-                    tma_prefetch_l2_2d(&ch.ph[q].tmW, (int)(u % sq.kb) * kTileK, (int)(u / sq.kb) * kTileN);
-            };
-            prefetch_phase(0);
             for (int p = 0; ok && p < ch.n; ++p) {
                 P = &ch.ph[p];
                 n_def = 0;
@@ -725,7 +706,6 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                         ++a_issued;
                         if (++a_slot == R.n) { a_slot = 0; a_phase ^= 1u; }
                     }
-                    prefetch_phase(p + 1);
                     // wait for the dependency even without a dependent unit: the grid
                     // barrier of the next phase is only meaningful once the previous
                     // kernel (which resets it) has completed
@@ -751,8 +731,12 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                     }
                     if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, err)) { ok = false; break; }
                     mbar_arrive_expect_tx(full + stage, kATileBytes + L.b_bytes);
-                    tma_load_2d(sA + (size_t)stage * kATileBytes, &P->tmW, kbi * kTileK, tile * kTileN, full + stage,
-                                pw);
+                    if (P->wt)
+                        bulk_load(sA + (size_t)stage * kATileBytes,
+                                  P->wt + ((size_t)tile * sp.kb + kbi) * kATileBytes, kATileBytes, full + stage, pw);
+                    else
+                        tma_load_2d(sA + (size_t)stage * kATileBytes, &P->tmW, kbi * kTileK, tile * kTileN,
+                                    full + stage, pw);
                     if (dep) {
                         load_x(*P, stage, kbi);
                     } else {
@@ -763,9 +747,7 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
                     ++issued;
                     if (++stage == L.stages) { stage = 0; phase ^= 1u; }
                     if (++kbi == sp.kb) { kbi = 0; ++tile; }
-                    if (i == n_units - 1) prefetch_phase(p + 1);
                 }
-                if (n_units == 0) prefetch_phase(p + 1);
                 if (ok && !dep) {
                     if (!dep_wait(p)) { ok = false; }
                     else {
@@ -1088,6 +1070,7 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
             continue;
         }
         P.tmW = *steps[p].g.tmW;
+        P.wt = m->w_tiled ? static_cast<const uint8_t*>(steps[p].g.W) : nullptr;
         P.tmX = m->tm_x[steps[p].xbuf][T_pad / 16 - 1];
         P.sp = make_split(m, steps[p].g.N, steps[p].g.K, T_pad);
         P.sp.part = m->gemm_part;
@@ -1100,7 +1083,6 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
     ch.bar = chain_bar(m);
     ch.done = chain_done(m);
     ch.wait_ns = kWaitLimitNs;
-    ch.l2_ahead = m->l2_ahead;
     ch.stall_cta = -1;
     if (n > 1 && m->test_stall_cta >= 0) {      // one-shot failure injection (tests)
         ch.stall_cta = m->test_stall_cta;
@@ -1110,6 +1092,8 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
     TcLayout L = tc_layout(T_pad, m->max_rows_pad, ch.attn >= 0);
     const size_t smem = tc_smem_bytes(L);
     if (smem > 227 * 1024) return set_error(SPEC_ERR_CAPACITY, "GEMM chain: shared memory layout too large");
+    // the attention phase's four warps take ring positions in turn: the ring must be longer
+    if (ch.attn >= 0 && L.attn_slots <= 4) return set_error(SPEC_ERR_CAPACITY, "GEMM chain: attention ring too short");
     static bool attr_set = false;
     if (!attr_set) {
         cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -1118,7 +1102,6 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
         attr_set = true;
     }
     const int slot = prof_start(m, st);
-    const int kind = (n == 1 && ch.attn == 0) ? PROF_ATTN : PROF_GEMM;    // an attention launch of its own
     if (ch.attn >= 0 && ch.ph[ch.attn].e.kvp.shift >= 0)
         launch_k(m->pdl, gemm_tc_kernel<true, true>, dim3(G), dim3(kTcThreads), smem, st, ch, L);
     else if (ch.attn >= 0)
@@ -1126,7 +1109,7 @@ static int launch_tc_chain(spec_model* m, const GemmStep* steps, int n, cudaStre
     else
         launch_k(m->pdl, gemm_tc_kernel<false>, dim3(G), dim3(kTcThreads), smem, st, ch, L);
     ++m->launches;
-    prof_stop(m, slot, st, kind, kind == PROF_GEMM ? bytes : 0.0);
+    prof_stop(m, slot, st, PROF_GEMM, bytes);
     return check_cuda(cudaGetLastError(), "GEMM launch");
 }
 

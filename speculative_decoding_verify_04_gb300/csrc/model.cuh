@@ -153,15 +153,17 @@ struct spec_model {
     // X tensor maps by buffer (0 x_in, 1 x_attn, 2 x_act) and T_pad/16 - 1
     CUtensorMap tm_x[3][spec::kMaxTPad / 16];
 
+    bool w_tiled = false;            // bf16: GEMM weights stored tile-major (16 KB blocks, pre-swizzled)
     bool pdl = true;                 // launch forward kernels with programmatic dependent launch
     bool chain = true;               // bf16: consecutive GEMMs of a layer share one launch
     int attn_phase = -1;             // bf16: attention as the first phase of each layer's chain:
                                      // 1 always, 0 never, -1 for calls of two or more sequences
-    int l2_ahead = 0;                // bf16 chains: weight units prefetched into L2 at phase starts
     int test_stall_cta = -1;         // failure injection for tests (spec_test_stall_next_chain)
     unsigned long long test_wait_ns = 0;
-    bool attn_ring = false;          // bf16: attention outside a chain runs as its own one-phase
-                                     // ring launch (TMA-fed) rather than the register-tile kernel
+    bool attn_ring = false;          // bf16: attention outside a chain with <= 8 query vectors per
+                                     // (sequence, KV head) takes the TMA-ring kernel (measured slower
+                                     // than the register-tile kernel at batch 1: off unless asked for)
+    int attn_ring_pairs = 0;         // ring kernel shape: 0 one CTA an SM (8 warps), 1 two (4 warps each)
 
     // tracing: kernel launches issued, and (when enabled) CUDA events around
     // every GEMM / attention launch with the launch's algorithmic bytes
@@ -325,8 +327,6 @@ int launch_gemm_chain(spec_model* m, const GemmStep* steps, int n, cudaStream_t 
 // Attention phase usable for this launch (bf16, cache maps, <= 16 queries per
 // sequence and KV head, workspace large enough)?
 bool attn_phase_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq);
-// The same attention as a launch of its own (a chain of one attention phase)?
-bool attn_ring_ok(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq);
 size_t attn_phase_part_floats(const spec_model* m);
 bool make_kv_tmaps(spec_kv* kv);
 size_t gemm_partial_floats_needed(const spec_model* m, int N, int K, int T_pad);
@@ -349,6 +349,10 @@ struct AttnParams {
     int* err;
 };
 int launch_attention(spec_model* m, const AttnParams& a, int max_rows_per_seq, cudaStream_t st);
+// attn_ring.cu: the TMA-ring attention kernel for calls of <= 8 query vectors per
+// (sequence, KV head) (bf16 caches with tensor maps, hd 64 or 128)
+bool attn_ring_fits(const spec_model* m, const spec_kv* kv, int batch, int max_rows_per_seq);
+int launch_attention_ring(spec_model* m, const spec_kv* kv, const AttnParams& a, cudaStream_t st);
 // paged caches (no-ops for contiguous ones): pages for slots below len[b] + n[b]
 // (relative) or n[b] (absolute) of sequences [0, batch); pages past the lengths back
 int kv_ensure_pages(spec_kv* kv, int batch, const int* n, bool relative, cudaStream_t st);

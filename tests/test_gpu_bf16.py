@@ -20,7 +20,7 @@ from _gpu_util import assert_tokens_match, cuda_i32, lib, model_pair, top_gap
 from oracle import accept as A
 from oracle import spec as OS
 from oracle.accept import argmax_lowest
-from synthetic import SHAPES, make_tokens, tree_parents
+from synthetic import SHAPES, ModelShape, make_tokens, tree_parents
 
 pytestmark = pytest.mark.gpu
 
@@ -178,3 +178,44 @@ def test_layer_skip_rounds_7b_layer_shape():
     worst, compared = _layer_skip_rounds(4, 2, [150, 301], k=4, rounds=3, seed=9)
     print(f"max logit error {worst:.3g}")
     assert compared == 3, f"compared {compared} of 3 rounds"
+
+
+@pytest.mark.parametrize("which", ["7b_layers", "tree8_layers"])
+def test_tile_major_weights_are_bit_identical(which, monkeypatch):
+    """The bf16 GEMM weights are stored tile-major (each 128-row x 64-column
+    block as 16 contiguous, pre-swizzled KB, fetched with one bulk copy) unless
+    SPEC_TILED_W=0 keeps them row-major (fetched as 2-D tensor boxes).  Both put
+    the same bytes in shared memory, so a draft and a verification give the
+    same tokens and logits bit for bit: on 3 layers of the 7B layer shape (GEMM
+    chains) and on 3 layers of the d-1024 model (GEMMs launched one by one)."""
+    from speculative_decoding_verify_04_gb300 import spec
+    from synthetic import make_kv_context, make_weights
+    from _gpu_util import to_cuda
+    import dataclasses
+    lib()
+    if which == "7b_layers":
+        shape = ModelShape(3, 4096, 32, 32, 128, 11008, 512, 1, "bf16")
+    else:
+        shape = dataclasses.replace(SHAPES["tree8"], n_layers=3, exit_layer=1)
+    w = make_weights(shape, 11, device="cpu")
+    kc, vc = make_kv_context(shape, 1, 300, 1100, device="cpu")
+    k = 4
+    outs = []
+    for tiled in ("0", "1"):
+        monkeypatch.setenv("SPEC_TILED_W", tiled)
+        model = spec.Model(shape, to_cuda(w), max_rows=64, max_batch=1, max_position=400)
+        kv = spec.KVCache(model, 1, 320)
+        kv.import_rows(0, 0, kc[:, 0].contiguous().cuda(), vc[:, 0].contiguous().cuda())
+        kv.set_lengths([300])
+        cand = torch.empty((1, k + 1), dtype=torch.int32, device="cuda")
+        hL = torch.empty((1, k + 1, shape.d_model), dtype=torch.float32, device="cuda")
+        dlog = torch.empty((1, k, shape.vocab), dtype=torch.float32, device="cuda")
+        logits = torch.empty((k + 1, shape.vocab), dtype=torch.float32, device="cuda")
+        spec.spec_draft(model, kv, cuda_i32([7]), k, cand, hL, dlog)
+        spec.spec_verify(model, kv, [k + 1], cand, k + 1, h_in=hL, h_stride=k + 1, logits=logits)
+        torch.cuda.synchronize()
+        assert model.device_error() == 0
+        outs.append((cand.cpu(), dlog.cpu(), logits.cpu()))
+        del kv, model
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
