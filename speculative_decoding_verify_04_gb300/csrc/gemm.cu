@@ -865,9 +865,11 @@ gemm_tc_kernel(const __grid_constant__ GemmChain ch, TcLayout L) {
             if (ok && ch.n > 1) {
                 // this CTA's share of phase p is written: count it (release)
                 named_bar(1, 128);
+                // the release reduction orders the CTA's writes (they reach thread 0
+                // through the barrier above); the proxy fence lets the next phase's
+                // tensor copies see them
                 if (etid() == 0 && !(c == ch.stall_cta && p == 0)) {
                     fence_proxy_async_global();
-                    __threadfence();
                     red_release_gpu_add(ch.bar, 1);
                 }
             }
