@@ -161,6 +161,8 @@ __host__ __device__ inline void cta_units(const Split& s, int c, long long& ub, 
 struct EpiSmem {
     float tile[kRowChunk][kTileN + 1];
     float rs_all[kMaxTPad];     // RMSNorm row scale of every row of the launch
+    long long row_kv[kRowChunk]; // QKV: cache row of KV head 0 for each row of the chunk, -1 none
+    int row_pos[kRowChunk];     // QKV: rotary position of each row of the chunk, -1 out of range
     int flag;
     int wait_ok;
 };
@@ -183,8 +185,12 @@ SPEC_DEV void load_row_scales(const EpiParams& e, EpiSmem& sm) {
     named_bar(1, 128);
 }
 
+// Q|K|V epilogue of one chunk of rows: rotary embedding on Q and K, Q to its
+// buffer, K and V to the cache.  This form walks the chunk element by element
+// (each row reads its position, rotary values and cache slot as it goes); it
+// is the faster one for chunks of a few rows.
 template <typename KT>
-SPEC_DEV void apply_qkv(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
+SPEC_DEV void apply_qkv_rows(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
     const int hd = e.head_dim, half = hd >> 1;
     const int qd = e.n_heads * hd, kvd = e.n_kv_heads * hd;
     for (int idx = etid(); idx < nr * kTileN; idx += 128) {
@@ -220,6 +226,70 @@ SPEC_DEV void apply_qkv(const EpiParams& e, int tile, int j0, int nr, EpiSmem& s
             const long long row = kv_row(e.kvp, e.n_kv_heads, e.layer, seq, kvh, slot);
             if (row < 0) { dev_error(e.err, SPEC_DEVERR_CAPACITY); continue; }
             static_cast<KT*>(e.vc)[(size_t)row * hd + i] = from_f32<KT>(v);
+        }
+    }
+}
+
+// The same for chunks of more rows: the rows' positions and cache rows are
+// looked up once per chunk, and every rotary value a thread needs is loaded
+// before its first store, so the chunk waits for one round of dependent loads
+// instead of one a row (measured: the 29-row tree verification's QKV epilogue
+// 20 -> 13 us; chunks of up to 8 rows keep the element walk, which measured
+// faster there).
+template <typename KT>
+SPEC_DEV void apply_qkv(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm) {
+    const int hd = e.head_dim, half = hd >> 1;
+    const int qd = e.n_heads * hd, kvd = e.n_kv_heads * hd;
+    if (nr <= 8) { apply_qkv_rows<KT>(e, tile, j0, nr, sm); return; }
+    if (etid() < nr) {
+        const int r = e.r0 + j0 + etid();
+        int pos = e.plan.row_pos[r];
+        if (pos < 0 || pos >= e.max_position) { dev_error(e.err, SPEC_DEVERR_POSITION); pos = -1; }
+        const int seq = e.plan.row_seq[r], slot = e.plan.row_slot[r];
+        long long row = -1;
+        if (slot < 0 || slot >= e.kv_ctx) dev_error(e.err, SPEC_DEVERR_CAPACITY);
+        else if ((row = kv_row(e.kvp, e.n_kv_heads, e.layer, seq, 0, slot)) < 0) dev_error(e.err, SPEC_DEVERR_CAPACITY);
+        sm.row_pos[etid()] = pos;
+        sm.row_kv[etid()] = row;
+    }
+    named_bar(1, 128);
+    const int mm = etid();
+    const int n = tile * kTileN + mm;
+    if (n >= e.N) return;
+    const int i = n & (hd - 1);
+    if (n < qd + kvd) {
+        const int pm = (i < half) ? mm + half : mm - half;
+        const int fi = i & (half - 1);
+        float cs[kRowChunk], sn[kRowChunk];
+#pragma unroll
+        for (int j = 0; j < kRowChunk; ++j) {
+            const int pos = j < nr ? sm.row_pos[j] : -1;
+            cs[j] = pos >= 0 ? __ldg(e.rope_cos + (size_t)pos * half + fi) : 0.f;
+            sn[j] = pos >= 0 ? __ldg(e.rope_sin + (size_t)pos * half + fi) : 0.f;
+        }
+        const int kvh = (n - qd) / hd;       // K features only
+#pragma unroll
+        for (int j = 0; j < kRowChunk; ++j) {
+            if (j >= nr || sm.row_pos[j] < 0) continue;
+            const float v = sm.tile[j][mm] * sm.rs_all[j0 + j];
+            const float pv = sm.tile[j][pm] * sm.rs_all[j0 + j];
+            const float o = (i < half) ? (v * cs[j] - pv * sn[j]) : (v * cs[j] + pv * sn[j]);
+            if (n < qd) {
+                e.q[(size_t)(e.r0 + j0 + j) * qd + n] = o * e.q_scale;
+            } else {
+                const long long row = sm.row_kv[j];
+                if (row >= 0) static_cast<KT*>(e.kc)[(size_t)(row + (long long)kvh * e.kvp.page) * hd + i] = from_f32<KT>(o);
+            }
+        }
+    } else {
+        const int kvh = (n - qd - kvd) / hd;
+#pragma unroll
+        for (int j = 0; j < kRowChunk; ++j) {
+            if (j >= nr) continue;
+            const long long row = sm.row_kv[j];
+            if (row >= 0)
+                static_cast<KT*>(e.vc)[(size_t)(row + (long long)kvh * e.kvp.page) * hd + i] =
+                    from_f32<KT>(sm.tile[j][mm] * sm.rs_all[j0 + j]);
         }
     }
 }
