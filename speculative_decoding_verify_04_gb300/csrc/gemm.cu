@@ -305,18 +305,21 @@ SPEC_DEV void load_resid(const EpiParams& e, int tile, int j0, int nr, float (&h
 
 template <typename XT>
 SPEC_DEV void apply_resid(const EpiParams& e, int tile, int j0, int nr, EpiSmem& sm, const float (&hv)[kRowChunk]) {
+    const int mm = etid();
+    const int n = tile * kTileN + mm;
+    // the feature's gain, read once: loaded inside the row loop it would be
+    // re-read after every store (the compiler cannot rule out aliasing)
+    const float gain = n < e.N ? e.gain_next[n] : 0.f;
 #pragma unroll
     for (int j = 0; j < kRowChunk; ++j) {
         if (j >= nr) break;
-        const int mm = etid();
-        const int n = tile * kTileN + mm;
         float sq = 0.f;
         if (n < e.N) {
             const int r = e.r0 + j0 + j;
             const size_t o = (size_t)r * e.d_model + n;
             const float hn = hv[j] + sm.tile[j][mm];
             e.h[o] = hn;
-            store_act(static_cast<XT*>(e.x_next), o, e.x_next_lo, hn * e.gain_next[n]);
+            store_act(static_cast<XT*>(e.x_next), o, e.x_next_lo, hn * gain);
             sq = hn * hn;
         }
         sm.tile[j][mm] = sq;
