@@ -464,6 +464,19 @@ SPEC_DEV void finish_segment(const EpiParams& e, const Split& sp, int tile, int 
     const int nchunks = (e.T + kRowChunk - 1) / kRowChunk;
     const bool resid = e.kind == EPI_RESID;
     float v[16];
+    if (nc == 1 && nchunks == 1) {
+        // one chunk: read the accumulator out and release it to the next
+        // segment's MMAs before the epilogue runs
+        if (resid && !hv_ready) load_resid(e, tile, 0, e.T, hv);
+        ld.load(0, v);
+        ld.release();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sm.tile[i][mm] = v[i];
+        named_bar(1, 128);
+        apply_chunk<XT>(e, tile, 0, e.T, sm, hv);
+        head_tile_done(e, sp.n_tiles, sm);
+        return;
+    }
     if (nc == 1) {
         for (int ch = 0; ch < nchunks; ++ch) {
             if (resid && (ch > 0 || !hv_ready)) load_resid(e, tile, ch * kRowChunk, min(kRowChunk, e.T - ch * kRowChunk), hv);
