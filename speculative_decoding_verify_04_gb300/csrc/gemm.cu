@@ -358,22 +358,77 @@ SPEC_DEV void apply_head(const EpiParams& e, int tile, int j0, int nr, EpiSmem& 
         sm.tile[j][mm] = l;
     }
     named_bar(1, 128);
+    // The tile's summary of a row: the largest logit with its lowest index, the
+    // largest value besides that element, and sum exp(l - top1).  A warp takes
+    // four rows at once (independent chains), reduces (top1, index, top2) across
+    // its lanes, then sums one exponential a logit.
     const int w = etid() >> 5, lane = etid() & 31;
-    for (int j = w; j < nr; j += 4) {
-        spec_row_stats s = stat_empty();
+    for (int jb = w; jb < nr; jb += 16) {
+        float t1[4], t2[4], x[4][4];
+        int ix[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int mm = lane + 32 * i;
-            const int v = tile * kTileN + mm;
-            const float l = sm.tile[j][mm];
-            if (v < e.vocab) {
-                spec_row_stats one;
-                one.top1 = l; one.top2 = -INFINITY; one.sum_exp = 1.f; one.argmax = v;
-                stat_merge(s, one);
+        for (int q = 0; q < 4; ++q) {
+            const int j = jb + 4 * q;
+            t1[q] = -INFINITY;
+            t2[q] = -INFINITY;
+            ix[q] = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int v = tile * kTileN + lane + 32 * i;
+                const float l = (j < nr && v < e.vocab) ? sm.tile[j][lane + 32 * i] : -INFINITY;
+                x[q][i] = l;
+                if (l > t1[q]) {          // indices rise with i: a tie keeps the lower one
+                    t2[q] = t1[q];
+                    t1[q] = l;
+                    ix[q] = v;
+                } else {
+                    t2[q] = fmaxf(t2[q], l);
+                }
             }
         }
-        s = stat_warp_merge(s);
-        if (lane == 0) e.stat_part[(size_t)tile * e.ss_stride + e.r0 + j0 + j] = s;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float u1 = __shfl_xor_sync(0xffffffffu, t1[q], o);
+                const float u2 = __shfl_xor_sync(0xffffffffu, t2[q], o);
+                const int ui = __shfl_xor_sync(0xffffffffu, ix[q], o);
+                const bool other = u1 > t1[q] || (u1 == t1[q] && ui < ix[q]);
+                t2[q] = fmaxf(fmaxf(t2[q], u2), other ? t1[q] : u1);
+                if (other) {
+                    t1[q] = u1;
+                    ix[q] = ui;
+                }
+            }
+        }
+        float se[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            se[q] = 0.f;
+            if (t1[q] != -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) se[q] += expf(x[q][i] - t1[q]);      // exp(-inf) = 0
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) se[q] += __shfl_xor_sync(0xffffffffu, se[q], o);
+        if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = jb + 4 * q;
+                if (j >= nr) break;
+                spec_row_stats st = stat_empty();
+                if (t1[q] != -INFINITY) {
+                    st.top1 = t1[q];
+                    st.top2 = t2[q];
+                    st.sum_exp = se[q];
+                    st.argmax = ix[q];
+                }
+                e.stat_part[(size_t)tile * e.ss_stride + e.r0 + j0 + j] = st;
+            }
+        }
     }
 }
 
