@@ -669,7 +669,13 @@ SPEC_DEV bool grid_wait(const int* bar, int target, volatile int* abort_flag, in
     if (ld_acquire_gpu(bar) >= target) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (ld_acquire_gpu(bar) >= target) return true;
+        // two pollers a CTA share one counter with every arrival: back off a
+        // little between plain reads, acquire once the count is reached
+        __nanosleep(40);
+        if (*reinterpret_cast<const volatile int*>(bar) >= target) {
+            (void)ld_acquire_gpu(bar);
+            return true;
+        }
         if ((it & 63u) == 0u) {
             if (abort_flag && *abort_flag) return false;
             if (global_timer_ns() - t0 > limit_ns) {
