@@ -311,14 +311,15 @@ struct AcceptArgs {
     int* acc_len; int* next_tok;
 };
 
-// The acceptance streams its one or two rows from memory once: 16 warps each
+// The acceptance streams its one or two rows from memory once: 32 warps each
 // own a contiguous segment, walked in steps of 256 tokens (8 loads a lane in
 // flight); every step's integer weight sum is kept, so the draw finds its
-// segment and step from the sums and re-reads only that step.
-constexpr int kAccThreads = 512;
+// segment and step from the sums and re-reads only that step.  Two such CTAs
+// fit an SM, so a batch of up to twice the SM count runs in one wave.
+constexpr int kAccThreads = 1024;
 constexpr int kAccWarps = kAccThreads / 32;
 constexpr int kAccStep = 256;
-constexpr int kAccMaxSteps = 16;            // vocab <= 16 warps x 16 steps x 256 = 65536
+constexpr int kAccMaxSteps = 8;             // vocab <= 32 warps x 8 steps x 256 = 65536
 constexpr int kAccMaxVocab = kAccWarps * kAccMaxSteps * kAccStep;
 
 struct AccSmem {
@@ -328,7 +329,7 @@ struct AccSmem {
     int a, wf, sf, tok;
 };
 
-__global__ void __launch_bounds__(kAccThreads)
+__global__ void __launch_bounds__(kAccThreads, 2)
 accept_rows_kernel(AcceptArgs a) {
     __shared__ AccSmem sm;
     pdl_wait();
