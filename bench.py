@@ -591,7 +591,7 @@ def run_accept(args, spec, world, rank, local, dist):
     extra = {
         "sequences_per_s": job_rate(world, B * steps, sec),
         "mean_accepted": float(a.mean()),
-        "roofline": {"bound": "hbm", "kernel": "accept_rows_kernel (one CTA of 768 threads a sequence)",
+        "roofline": {"bound": "hbm", "kernel": "accept_rows_kernel (one CTA of 1024 threads a sequence, two an SM)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
                      "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg,
                      "dense_bytes_per_launch": B * (2 * k + 1) * V * 4},
